@@ -1,0 +1,30 @@
+"""CPU oracle for the fused transformer-layer decode path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The product path (``transformer_layer_gb300``) never imports it, and
+this package imports nothing from the product path.
+
+Everything here is plain numpy in float64 with no intermediate rounding: it
+states what one pre-LN GPT-style layer computes, region by region, as the page
+"DeepSpeed Inference 内核优化深度解析：多 GPU 自适应并行、算子融合推理内核与
+MoQ 量化支持" describes it (§3 "面向 Transformer 块的定制化推理内核", §3.2
+"一个 Transformer 层中的四大融合区域", and §5.2 for the int8 weights).  The
+pages print no formula, so each function names the reading it takes; the
+readings are listed once more in the design doc of the repository.
+
+Modules
+-------
+layer   LayerNorm, linear, GeLU(tanh), softmax, KV-cache decode attention and
+        the whole layer / stack forward.
+quant   MoQ-style symmetric per-group int8 quantisation and dequantisation.
+"""
+from .layer import (layer_norm, linear, gelu_tanh, softmax, decode_attention,
+                    layer_forward, stack_forward, LAYER_PARAM_NAMES)
+from .quant import quantize_int8, dequantize_int8, fp16_scale_from_amax
+
+__all__ = [
+    "layer_norm", "linear", "gelu_tanh", "softmax", "decode_attention",
+    "layer_forward", "stack_forward", "LAYER_PARAM_NAMES",
+    "quantize_int8", "dequantize_int8", "fp16_scale_from_amax",
+]

@@ -1,0 +1,339 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks the oracle against mathematics or a library routine that
+reduces to a special case: exact integer brute force, closed forms, invariants
+and hand-derived values.  They are chosen so that a plausible slip in the
+oracle (dropped term, wrong sign or index, transposed operand, wrong scale,
+off-by-one in the causal mask, wrong QKV block order) fails at least one.
+
+Source page for the layer maths: "DeepSpeed Inference 内核优化深度解析：多 GPU
+自适应并行、算子融合推理内核与 MoQ 量化支持", §3.2 (four fusion regions) and §5.2
+(int8 inference).
+"""
+import math
+import os
+import statistics
+from fractions import Fraction
+
+import numpy as np
+import pytest
+from scipy.special import ndtr, softmax as sp_softmax
+from scipy.stats import zscore
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- GEMV / linear
+def test_linear_exact_integer_brute_force():
+    rng = np.random.default_rng(1)
+    N, K, B = 5, 7, 3   # non-square: a transposed operand cannot pass
+    W = rng.integers(-9, 10, size=(N, K))
+    x = rng.integers(-9, 10, size=(B, K))
+    b = rng.integers(-9, 10, size=(N,))
+    got = oracle.linear(x, W, b)
+    for i in range(B):
+        for n in range(N):
+            want = int(b[n]) + sum(int(x[i, k]) * int(W[n, k]) for k in range(K))
+            assert got[i, n] == want
+
+
+def test_linear_random_against_fsum():
+    rng = np.random.default_rng(2)
+    W = rng.standard_normal((4, 33))
+    x = rng.standard_normal((2, 33))
+    got = oracle.linear(x, W)
+    for i in range(2):
+        for n in range(4):
+            want = math.fsum(float(x[i, k]) * float(W[n, k]) for k in range(33))
+            assert abs(got[i, n] - want) <= 1e-13
+
+
+# ---------------------------------------------------------------- LayerNorm
+def test_layernorm_moments_before_affine():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((4, 257)) * 3.0 + 1.5
+    gamma = 1.0 + 0.1 * rng.standard_normal(257)
+    beta = 0.1 * rng.standard_normal(257)
+    eps = 1e-5
+    y = oracle.layer_norm(x, gamma, beta, eps)
+    z = (y - beta) / gamma
+    for r in range(4):
+        var = statistics.pvariance([float(v) for v in x[r]])   # population variance
+        assert abs(z[r].mean()) < 1e-12
+        assert abs(z[r].var() - var / (var + eps)) < 1e-12
+
+
+def test_layernorm_eps_placement():
+    # Variance equal to eps: the normalised variance must be exactly 1/2.
+    eps = 1e-5
+    x = np.array([[-1.0, 1.0] * 64]) * math.sqrt(eps)
+    y = oracle.layer_norm(x, np.ones(128), np.zeros(128), eps)
+    assert abs(y.var() - 0.5) < 1e-12
+
+
+def test_layernorm_constant_input_gives_beta():
+    beta = np.linspace(-1, 1, 64)
+    y = oracle.layer_norm(np.full((2, 64), 3.25), np.full(64, 7.0), beta)
+    assert np.array_equal(y, np.broadcast_to(beta, (2, 64)))
+
+
+def test_layernorm_reduces_to_zscore():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, 100))
+    y = oracle.layer_norm(x, np.ones(100), np.zeros(100), eps=0.0)
+    np.testing.assert_allclose(y, zscore(x, axis=-1, ddof=0), rtol=0, atol=1e-13)
+
+
+# ---------------------------------------------------------------- GeLU (tanh form)
+def test_gelu_zero_and_odd_part_identity():
+    assert oracle.gelu_tanh(0.0) == 0.0
+    x = np.linspace(-6, 6, 1201)
+    # gelu(x) - gelu(-x) = x because 0.5(1 + tanh u) + 0.5(1 + tanh(-u)) = 1
+    np.testing.assert_allclose(oracle.gelu_tanh(x) - oracle.gelu_tanh(-x), x, atol=1e-14)
+
+
+def test_gelu_close_to_exact_erf_gelu():
+    # The tanh form approximates x * Phi(x); its largest deviation is 4.73e-4
+    # (near x = 2.7).  Dropping the cubic term, squaring instead of cubing or a
+    # wrong sqrt(2/pi) all give deviations above 3e-2.
+    x = np.linspace(-10, 10, 200001)
+    err = np.abs(oracle.gelu_tanh(x) - x * ndtr(x))
+    assert err.max() < 5e-4
+
+
+def test_gelu_slope_and_tails():
+    h = 1e-6
+    assert abs((oracle.gelu_tanh(h) - oracle.gelu_tanh(-h)) / (2 * h) - 0.5) < 1e-9
+    assert abs(oracle.gelu_tanh(10.0) - 10.0) < 1e-12
+    assert abs(oracle.gelu_tanh(-10.0)) < 1e-12
+
+
+# ---------------------------------------------------------------- softmax / attention
+def test_softmax_rows_sum_to_one_and_match_scipy():
+    rng = np.random.default_rng(5)
+    s = rng.standard_normal((5, 37)) * 20
+    p = oracle.softmax(s)
+    np.testing.assert_allclose(p.sum(-1), 1.0, atol=1e-14)
+    np.testing.assert_allclose(p, sp_softmax(s, axis=-1), atol=1e-15)
+
+
+def _rand_cache(rng, B, nh, max_len, d):
+    return rng.standard_normal((B, nh, max_len, d)), rng.standard_normal((B, nh, max_len, d))
+
+
+def test_attention_single_key_returns_v():
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((1, 1, 2, 8))
+    K, V = _rand_cache(rng, 1, 2, 4, 8)
+    o = oracle.decode_attention(q, K, V, past_len=[0])
+    np.testing.assert_allclose(o[0, 0], V[0, :, 0, :], atol=1e-15)
+
+
+def test_attention_equal_keys_or_zero_query_give_mean_v():
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal((1, 1, 2, 8))
+    K, V = _rand_cache(rng, 1, 2, 9, 8)
+    K[:] = K[:, :, :1, :]                       # all keys equal
+    o = oracle.decode_attention(q, K, V, past_len=[6])
+    np.testing.assert_allclose(o[0, 0], V[0, :, :7, :].mean(axis=1), atol=1e-14)
+    K2, _ = _rand_cache(rng, 1, 2, 9, 8)
+    o2 = oracle.decode_attention(np.zeros_like(q), K2, V, past_len=[6])
+    np.testing.assert_allclose(o2[0, 0], V[0, :, :7, :].mean(axis=1), atol=1e-14)
+
+
+def test_attention_two_keys_closed_form_scale():
+    d = 16
+    a = 3.0
+    q = np.zeros((1, 1, 1, d)); q[0, 0, 0, 0] = a
+    K = np.zeros((1, 1, 2, d)); K[0, 0, 0, 0] = 1.0     # score a/sqrt(d) vs 0
+    V = np.zeros((1, 1, 2, d)); V[0, 0, 0, :] = 2.0; V[0, 0, 1, :] = -1.0
+    o = oracle.decode_attention(q, K, V, past_len=[1])
+    p0 = 1.0 / (1.0 + math.exp(-a / math.sqrt(d)))
+    np.testing.assert_allclose(o[0, 0, 0], p0 * 2.0 + (1 - p0) * -1.0, atol=1e-15)
+
+
+def test_attention_causal_mask_hides_later_new_tokens():
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((1, 3, 2, 8))
+    K, V = _rand_cache(rng, 1, 2, 10, 8)
+    past = 4
+    o = oracle.decode_attention(q, K, V, past_len=[past])
+    V2 = V.copy()
+    V2[0, :, past + 2, :] += 100.0               # only the last new token's value
+    o2 = oracle.decode_attention(q, K, V2, past_len=[past])
+    np.testing.assert_array_equal(o[0, :2], o2[0, :2])   # tokens 0, 1 never see it
+    assert np.abs(o[0, 2] - o2[0, 2]).max() > 1e-3
+
+
+# ---------------------------------------------------------------- whole layer
+def _layer(rng, H, F, scale=1.0):
+    p = {
+        "ln1_g": 1 + 0.1 * rng.standard_normal(H), "ln1_b": 0.1 * rng.standard_normal(H),
+        "w_qkv": 0.2 * rng.standard_normal((3 * H, H)), "b_qkv": 0.1 * rng.standard_normal(3 * H),
+        "w_o": 0.2 * rng.standard_normal((H, H)), "b_o": 0.1 * rng.standard_normal(H),
+        "ln2_g": 1 + 0.1 * rng.standard_normal(H), "ln2_b": 0.1 * rng.standard_normal(H),
+        "w_fc1": 0.2 * rng.standard_normal((F, H)), "b_fc1": 0.1 * rng.standard_normal(F),
+        "w_fc2": 0.2 * rng.standard_normal((H, F)), "b_fc2": 0.1 * rng.standard_normal(H),
+    }
+    return {k: v * scale for k, v in p.items()}
+
+
+def test_zero_layer_is_identity():
+    rng = np.random.default_rng(9)
+    H, F, nh = 16, 32, 4
+    p = {k: np.zeros_like(v) for k, v in _layer(rng, H, F).items()}
+    x = rng.standard_normal((2, 1, H))
+    K, V = _rand_cache(rng, 2, nh, 6, H // nh)
+    r = oracle.layer_forward(x, p, K, V, [2, 4], nh)
+    np.testing.assert_array_equal(r["y"], x)
+    assert np.all(K[0, :, 2] == 0) and np.all(V[1, :, 4] == 0)
+
+
+def test_bias_only_layer_places_biases_and_qkv_blocks():
+    rng = np.random.default_rng(10)
+    H, F, nh = 16, 32, 4
+    d = H // nh
+    p = _layer(rng, H, F)
+    for k in ("w_qkv", "w_o", "w_fc1", "w_fc2"):
+        p[k] = np.zeros_like(p[k])
+    x = rng.standard_normal((1, 1, H))
+    K, V = _rand_cache(rng, 1, nh, 5, d)
+    r = oracle.layer_forward(x, p, K, V, [3], nh)
+    np.testing.assert_allclose(r["y"][0, 0], x[0, 0] + p["b_o"] + p["b_fc2"], atol=1e-14)
+    np.testing.assert_array_equal(K[0, :, 3, :], p["b_qkv"][H:2 * H].reshape(nh, d))
+    np.testing.assert_array_equal(V[0, :, 3, :], p["b_qkv"][2 * H:].reshape(nh, d))
+    np.testing.assert_array_equal(r["q"][0, 0], p["b_qkv"][:H].reshape(nh, d))
+
+
+def test_zero_query_attention_averages_values_including_new_token():
+    rng = np.random.default_rng(11)
+    H, F, nh = 16, 32, 2
+    d = H // nh
+    p = _layer(rng, H, F)
+    p["w_qkv"][:H] = 0.0
+    p["b_qkv"][:H] = 0.0                     # q = 0 -> uniform attention
+    x = rng.standard_normal((1, 1, H))
+    K, V = _rand_cache(rng, 1, nh, 6, d)
+    r = oracle.layer_forward(x, p, K, V, [4], nh)
+    want = V[0, :, :5, :].mean(axis=1).reshape(H)   # includes the new value at 4
+    np.testing.assert_allclose(r["attn"][0, 0], want, atol=1e-14)
+
+
+def test_head_permutation_equivariance():
+    rng = np.random.default_rng(12)
+    H, F, nh = 16, 24, 4
+    d = H // nh
+    p = _layer(rng, H, F)
+    x = rng.standard_normal((2, 2, H))
+    K, V = _rand_cache(rng, 2, nh, 7, d)
+    r = oracle.layer_forward(x, p, K.copy(), V.copy(), [3, 1], nh)
+    perm = np.array([2, 0, 3, 1])
+    cols = np.concatenate([np.arange(h * d, (h + 1) * d) for h in perm])
+    p2 = dict(p)
+    rows = np.concatenate([cols, H + cols, 2 * H + cols])
+    p2["w_qkv"] = p["w_qkv"][rows]
+    p2["b_qkv"] = p["b_qkv"][rows]
+    p2["w_o"] = p["w_o"][:, cols]
+    r2 = oracle.layer_forward(x, p2, K[:, perm].copy(), V[:, perm].copy(), [3, 1], nh)
+    np.testing.assert_allclose(r2["y"], r["y"], atol=1e-12)
+
+
+def test_ffn_identity_weights_reduce_to_zscore_and_gelu():
+    rng = np.random.default_rng(13)
+    H, nh = 32, 4
+    p = _layer(rng, H, H)
+    p["w_o"] = np.zeros((H, H)); p["b_o"] = np.zeros(H)
+    p["w_fc1"] = np.eye(H); p["b_fc1"] = np.zeros(H)
+    p["w_fc2"] = np.eye(H); p["b_fc2"] = np.zeros(H)
+    p["ln2_g"] = np.ones(H); p["ln2_b"] = np.zeros(H)
+    x = rng.standard_normal((1, 1, H)) * 2.0
+    K, V = _rand_cache(rng, 1, nh, 4, H // nh)
+    r = oracle.layer_forward(x, p, K, V, [1], nh, eps=0.0)
+    z = zscore(x[0, 0], ddof=0)
+    gelu_erf = z * ndtr(z)
+    np.testing.assert_allclose(r["y"][0, 0], x[0, 0] + gelu_erf, atol=5e-4)
+
+
+# ---------------------------------------------------------------- int8 (MoQ)
+def _fp16_rne_of_fraction(fr):
+    """Round a positive Fraction to the nearest float16, ties to even, exactly."""
+    approx = np.float16(float(fr))
+    cands = set()
+    for v in (approx, np.nextafter(approx, np.float16(0)), np.nextafter(approx, np.float16(np.inf))):
+        if np.isfinite(v):
+            cands.add(np.float16(v))
+    best = None
+    for c in sorted(cands, key=float):
+        err = abs(Fraction(float(c)) - fr)
+        key = (err, int(np.array(c).view(np.uint16)) & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+def test_scale_exhaustive_over_all_fp16_amax():
+    bits = np.arange(1, 0x7C00, dtype=np.uint16)         # every positive finite fp16
+    amax = bits.view(np.float16)
+    got = oracle.fp16_scale_from_amax(amax)
+    for a, s in zip(amax, got):
+        want = _fp16_rne_of_fraction(Fraction(float(a)) / 127)
+        assert s.view(np.uint16) == np.float16(want).view(np.uint16), (a, s, want)
+
+
+def test_codes_match_exact_rational_rounding():
+    rng = np.random.default_rng(14)
+    w = (rng.standard_normal((64, 256)) * 0.02).astype(np.float16)
+    q, s = oracle.quantize_int8(w, 64)
+    for n in range(0, 64, 7):
+        for k in range(256):
+            sv = Fraction(float(s[n, k // 64]))
+            want = 0 if sv == 0 else round(Fraction(float(w[n, k])) / sv)   # half-even
+            want = max(-127, min(127, want))
+            assert int(q[n, k]) == want
+
+
+def test_int8_invariants():
+    rng = np.random.default_rng(15)
+    w = (rng.standard_normal((32, 128)) * 0.02).astype(np.float16)
+    q, s = oracle.quantize_int8(w, 64)
+    deq = oracle.dequantize_int8(q, s, 64)
+    assert np.abs(q.astype(int)).max() <= 127
+    s64 = np.repeat(s.astype(np.float64), 64, axis=1)
+    assert np.all(np.abs(w.astype(np.float64) - deq) <= s64 / 2 * (1 + 2 ** -10))
+    wg = np.abs(w.astype(np.float64)).reshape(32, 2, 64)
+    qg = np.abs(q.astype(int)).reshape(32, 2, 64)
+    idx = wg.argmax(axis=-1)
+    assert np.all(np.take_along_axis(qg, idx[..., None], -1) == 127)
+
+
+def test_int8_zero_group_and_round_trip():
+    z = np.zeros((2, 64), dtype=np.float16)
+    q, s = oracle.quantize_int8(z, 64)
+    assert np.all(q == 0) and np.all(s == 0)
+    rng = np.random.default_rng(16)
+    codes = rng.integers(-127, 128, size=(8, 128)).astype(np.int8)
+    codes[:, 0] = 127; codes[:, 64] = -127
+    scale = np.float16(2.0 ** -7)
+    w = (codes.astype(np.float64) * float(scale)).astype(np.float16)   # exact in fp16
+    q2, s2 = oracle.quantize_int8(w, 64)
+    np.testing.assert_array_equal(q2, codes)
+    assert np.all(s2 == scale)
+
+
+def test_int8_hand_derived_ties():
+    rows = []
+    with open(os.path.join(GOLDEN, "int8_ties.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                i, w, c = line.split()
+                rows.append((int(i), float(w), int(c)))
+    w = np.zeros((1, 64), dtype=np.float16)
+    for i, v, _ in rows:
+        w[0, i] = v
+    q, s = oracle.quantize_int8(w, 64)
+    assert float(s[0, 0]) == 1.0
+    for i, _, c in rows:
+        assert int(q[0, i]) == c, (i, int(q[0, i]), c)
