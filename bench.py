@@ -1,0 +1,416 @@
+"""Decode-throughput benchmark of the fused layer stack (one JSON line on rank 0).
+
+Workload: the 7B-shaped GPT-style stack (32 pre-LN layers, hidden 4096, 32
+heads, FFN 16384, fp16 weights ~ N(0, 0.02), seeded synthetic), batch 1, a KV
+cache of 512 positions ~ N(0, 1); each step decodes one token through all 32
+layers.  Steps cycle over cache positions 512..575 (64 decode positions),
+resetting the device-side sequence length every 64 steps.
+
+A step is one ds_stack_decode_step (160 kernels, replayed as one CUDA graph).
+`value` = tokens/s over the timed steps with every input already in HBM;
+`e2e` = the same through ds_stack_decode_host (host input copied in, output
+copied back and the stream synchronised every step).  `roofline` is the
+dominant region kernel (FFN) timed alone in profile mode; `step_roofline` is
+the whole step's algorithmic bytes over its time.
+
+--impl reference times the float64 CPU oracle (oracle/) on this machine's host
+cores on the same workload (bounded samples, see `cpu_baseline.sample`).
+
+Multi-GPU (torchrun, N > 1): every rank runs an independent replica (its own
+weights and caches; decode of independent sequences needs no exchange), the
+timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/sec at batch 1 (7B-shaped fp16 stack); % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+CYCLE = 64  # decode positions per pass over the cache
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=4)
+    return ap.parse_args()
+
+
+def workload_config(B, layers):
+    return {
+        "workload": f"7B-shaped GPT-style stack: {layers} pre-LN layers, hidden 4096, 32 heads "
+                    f"(head_dim 128), FFN 16384, GeLU(tanh), fp16 weights; batch {B}; KV cache "
+                    f"512 cached positions + 64 decode positions",
+        "batch": B, "layers": layers, "hidden": 4096, "heads": 32, "ffn": 16384,
+        "past": 512, "decode_positions": CYCLE,
+        "l2": "inputs larger than L2: 12.9 GB of weights streamed per step (L2 is 129 MB)",
+        "parallelism": "replicas",
+    }
+
+
+def load_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+                if k in d and d[k]:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "transformer_layer_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, or None
+    when the kernels changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        if d.get("csrc_hash") != csrc_hash():
+            return None
+        v = d.get("per_launch_dram_bytes", {}).get(kernel_key)
+        return float(v) if v is not None else None
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [ln.strip().split(",") for ln in self.f.read().splitlines() if ln.strip()]
+        self.f.close()
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                for i, n in enumerate(names):
+                    if r[5 + i].strip().lower() == "active":
+                        reasons.add(n)
+            except Exception:
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def layer_bytes(H, F):
+    n_w = 3 * H * H + H * H + F * H + H * F
+    n_small = 3 * H + H + F + H + 4 * H
+    return 2 * n_w + 2 * n_small
+
+
+def step_bytes(H, F, layers, B, past, steps):
+    """Average algorithmic bytes of one decode step over positions past..past+CYCLE-1:
+    weights + biases + LN params, K/V read (S = past + 1 + i keys), K/V write."""
+    kv = 0.0
+    for i in range(steps):
+        S = past + 1 + (i % CYCLE)
+        kv += B * layers * 2 * S * H * 2 + B * layers * 2 * H * 2
+    return layers * layer_bytes(H, F) + kv / steps
+
+
+def region_bytes(H, F, B, past):
+    """Algorithmic bytes of one launch of each region kernel (weights + vectors in/out)."""
+    S = past + 1 + CYCLE // 2
+    return {
+        "ln_qkv": 3 * H * H * 2 + 3 * H * 2 + 4 * H + B * (H * 2 + H * 4 + 2 * H * 2),
+        "attention": B * (2 * S * H * 2 + H * 4 + H * 4),
+        "oproj_res": H * H * 2 + 2 * H + B * (H * 4 + H * 2 + H * 4),
+        "ffn_up": F * H * 2 + 2 * F + 4 * H + B * (H * 4 + F * 4),
+        "ffn_down": H * F * 2 + 2 * H + B * (F * 4 + H * 4 + H * 2),
+    }
+
+
+REGIONS = ("ln_qkv", "attention", "oproj_res", "ffn_up", "ffn_down")
+
+
+def cpu_baseline_sample(B, budget_s=10.0, layers=32):
+    """The oracle, as it stands, on one 7B-shaped layer at a time (float64 numpy);
+    returns (tokens/s for the whole stack, cores, sample description)."""
+    import numpy as np
+    import oracle
+    from transformer_layer_gb300 import inputs
+    H, F, nh, d, past = 4096, 16384, 32, 128, 512
+    p = {k: v.numpy() for k, v in inputs.layer_params(H, F, 1002, 0, device="cpu").items()}
+    kc, vc = inputs.kv_cache(B, nh, past + 1, d, 1002, device="cpu")
+    K0, V0 = kc.numpy(), vc.numpy()
+    x = inputs.hidden(B, 1, H, 1002, device="cpu").numpy()
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < 2 or (time.perf_counter() < t_end and len(times) < 16):
+        K, V = K0.astype(np.float64), V0.astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.layer_forward(x, p, K, V, [past] * B, nh)
+        times.append(time.perf_counter() - t0)
+    per_layer = statistics.median(times)
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"{len(times)} single-layer forwards of the float64 oracle (numpy; BLAS threads "
+              f"over {cores} host cores) on one 7B-shaped layer, batch {B}, 512 cached positions; "
+              f"median {per_layer:.3f} s/layer scaled to {layers} layers per token")
+    return B / (per_layer * layers), cores, sample
+
+
+def run_reference(args):
+    """--impl reference: the float64 CPU oracle on this host's cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from transformer_layer_gb300 import inputs
+    B, layers = args.batch, args.layers
+    H, F, nh, d, past = 4096, 16384, 32, 128, 512
+    p = {k: v.numpy() for k, v in inputs.layer_params(H, F, 1002, 0, device="cpu").items()}
+    kc, vc = inputs.kv_cache(B, nh, past + CYCLE, d, 1002, device="cpu")
+    K0, V0 = kc.numpy(), vc.numpy()
+    xs = [inputs.hidden(B, 1, H, 1002, step=i, device="cpu").numpy() for i in range(4)]
+
+    def one_layer(i):
+        K, V = K0.astype(np.float64), V0.astype(np.float64)
+        t0 = time.perf_counter()
+        oracle.layer_forward(xs[i % 4], p, K, V, [past + (i % CYCLE)] * B, nh)
+        return time.perf_counter() - t0
+
+    for i in range(max(args.warmup, 0)):
+        one_layer(i)
+    ts = [one_layer(i) for i in range(args.steps)]
+    per_layer = sum(ts) / len(ts)
+    value = B / (per_layer * layers)
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"each step = one float64 oracle forward of one 7B-shaped layer (1/{layers} of a "
+              f"decode step), batch {B}, cache {past}+i positions; tokens/s scaled by {layers} layers")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_layer * layers * 1000.0, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": workload_config(B, layers),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from transformer_layer_gb300 import ds, inputs
+
+    B, L = args.batch, args.layers
+    H, nh, F, d, past = 4096, 32, 16384, 128, 512
+    max_len = past + CYCLE
+    seed = 1002 + rank
+    stream = torch.cuda.Stream(device=dev)
+
+    # ---- weights, caches, workspace (all resident in HBM before timing)
+    layers, params, kcs, vcs = [], [], [], []
+    for l in range(L):
+        p = inputs.layer_params(H, F, seed, l, device=dev)
+        params.append(p)
+        layers.append(ds.ds_layer_create(H, nh, F, p, torch.float16, torch.float16))
+        k, v = inputs.kv_cache(B, nh, max_len, d, seed, l, device=dev)
+        kcs.append(k)
+        vcs.append(v)
+    stack = ds.ds_stack_create(layers)
+    nbytes = ds.ds_stack_workspace_bytes(stack, B)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ds.ds_workspace_init(ws, nbytes, stream)
+    seq = torch.full((B,), past, dtype=torch.int32, device=dev)
+    seq0 = seq.clone()
+    n_x = 8
+    xs = [inputs.hidden(B, 1, H, seed, step=i, device=dev).reshape(B, H) for i in range(n_x)]
+    out = torch.empty(B, H, dtype=torch.float16, device=dev)
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        if i % CYCLE == 0:
+            seq.copy_(seq0)
+        ds.ds_stack_decode_step(stack, xs[i % n_x], out, B, kcs, vcs, max_len, seq, ws, nbytes, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+
+    # ---- timed region
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = ds.ds_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    launches = ds.ds_launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = B * args.steps * world / (ms_max / 1000.0)
+
+    # ---- end to end through the host-buffer entry point
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = torch.empty(B, H, dtype=torch.float16).pin_memory()
+    xd, yd = torch.empty_like(xs[0]), torch.empty_like(out)
+    seq.copy_(seq0)
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(8, min(args.steps, 64))
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        if i % CYCLE == 0 and i > 0:
+            seq.copy_(seq0)
+        ds.ds_stack_decode_host(stack, xh[i % n_x], yh, xd, yd, B, kcs, vcs, max_len, seq, ws, nbytes,
+                                stream)
+    e2e_s = time.perf_counter() - t0
+    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+    e2e_value = B * e2e_steps * world / float(te.item())
+
+    # ---- per-region kernel times (profile mode: no graph, no PDL; each kernel alone)
+    ds.ds_stack_set_profiling(stack, True)
+    seq.copy_(seq0)
+    torch.cuda.synchronize(dev)
+    ds.ds_stack_region_times(stack)
+    with torch.cuda.stream(stream):
+        for i in range(args.profile_steps):
+            step(i + 1)   # avoid the seq reset at i % 64 == 0 on the first profiled step
+    us, counts = ds.ds_stack_region_times(stack)
+    ds.ds_stack_set_profiling(stack, False)
+
+    peak, peak_kind = load_peak()
+    rbytes = region_bytes(H, F, B, past)
+    shares = {r: us[i] for i, r in enumerate(REGIONS)}
+    dom = max(("ffn_up", "ffn_down", "ln_qkv", "oproj_res"), key=lambda r: shares[r])
+    dom_us = shares[dom]
+    achieved = rbytes[dom] / (dom_us * 1e-6) / 1e9
+    sbytes = step_bytes(H, F, L, B, past, args.steps)
+    step_gbs = sbytes / (ms_max / args.steps / 1000.0) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = cpu_baseline_sample(B, layers=L)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded: weights N(0,0.02), biases N(0,0.01), LN gamma 1+N(0,0.1), "
+                "beta N(0,0.1), KV cache and inputs N(0,1))",
+        "config": workload_config(B, L),
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} HBM copy",
+                     "bytes_per_launch": rbytes[dom], "us_per_launch": dom_us,
+                     "traffic": ncu_traffic(dom)},
+        "step_roofline": {"bytes_per_step": sbytes, "achieved": step_gbs, "peak": peak, "unit": "GB/s",
+                          "frac": step_gbs / peak, "peak_source": f"{peak_kind} HBM copy"},
+        "region_us": {r: shares[r] for r in REGIONS},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": B * H * 2,
+                "d2h_bytes_per_step": B * H * 2, "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ds.ds_stack_destroy(stack)
+    for l in layers:
+        ds.ds_layer_destroy(l)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+/*
+ * ds_layer.h -- C ABI of libdslayer.so: fused decode steps of a pre-LN
+ * GPT-style transformer layer, or a stack of such layers, on one GB300 GPU.
+ *
+ * Source pages (cited by title and section):
+ *   [P1] "DeepSpeed Inference 内核优化深度解析：多 GPU 自适应并行、算子融合推理内核
+ *        与 MoQ 量化支持" -- §3 intro (vector-matrix / skinny matrix-matrix GEMM
+ *        with ops fused at its reduction boundary), §3.1 (fusion principles),
+ *        §3.2 (the four fusion regions of a layer), §3.3 (shared memory and
+ *        warp-level reductions), §5.2 (int8 inference kernels, quantisation
+ *        groups).
+ *   [P3] "DeepSpeed MoE 大规模稀疏模型推理实战指南：并行切分、PR-MoE 优化与
+ *        init_inference 全解析" -- table "推理配置参数详解" (dtype choices,
+ *        triangular_masking).
+ *
+ * What one layer computes (regions of [P1] §3.2; T new tokens per sequence):
+ *   R1  h1 = LayerNorm1(x);  [q|k|v] = h1 W_qkv^T + b_qkv;  k, v are appended
+ *       to the caller's KV cache at positions past_len[b] .. past_len[b]+T-1.
+ *   R2  o = softmax(q K^T / sqrt(d), causal) V per head, over the cache.
+ *   R3  x1 = x + o W_o^T + b_o, and the statistics of LayerNorm2(x1).
+ *   R4  g = GeLU_tanh(LN2(x1) W_1^T + b_1);  y = x1 + g W_2^T + b_2.
+ * LayerNorm: biased variance, eps from the config (1e-5 by default), affine
+ * after the normalisation.  GeLU: 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3))).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are caller-owned DEVICE memory unless a parameter says HOST.
+ *     The library copies no weights: create() stores the pointers, so the
+ *     caller keeps them alive and unchanged until destroy().
+ *   - Weights are [out][in] row-major (the input axis K is contiguous).
+ *     Fused QKV rows: q block (rows 0..H-1), k block, v block; inside a block
+ *     head i owns rows i*d .. (i+1)*d-1.
+ *   - Hidden states are [B][T][H] (batch rows, new tokens, features) in the
+ *     activation dtype.  The K and V caches of a layer are two separate
+ *     arrays [B][nh][max_len][d] in the activation dtype.
+ *   - Every pointer must be 16-byte aligned; H, F and d must be multiples of
+ *     64; d must be 64 or 128; B*T must be 1..64.
+ *   - Calls are asynchronous on the given stream (never synchronising, except
+ *     ds_stack_region_times, ds_workspace_status and ds_stack_decode_host,
+ *     which say so).  A stream of 0 means the legacy default stream.
+ *   - Errors: arguments are validated before any launch; a bad argument
+ *     returns DS_ERR_INVALID_ARG or DS_ERR_UNSUPPORTED and launches nothing.
+ *     A launch failure returns DS_ERR_CUDA.  Faults that happen later on the
+ *     device surface on a later call.  No C++ exception crosses this ABI.
+ *     ds_last_error() gives a human-readable detail of the last failure on
+ *     the calling thread.  There is no CPU fallback.
+ *   - A handle may be used from one stream at a time.
+ */
+#ifndef DS_LAYER_H
+#define DS_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DS_API __attribute__((visibility("default")))
+#else
+#define DS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DS_OK = 0,
+  DS_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size or shape      */
+  DS_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement     */
+  DS_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed        */
+  DS_ERR_WORKSPACE = 4,     /* workspace smaller than ds_*_workspace_bytes()      */
+  DS_ERR_DEVICE = 5         /* a device-side check failed (see ds_workspace_status) */
+} ds_status;
+
+typedef enum { DS_F16 = 0, DS_BF16 = 1, DS_I8 = 2 } ds_dtype;
+
+/* Shape and numeric format of one layer ([P1] §3.2; dtypes as in the [P3]
+ * configuration table; int8 weights as in [P1] §5.2). */
+typedef struct {
+  int hidden;          /* H                                                   */
+  int heads;           /* nh; head_dim d = H / nh                             */
+  int ffn;             /* F, width of the FFN up-projection                   */
+  float ln_eps;        /* LayerNorm epsilon (1e-5 in every shipped workload)  */
+  ds_dtype act_dtype;  /* DS_F16 or DS_BF16: hidden states, caches, biases, LN */
+  ds_dtype weight_dtype; /* DS_F16 / DS_BF16 (must equal act_dtype) or DS_I8    */
+  int quant_group;     /* DS_I8 only: group length along K; must be 64        */
+} ds_layer_config;
+
+/* Device pointers to one layer's parameters.  Vectors are in act_dtype.
+ * Matrices are [out][in]: w_qkv [3H][H], w_o [H][H], w_fc1 [F][H], w_fc2 [H][F],
+ * in weight_dtype (int8 codes for DS_I8).  For DS_I8, s_* hold the float16
+ * group scales [out][in / quant_group]; they are ignored otherwise. */
+typedef struct {
+  const void *ln1_g, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o;
+  const void *ln2_g, *ln2_b, *w_fc1, *b_fc1, *w_fc2, *b_fc2;
+  const void *s_qkv, *s_o, *s_fc1, *s_fc2;
+} ds_layer_weights;
+
+typedef struct ds_layer ds_layer;
+typedef struct ds_stack ds_stack;
+
+/* Validates the config and stores the weight pointers (no copy, no launch).
+ * *out receives a handle owned by the caller; free it with ds_layer_destroy. */
+DS_API ds_status ds_layer_create(const ds_layer_config* cfg, const ds_layer_weights* w,
+                          ds_layer** out);
+DS_API ds_status ds_layer_destroy(ds_layer* layer);
+
+/* Bytes of device workspace that ds_layer_forward needs for `batch` sequences
+ * of `new_tokens` tokens each.  Returns 0 for invalid arguments. */
+DS_API size_t ds_layer_workspace_bytes(const ds_layer* layer, int batch, int new_tokens);
+
+/* Zero-fills a workspace (the counters inside it must start at zero).  Call it
+ * once after allocating a workspace; every successful call leaves the
+ * counters at zero again, so one workspace serves any number of calls. */
+DS_API ds_status ds_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* One layer forward over T = new_tokens new tokens per sequence (regions
+ * R1..R4 of [P1] §3.2).
+ *   x_in     [B][T][H] act_dtype, read only
+ *   x_out    [B][T][H] act_dtype, written (must not alias x_in)
+ *   k_cache, v_cache  [B][nh][max_len][d]; positions past_len[b]+t are written
+ *   past_len [B] int32 DEVICE array, read only; past_len[b] + T <= max_len is
+ *            required.  A violating row is not written: its outputs are left
+ *            unspecified and the workspace status word records
+ *            DS_DEVFLAG_CACHE_OVERFLOW (read it with ds_workspace_status).
+ *   workspace  device scratch of at least ds_layer_workspace_bytes() bytes,
+ *            zero-filled once (ds_workspace_init) before first use.
+ * Five kernels are enqueued on `stream` (a cudaStream_t). */
+DS_API ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out, int batch,
+                           int new_tokens, void* k_cache, void* v_cache, int max_len,
+                           const int32_t* past_len, void* workspace, size_t ws_bytes,
+                           void* stream);
+
+/* A stack of layers that share one config.  The layer handles stay owned by
+ * the caller and must outlive the stack. */
+DS_API ds_status ds_stack_create(ds_layer* const* layers, int n_layers, ds_stack** out);
+DS_API ds_status ds_stack_destroy(ds_stack* stack);
+DS_API size_t ds_stack_workspace_bytes(const ds_stack* stack, int batch);
+
+/* One decode step (T = 1) through every layer of the stack.
+ *   x_in, x_out  [B][H] act_dtype (must not alias)
+ *   k_caches, v_caches  HOST arrays of n_layers DEVICE pointers, one cache
+ *            pair per layer, each [B][nh][max_len][d]
+ *   seq_len  [B] int32 DEVICE array: positions already cached; the new token
+ *            is written at seq_len[b], and the step adds 1 to every entry on
+ *            the device after the last layer has read it.
+ * The launch sequence (5 kernels per layer, chained with programmatic
+ * dependent launch) is captured into a CUDA graph on the first call with a
+ * given argument set and replayed afterwards; when `stream` is the legacy
+ * default stream or is already capturing, the kernels are launched directly. */
+DS_API ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, int batch,
+                               void* const* k_caches, void* const* v_caches, int max_len,
+                               int32_t* seq_len, void* workspace, size_t ws_bytes,
+                               void* stream);
+
+/* The same decode step with the step's input and output in HOST memory:
+ * copies x_host -> x_dev_in, runs ds_stack_decode_step, copies x_dev_out ->
+ * y_host and synchronises `stream` before returning (end-to-end timing).
+ * x_dev_in / x_dev_out are caller-owned device staging buffers [B][H]. */
+DS_API ds_status ds_stack_decode_host(ds_stack* stack, const void* x_host, void* y_host,
+                               void* x_dev_in, void* x_dev_out, int batch,
+                               void* const* k_caches, void* const* v_caches, int max_len,
+                               int32_t* seq_len, void* workspace, size_t ws_bytes,
+                               void* stream);
+
+/* Profile mode: when on, ds_stack_decode_step launches without the graph and
+ * without programmatic dependent launch, records a CUDA event pair around
+ * every region kernel, synchronises the stream at the end of the step and
+ * accumulates the per-region kernel times. */
+DS_API ds_status ds_stack_set_profiling(ds_stack* stack, int enabled);
+/* Average microseconds per launch of each region kernel since the last reset:
+ * us_out[0] R1 LN1+QKV, [1] R2 attention, [2] R3 O-proj+residual+LN2 stats,
+ * [3] R4a FFN-up+GeLU, [4] R4b FFN-down+residual; launches_out[i] = launches
+ * averaged.  Resets the accumulators. */
+DS_API ds_status ds_stack_region_times(ds_stack* stack, float us_out[5], int launches_out[5]);
+
+/* MoQ-style quantisation of a float16 weight matrix w_f16 [n][k] ([P1] §5.2):
+ * per group of `group` (= 64) consecutive weights along k, scale
+ * s = fp16_rne(float32(max|w|) / 127) and code q = clamp(rne(w / s), -127, 127)
+ * (IEEE float32 division); s = 0 and q = 0 for an all-zero group.
+ * codes [n][k] int8 and scales_f16 [n][k/group] are written on `stream`. */
+DS_API ds_status ds_quantize_int8(const void* w_f16, int n, int k, int group, int8_t* codes,
+                           void* scales_f16, void* stream);
+
+/* Device-side status flags recorded in the workspace. */
+#define DS_DEVFLAG_CACHE_OVERFLOW 0x1  /* past_len[b] + T > max_len for some row */
+
+/* Copies the workspace status word to *flags_out, clears it, and synchronises
+ * `stream`.  Returns DS_ERR_DEVICE when a flag was set, DS_OK otherwise. */
+DS_API ds_status ds_workspace_status(void* workspace, uint32_t* flags_out, void* stream);
+
+/* Number of kernels this library has launched (a graph replay counts every
+ * kernel node in the graph) since the process started. */
+DS_API uint64_t ds_launch_count(void);
+
+DS_API const char* ds_status_string(ds_status s);
+/* Detail of the last failure on the calling thread ("" if none). */
+DS_API const char* ds_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DS_LAYER_H */

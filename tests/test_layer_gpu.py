@@ -1,0 +1,168 @@
+"""GPU parity of one layer forward (all four fusion regions) against the oracle.
+
+Cases span several 16-row tiles and K slices, ragged cache lengths across
+batch rows, several new tokens per sequence (the causal mask inside the new
+tokens), the empty cache (past_len = 0), batch rows 1..64 (one to eight MMA
+column tiles) and the three weight formats.  Page: "DeepSpeed Inference 内核优化
+深度解析：多 GPU 自适应并行、算子融合推理内核与 MoQ 量化支持", §3.2 and §5.2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import DeviceLayer, check_close, new_workspace, to64
+from transformer_layer_gb300 import ds, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def run_layer(L, B, T, past, max_len, seed=7):
+    H, nh = L.hidden, L.heads
+    d = H // nh
+    kc, vc = inputs.kv_cache(B, nh, max_len, d, seed, dtype=L.act_dtype, device="cuda")
+    x = inputs.hidden(B, T, H, seed, dtype=L.act_dtype, device="cuda")
+    K0, V0 = to64(kc), to64(vc)
+    kc0, vc0 = kc.clone(), vc.clone()
+    past_t = torch.tensor(past, dtype=torch.int32, device="cuda")
+    out = torch.full_like(x, float("nan"))
+    nbytes = ds.ds_layer_workspace_bytes(L.handle, B, T)
+    ws = new_workspace(nbytes)
+    ds.ds_layer_forward(L.handle, x, out, B, T, kc, vc, max_len, past_t, ws, nbytes)
+    torch.cuda.synchronize()
+    code, flags = ds.ds_workspace_status(ws)
+    assert code == ds.DS_OK and flags == 0
+    r = oracle.layer_forward(to64(x), L.oracle_params(), K0, V0, past, nh)
+    return dict(out=out, kc=kc, vc=vc, kc0=kc0, vc0=vc0, ref=r, ws=ws, nbytes=nbytes, x=x,
+                past_t=past_t)
+
+
+def check_layer(L, res, B, T, past, what):
+    dt = L.act_dtype
+    check_close(res["out"].reshape(B, T, -1), res["ref"]["y"], dt, what=what + " y")
+    kc, vc = res["kc"], res["vc"]
+    newmask = torch.zeros(kc.shape[:3], dtype=torch.bool, device=kc.device)
+    for b in range(B):
+        for t in range(T):
+            pos = past[b] + t
+            check_close(kc[b, :, pos, :], res["ref"]["k_new"][b, t], dt, what=f"{what} k[{b},{t}]")
+            check_close(vc[b, :, pos, :], res["ref"]["v_new"][b, t], dt, what=f"{what} v[{b},{t}]")
+            newmask[b, :, pos] = True
+    # every other cache position is untouched, bit for bit
+    assert torch.equal(kc[~newmask], res["kc0"][~newmask])
+    assert torch.equal(vc[~newmask], res["vc0"][~newmask])
+
+
+@pytest.mark.parametrize("B,T,past", [
+    (1, 1, [32]),          # the single-layer workload: H=256, 4 heads, 32 cached
+    (1, 1, [0]),           # empty cache: attention over the new token only
+    (3, 1, [5, 31, 0]),    # ragged cache lengths
+    (2, 3, [4, 17]),       # three new tokens: causal mask among them
+    (8, 1, list(range(0, 40, 5))),
+    (16, 1, [(7 * i) % 40 for i in range(16)]),
+    (5, 8, [1, 9, 3, 30, 12]),   # 40 rows: four column tiles of the MMA
+    (64, 1, [(11 * i) % 45 for i in range(64)]),
+])
+def test_layer256_f16(B, T, past):
+    L = DeviceLayer(256, 4, 1024, seed=1000)
+    try:
+        res = run_layer(L, B, T, past, max_len=48)
+        check_layer(L, res, B, T, past, f"f16 B={B} T={T}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("B,T,past", [(1, 1, [32]), (4, 2, [3, 0, 21, 8]), (24, 1, [(5 * i) % 40 for i in range(24)])])
+def test_layer256_bf16(B, T, past):
+    L = DeviceLayer(256, 4, 1024, seed=1001, act_dtype=torch.bfloat16, weight_dtype=torch.bfloat16)
+    try:
+        res = run_layer(L, B, T, past, max_len=48)
+        check_layer(L, res, B, T, past, f"bf16 B={B} T={T}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("act", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("B,T,past", [(1, 1, [40]), (6, 1, [0, 3, 9, 27, 33, 12]), (16, 1, [(3 * i) % 41 for i in range(16)])])
+def test_layer512_int8(act, B, T, past):
+    L = DeviceLayer(512, 4, 1024, seed=1002, act_dtype=act, weight_dtype=torch.int8)
+    try:
+        for k in ("w_qkv", "w_o", "w_fc1", "w_fc2"):     # codes and scales bit-exact
+            q, s = oracle.quantize_int8(L.p[k].cpu().numpy(), 64)
+            assert np.array_equal(L.codes[k].cpu().numpy(), q)
+            assert np.array_equal(L.scales[k].cpu().numpy().view(np.uint16), s.view(np.uint16))
+        res = run_layer(L, B, T, past, max_len=48)
+        check_layer(L, res, B, T, past, f"int8/{act} B={B}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("H,nh,F,B", [(2560, 20, 10240, 1), (4096, 32, 16384, 1), (4096, 32, 16384, 4)])
+def test_full_width_layer_f16(H, nh, F, B):
+    """One layer at the full widths of the GPT-Neo-2.7B- and 7B-shaped stacks
+    (many K slices and split-K fix-ups), every output element checked."""
+    L = DeviceLayer(H, nh, F, seed=1003)
+    try:
+        past = [128 + 97 * b for b in range(B)]
+        res = run_layer(L, B, 1, past, max_len=640)
+        check_layer(L, res, B, 1, past, f"H={H} B={B}")
+    finally:
+        L.close()
+
+
+def test_zero_weight_layer_is_identity():
+    L = DeviceLayer(256, 4, 1024, seed=5)
+    try:
+        for k in list(L.dev):
+            L.dev[k].zero_()
+        B, T = 2, 1
+        res = run_layer(L, B, T, [3, 7], max_len=16)
+        assert torch.equal(res["out"], res["x"])
+    finally:
+        L.close()
+
+
+def test_cache_overflow_is_flagged_not_written():
+    L = DeviceLayer(256, 4, 1024, seed=6)
+    try:
+        B, T, max_len = 2, 2, 16
+        kc, vc = inputs.kv_cache(B, 4, max_len, 64, 1, device="cuda")
+        kc0 = kc.clone()
+        x = inputs.hidden(B, T, 256, 1, device="cuda")
+        out = torch.empty_like(x)
+        past = torch.tensor([3, 15], dtype=torch.int32, device="cuda")   # 15 + 2 > 16
+        nbytes = ds.ds_layer_workspace_bytes(L.handle, B, T)
+        ws = new_workspace(nbytes)
+        ds.ds_layer_forward(L.handle, x, out, B, T, kc, vc, max_len, past, ws, nbytes)
+        torch.cuda.synchronize()
+        code, flags = ds.ds_workspace_status(ws)
+        assert code == ds.DS_ERR_DEVICE and flags & ds.DS_DEVFLAG_CACHE_OVERFLOW
+        assert torch.equal(kc[1, :, :15], kc0[1, :, :15])       # nothing before the slot changed
+        code, flags = ds.ds_workspace_status(ws)                 # the flag was cleared
+        assert code == ds.DS_OK and flags == 0
+    finally:
+        L.close()
+
+
+def test_bad_arguments_rejected_before_launch():
+    L = DeviceLayer(256, 4, 1024, seed=7)
+    try:
+        x = torch.zeros(1, 1, 256, dtype=torch.float16, device="cuda")
+        out = torch.empty_like(x)
+        kc = torch.zeros(1, 4, 8, 64, dtype=torch.float16, device="cuda")
+        past = torch.zeros(1, dtype=torch.int32, device="cuda")
+        nbytes = ds.ds_layer_workspace_bytes(L.handle, 1, 1)
+        ws = new_workspace(nbytes)
+        n0 = ds.ds_launch_count()
+        with pytest.raises(ds.DSError) as e:
+            ds.ds_layer_forward(L.handle, x, out, 1, 1, kc, kc, 8, past, ws, nbytes - 256)
+        assert e.value.code == ds.DS_ERR_WORKSPACE
+        with pytest.raises(ds.DSError) as e:
+            ds.ds_layer_forward(L.handle, x, x, 1, 1, kc, kc, 8, past, ws, nbytes)
+        assert e.value.code == ds.DS_ERR_INVALID_ARG
+        with pytest.raises(ds.DSError) as e:
+            ds.ds_layer_forward(L.handle, x, out, 65, 1, kc, kc, 8, past, ws, nbytes)
+        assert e.value.code == ds.DS_ERR_UNSUPPORTED
+        assert ds.ds_launch_count() == n0
+    finally:
+        L.close()

@@ -1,0 +1,170 @@
+"""GPU parity of the stack decode step (graph replay, device-side seq_len).
+
+Each decode step is judged layer by layer, teacher-forced: the oracle gets
+the device's input to that layer and the cache contents the device had before
+the step, and its float64 result is compared with the device's layer output
+and new cache entries.  Free-running drift of the whole stack is bounded
+loosely.  Page: "DeepSpeed Inference 内核优化深度解析：多 GPU 自适应
+并行、算子融合推理内核与 MoQ 量化支持", §3.2 (layer regions; the stack is the
+token-by-token generation loop calling every layer once per token).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import DeviceLayer, check_close, new_workspace, to64
+from transformer_layer_gb300 import ds, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+class DeviceStack:
+    def __init__(self, n_layers, H, nh, F, B, max_len, past, seed, act=torch.float16, wdt=torch.float16):
+        self.layers = [DeviceLayer(H, nh, F, seed, layer=l, act_dtype=act, weight_dtype=wdt)
+                       for l in range(n_layers)]
+        self.handle = ds.ds_stack_create([l.handle for l in self.layers])
+        d = H // nh
+        self.kc, self.vc = [], []
+        for l in range(n_layers):
+            k, v = inputs.kv_cache(B, nh, max_len, d, seed, layer=l, dtype=act, device="cuda")
+            self.kc.append(k)
+            self.vc.append(v)
+        self.B, self.H, self.nh, self.max_len = B, H, nh, max_len
+        self.seq = torch.tensor(past, dtype=torch.int32, device="cuda")
+        self.nbytes = ds.ds_stack_workspace_bytes(self.handle, B)
+        self.ws = new_workspace(self.nbytes)
+        self.act = act
+
+    def step(self, x, out, stream=None):
+        ds.ds_stack_decode_step(self.handle, x, out, self.B, self.kc, self.vc, self.max_len, self.seq,
+                                self.ws, self.nbytes, stream)
+
+    def close(self):
+        ds.ds_stack_destroy(self.handle)
+        for l in self.layers:
+            l.close()
+
+
+def prefix_outputs(S, x, stream):
+    """Device input of every layer for one step: run stacks of layers [0..l] on
+    copies of the caches and sequence lengths.  The kernels are deterministic,
+    so layer l's input inside the full stack is bit-identical to the output of
+    the prefix [0..l-1]."""
+    outs = []
+    for l in range(len(S.layers)):
+        h = ds.ds_stack_create([lay.handle for lay in S.layers[:l + 1]])
+        try:
+            kc = [k.clone() for k in S.kc[:l + 1]]
+            vc = [v.clone() for v in S.vc[:l + 1]]
+            seq = S.seq.clone()
+            nb = ds.ds_stack_workspace_bytes(h, S.B)
+            ws = new_workspace(nb)
+            o = torch.empty_like(x)
+            ds.ds_stack_decode_step(h, x, o, S.B, kc, vc, S.max_len, seq, ws, nb, stream)
+            stream.synchronize()
+            outs.append(o)
+        finally:
+            ds.ds_stack_destroy(h)
+    return outs
+
+
+@pytest.mark.parametrize("act", [torch.float16, torch.bfloat16])
+def test_stack_steps_graph_vs_oracle(act):
+    """Four graph-replayed decode steps of a 3-layer stack.  Each layer is judged
+    against the oracle fed that layer's device input and the device cache
+    contents before the step (teacher-forced, layer by layer); the step output
+    must equal the last prefix's output bit for bit; the free-running drift of
+    the whole stack against the oracle is checked only loosely."""
+    n_layers, H, nh, F, B, max_len = 3, 512, 8, 2048, 2, 40
+    past = [7, 20]
+    S = DeviceStack(n_layers, H, nh, F, B, max_len, past, seed=1100, act=act, wdt=act)
+    stream = torch.cuda.Stream()
+    try:
+        with torch.cuda.stream(stream):
+            for step in range(4):
+                x = inputs.hidden(B, 1, H, 1100, step=step, dtype=act, device="cuda").reshape(B, H)
+                out = torch.empty_like(x)
+                K = [to64(k) for k in S.kc]
+                V = [to64(v) for v in S.vc]
+                cur = S.seq.cpu().tolist()
+                assert cur == [p + step for p in past]
+                pre = prefix_outputs(S, x, stream)
+                S.step(x, out, stream)
+                stream.synchronize()
+                assert torch.equal(out, pre[-1])
+                params = [l.oracle_params() for l in S.layers]
+                for l in range(n_layers):
+                    xin = x if l == 0 else pre[l - 1]
+                    r = oracle.layer_forward(to64(xin).reshape(B, 1, H), params[l], K[l], V[l], cur, nh)
+                    check_close(pre[l].reshape(B, 1, H), r["y"], act, what=f"step {step} layer {l} y")
+                    for b in range(B):
+                        check_close(S.kc[l][b, :, cur[b], :], r["k_new"][b, 0], act,
+                                    what=f"step {step} layer {l} k")
+                        check_close(S.vc[l][b, :, cur[b], :], r["v_new"][b, 0], act,
+                                    what=f"step {step} layer {l} v")
+                free = oracle.stack_forward(to64(x).reshape(B, 1, H), params, K, V, cur, nh)
+                drift = float(np.linalg.norm(to64(out) - free[-1]["y"].reshape(B, H)) /
+                              np.linalg.norm(free[-1]["y"]))
+                assert drift < 1e-2, drift
+        assert S.seq.cpu().tolist() == [p + 4 for p in past]
+    finally:
+        S.close()
+
+
+def test_graph_replay_matches_direct_and_profile_launches():
+    """Graph replay, profile mode (no graph, no PDL) and the legacy-stream direct
+    path run the same kernels in the same order: results are bit-identical."""
+    n_layers, H, nh, F, B, max_len = 2, 256, 4, 1024, 3, 24
+    past = [2, 9, 0]
+    outs = []
+    for mode in ("graph", "profile", "legacy"):
+        S = DeviceStack(n_layers, H, nh, F, B, max_len, past, seed=1200)
+        try:
+            stream = torch.cuda.Stream() if mode != "legacy" else None
+            if mode == "profile":
+                ds.ds_stack_set_profiling(S.handle, True)
+            ys = []
+            for step in range(3):
+                x = inputs.hidden(B, 1, H, 1200, step=step, device="cuda").reshape(B, H)
+                out = torch.empty_like(x)
+                torch.cuda.synchronize()
+                if mode == "legacy":
+                    ds.ds_stack_decode_step(S.handle, x, out, B, S.kc, S.vc, max_len, S.seq, S.ws,
+                                            S.nbytes, 0)
+                else:
+                    S.step(x, out, stream)
+                torch.cuda.synchronize()
+                ys.append(out.clone())
+            if mode == "profile":
+                us, n = ds.ds_stack_region_times(S.handle)
+                assert n == [3 * n_layers] * 5 and all(u > 0 for u in us)
+            outs.append((torch.stack(ys), torch.stack([k.clone() for k in S.kc])))
+        finally:
+            S.close()
+    for y, k in outs[1:]:
+        assert torch.equal(y, outs[0][0])
+        assert torch.equal(k, outs[0][1])
+
+
+def test_decode_host_entry_point():
+    n_layers, H, nh, F, B, max_len = 2, 256, 4, 1024, 2, 20
+    S = DeviceStack(n_layers, H, nh, F, B, max_len, [4, 11], seed=1300)
+    S2 = DeviceStack(n_layers, H, nh, F, B, max_len, [4, 11], seed=1300)
+    try:
+        stream = torch.cuda.Stream()
+        x = inputs.hidden(B, 1, H, 1300, device="cuda").reshape(B, H)
+        xh = x.cpu().pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        xd, yd = torch.empty_like(x), torch.empty_like(x)
+        n0 = ds.ds_launch_count()
+        ds.ds_stack_decode_host(S.handle, xh, yh, xd, yd, B, S.kc, S.vc, max_len, S.seq, S.ws, S.nbytes,
+                                stream)
+        assert ds.ds_launch_count() - n0 == 5 * n_layers
+        out = torch.empty_like(x)
+        S2.step(x, out, stream)
+        stream.synchronize()
+        assert torch.equal(yh, out.cpu())
+    finally:
+        S.close()
+        S2.close()

@@ -1,0 +1,101 @@
+// Internal launch interface between the C-ABI layer (ds_api.cu) and the
+// region kernels.  Nothing here is exported from the shared library.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ds {
+
+enum class WKind : int { F16 = 0, BF16 = 1, I8 = 2 };
+enum class ActKind : int { F16 = 0, BF16 = 1 };
+
+// The four GEMV-based region kernels ([P1] §3.2 regions 1, 3, 3/4 and 4).
+enum class Region : int {
+  LnQkv = 0,     // R1: LayerNorm1 prologue, QKV GEMV, bias, KV-cache append
+  OprojRes = 1,  // R3: O-proj GEMV, bias, residual, LayerNorm2 statistics
+  FfnUp = 2,     // R4a: LayerNorm2 prologue, FFN-up GEMV, bias, GeLU
+  FfnDown = 3    // R4b: FFN-down GEMV, bias, residual (+ next LayerNorm statistics)
+};
+
+// Work split of one skinny GEMM y[M][N] = x[M][K] W[N][K]^T (see gemv.cu).
+struct GemvPlan {
+  int KS = 1;       // number of K slices
+  int K_S = 0;      // slice length (multiple of 8 * step_k)
+  int tiles = 0;    // N / 16 row tiles
+  int items = 0;    // KS * tiles work items
+  int grid = 0;     // CTAs
+  int nt = 1;       // n-tiles of 8 batch rows (1, 2, 4, 8)
+  int nblk = 2;     // k-blocks per warp step (2, or 1 for narrow K)
+  size_t smem = 0;  // dynamic shared memory bytes
+};
+
+struct RegionArgs {
+  // GEMV operand
+  const void* W = nullptr;         // [N][K] weights (fp16/bf16) or int8 codes
+  const __half* Wscale = nullptr;  // int8: fp16 scales [N][K/64]
+  int N = 0, K = 0, M = 0;         // M = B * T rows
+  int B = 1, T = 1;
+  GemvPlan plan;
+  float* partials = nullptr;       // [KS][N][M] split-K partial sums
+  int* counters = nullptr;         // [tiles] arrival counters (self-resetting)
+  const void* bias = nullptr;      // [N] act dtype
+  // prologue
+  const void* x_act = nullptr;     // R1: layer input [M][K] act dtype
+  const float* x_f32 = nullptr;    // R3: attention output; R4a: x1; R4b: GeLU output
+  const void* ln_g = nullptr;      // LayerNorm gamma / beta (R1, R4a)
+  const void* ln_b = nullptr;
+  float eps = 1e-5f;
+  const float* stats_in = nullptr; // [K/16][M][2] (sum, M2) partials, or null
+  // epilogue
+  float* out_f32 = nullptr;        // R1: q [M][H]; R3: x1; R4a: g
+  void* out_act = nullptr;         // R4b: layer output [M][N]
+  const void* resid_act = nullptr; // R3: layer input (residual)
+  const float* resid_f32 = nullptr;// R4b: x1 (residual)
+  float* stats_out = nullptr;      // R3 / R4b: [N/16][M][2] partials, or null
+  // R1 cache append
+  void* k_cache = nullptr;
+  void* v_cache = nullptr;
+  int heads = 0, head_dim = 0, max_len = 0, H = 0;
+  const int32_t* past_len = nullptr;
+  unsigned* status = nullptr;
+  // R4b of the last layer of a stack step: add 1 to seq_len[0..B) at the end
+  int32_t* seq_len_inc = nullptr;
+};
+
+struct AttnArgs {
+  const float* q = nullptr;         // [B*T][H] fp32
+  const void* k_cache = nullptr;    // [B][nh][max_len][d]
+  const void* v_cache = nullptr;
+  const int32_t* past_len = nullptr;
+  int B = 1, T = 1, heads = 0, head_dim = 0, max_len = 0, H = 0;
+  int nsplit = 1;
+  int chunk_cap = 0;                // keys per split the smem was sized for
+  float scale_log2 = 0.f;           // log2(e) / sqrt(head_dim)
+  size_t smem = 0;
+  float* part = nullptr;            // [B*T][nh][nsplit][d + 2]
+  int* counters = nullptr;          // [B][nh]
+  float* out = nullptr;             // [B*T][H] fp32
+  unsigned* status = nullptr;
+};
+
+// Chooses the work split for one GEMV; returns false if no valid split exists.
+bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int ctas_per_sm,
+                    GemvPlan* plan);
+cudaError_t launch_region(Region r, WKind wk, ActKind ak, const RegionArgs& a,
+                          cudaStream_t st, bool pdl);
+// Sets the dynamic shared-memory limit of every region kernel (call once per
+// device before the first launch).
+cudaError_t prepare_region_kernels(int max_smem);
+
+int attn_nsplit(int B, int heads, int max_len, int num_sms);
+size_t attn_smem_bytes(int head_dim, int chunk_cap);
+cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl);
+cudaError_t prepare_attention_kernels(int max_smem);
+
+cudaError_t launch_quantize_int8(const void* w, int n, int k, int8_t* codes, void* scales,
+                                 cudaStream_t st);
+
+}  // namespace ds
