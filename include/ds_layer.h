@@ -32,8 +32,9 @@
  *   - Hidden states are [B][T][H] (batch rows, new tokens, features) in the
  *     activation dtype.  The K and V caches of a layer are two separate
  *     arrays [B][nh][max_len][d] in the activation dtype.
- *   - Every pointer must be 16-byte aligned; H, F and d must be multiples of
- *     64; d must be 64 or 128; B*T must be 1..64.
+ *   - Every pointer must be 16-byte aligned (the workspace 256-byte aligned);
+ *     d must be 64 or 128; H and F must be multiples of 256 for fp16/bf16
+ *     weights and of 512 for int8 weights; B*T must be 1..64.
  *   - Calls are asynchronous on the given stream (never synchronising, except
  *     ds_stack_region_times, ds_workspace_status and ds_stack_decode_host,
  *     which say so).  A stream of 0 means the legacy default stream.
@@ -182,6 +183,7 @@ DS_API ds_status ds_quantize_int8(const void* w_f16, int n, int k, int group, in
 
 /* Device-side status flags recorded in the workspace. */
 #define DS_DEVFLAG_CACHE_OVERFLOW 0x1  /* past_len[b] + T > max_len for some row */
+#define DS_DEVFLAG_WAIT_TIMEOUT 0x2    /* an in-kernel pipeline wait gave up (outputs invalid) */
 
 /* Copies the workspace status word to *flags_out, clears it, and synchronises
  * `stream`.  Returns DS_ERR_DEVICE when a flag was set, DS_OK otherwise. */

@@ -37,8 +37,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   extern __shared__ __align__(16) float sm[];
   float* sc = sm;                         // [chunk_cap] scores, then probabilities
   float* ored = sc + a.chunk_cap;         // [KPI][D]
-  float* red = ored + KPI * D;            // [8] block-reduction scratch
-  int* flag = reinterpret_cast<int*>(red + 8);
+  float* red = ored + KPI * D;            // [32] block-reduction / merge scratch
+  int* flag = reinterpret_cast<int*>(red + 32);
 
   const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     // scores (log2 domain)
     float mloc = -INFINITY;
     const int passes = (n_keys + KPI - 1) / KPI;
-#pragma unroll 4
+#pragma unroll 8
     for (int ps = 0; ps < passes; ++ps) {
       const int j = ps * KPI + kr;
       float s = 0.f;
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     if (lane == 0) red[4 + warp] = lsum;
     // o = sum_j p_j v_j
     float o8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll 8
     for (int ps = 0; ps < passes; ++ps) {
       const int j = ps * KPI + kr;
       if (j < n_keys) {
@@ -166,19 +166,25 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   __syncthreads();
   if (*flag) {
     __threadfence();
+    float* wsm = red;  // [nsplit] merge weights (nsplit <= 32)
     for (int t = 0; t < a.T; ++t) {
-      if (tid < D) {
-        const float* base = a.part + ((size_t)(b * a.T + t) * a.heads + h) * a.nsplit * (D + 2);
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < a.nsplit; ++s2) M = fmaxf(M, ld_cg(base + s2 * (D + 2) + D));
-        float Lsum = 0.f, O = 0.f;
-        for (int s2 = 0; s2 < a.nsplit; ++s2) {
-          const float w = exp2f(ld_cg(base + s2 * (D + 2) + D) - M);
-          Lsum += w * ld_cg(base + s2 * (D + 2) + D + 1);
-          O += w * ld_cg(base + s2 * (D + 2) + tid);
-        }
-        a.out[(size_t)(b * a.T + t) * a.H + h * D + tid] = O / Lsum;
+      const float* base = a.part + ((size_t)(b * a.T + t) * a.heads + h) * a.nsplit * (D + 2);
+      if (warp == 0) {
+        const float ms = lane < a.nsplit ? ld_cg(base + lane * (D + 2) + D) : -INFINITY;
+        const float ls = lane < a.nsplit ? ld_cg(base + lane * (D + 2) + D + 1) : 0.f;
+        const float mx = warp_max(ms);
+        const float w = lane < a.nsplit ? exp2f(ms - mx) : 0.f;
+        const float lsum = warp_sum(w * ls);
+        if (lane < a.nsplit) wsm[lane] = w / lsum;
       }
+      __syncthreads();
+      if (tid < D) {
+        float O = 0.f;
+#pragma unroll 8
+        for (int s2 = 0; s2 < a.nsplit; ++s2) O += wsm[s2] * ld_cg(base + s2 * (D + 2) + tid);
+        a.out[(size_t)(b * a.T + t) * a.H + h * D + tid] = O;
+      }
+      __syncthreads();
     }
     if (tid == 0) a.counters[b * a.heads + h] = 0;
   }
@@ -196,7 +202,7 @@ int attn_nsplit(int B, int heads, int max_len, int num_sms) {
 
 size_t attn_smem_bytes(int head_dim, int chunk_cap) {
   const int kpi = kAttnThreads / (head_dim / 8);
-  return sizeof(float) * ((size_t)chunk_cap + (size_t)kpi * head_dim + 8) + 16;
+  return sizeof(float) * ((size_t)chunk_cap + (size_t)kpi * head_dim + 32) + 16;
 }
 
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl) {

@@ -104,10 +104,10 @@ bool make_plans(const ds_layer& L, int M, int B, Plans* p) {
   const int H = L.cfg.hidden, F = L.cfg.ffn;
   const WKind wk = wkind(L.cfg.weight_dtype);
   const ActKind ak = akind(L.cfg.act_dtype);
-  if (!gemv_make_plan(wk, ak, 3 * H, H, M, L.sms, L.ctas_per_sm, &p->qkv)) return false;
-  if (!gemv_make_plan(wk, ak, H, H, M, L.sms, L.ctas_per_sm, &p->o)) return false;
-  if (!gemv_make_plan(wk, ak, F, H, M, L.sms, L.ctas_per_sm, &p->up)) return false;
-  if (!gemv_make_plan(wk, ak, H, F, M, L.sms, L.ctas_per_sm, &p->down)) return false;
+  if (!gemv_make_plan(wk, ak, 3 * H, H, M, L.sms, L.ctas_per_sm, L.max_smem, &p->qkv)) return false;
+  if (!gemv_make_plan(wk, ak, H, H, M, L.sms, L.ctas_per_sm, L.max_smem, &p->o)) return false;
+  if (!gemv_make_plan(wk, ak, F, H, M, L.sms, L.ctas_per_sm, L.max_smem, &p->up)) return false;
+  if (!gemv_make_plan(wk, ak, H, F, M, L.sms, L.ctas_per_sm, L.max_smem, &p->down)) return false;
   p->nsplit_max = attn_nsplit(B, L.cfg.heads, 1 << 30, L.sms);
   return true;
 }
@@ -143,9 +143,8 @@ WsLayout ws_layout(const ds_layer& L, int B, int T, const Plans& p) {
   w.stats_b = take((size_t)(H / 16) * M * 2 * 4);
   size_t part = 0;
   const GemvPlan* ps[4] = {&p.qkv, &p.o, &p.up, &p.down};
-  const int ns[4] = {3 * H, H, F, H};
   for (int i = 0; i < 4; ++i)
-    if (ps[i]->KS > 1) part = std::max(part, (size_t)ps[i]->KS * ns[i] * M * 4);
+    part = std::max(part, (size_t)ps[i]->tiles * ps[i]->KS * ps[i]->maxc * 16 * M * 4);
   w.partials = take(part);
   w.attn_part = take(M * nh * (size_t)p.nsplit_max * (d + 2) * 4);
   w.act = take(2 * M * H * 2);

@@ -13,60 +13,45 @@ cudaError_t prepare_region_f16(int max_smem);
 cudaError_t prepare_region_bf16(int max_smem);
 cudaError_t prepare_region_i8(int max_smem);
 
-// Bytes of shared memory the staged x slice may use.
-static constexpr size_t kXBudget = 96 * 1024;
+// Bytes of shared memory the staged x slice may use (two CTAs share an SM).
+static constexpr size_t kXBudget = 80 * 1024;
 
-// Chooses K slice length and grid so that every CTA gets the same number of
-// items to within one.  Items are 16 rows x K_S; the score is the fraction of
-// the grid's item slots that hold work, preferring longer slices on ties
-// (fewer split-K partials to reduce).
+static size_t xs_bytes_nt(int nt, int M, int K_S, int pad, bool split) {
+  switch (nt) {
+    case 1: return SmemLayout<1>::xs_bytes(M, K_S, pad, split);
+    case 2: return SmemLayout<2>::xs_bytes(M, K_S, pad, split);
+    case 4: return SmemLayout<4>::xs_bytes(M, K_S, pad, split);
+    default: return SmemLayout<8>::xs_bytes(M, K_S, pad, split);
+  }
+}
+static size_t fixed_nt(int nt, int M, int K_S, int pad, bool split) {
+  switch (nt) {
+    case 1: return SmemLayout<1>::fixed(M, K_S, pad, split);
+    case 2: return SmemLayout<2>::fixed(M, K_S, pad, split);
+    case 4: return SmemLayout<4>::fixed(M, K_S, pad, split);
+    default: return SmemLayout<8>::fixed(M, K_S, pad, split);
+  }
+}
+
 bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int ctas_per_sm,
-                    GemvPlan* plan) {
-  if (N <= 0 || K <= 0 || M < 1 || M > 64 || (N % 16) != 0) return false;
-  GemvPlan p;
-  p.nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
-  const int blk_k = (wk == WKind::I8) ? 64 : 32;
-  const int pad = (wk == WKind::I8) ? 8 : 32;
+                    int max_smem, GemvPlan* plan) {
+  const bool i8 = (wk == WKind::I8);
+  const int blk_k = i8 ? 64 : 32;
+  const int pad = i8 ? 8 : 32;
+  const int esize = i8 ? 1 : 2;
   const bool split = (ak == ActKind::BF16);
-  p.nblk = (K % (kWarps * 2 * blk_k) == 0) ? 2 : 1;
-  const int unit = kWarps * p.nblk * blk_k;
-  if (K % unit != 0) return false;
-  p.tiles = N / 16;
-  const int G = num_sms * ctas_per_sm;
-  double best = -1.0;
-  int best_ks = 0;
-  for (int d = 1; d <= K / unit; ++d) {  // K_S = K / d, longest first
-    if ((K / unit) % d != 0) continue;
-    const int K_S = K / d;
-    size_t xs = 0;
-    switch (p.nt) {
-      case 1: xs = SmemLayout<1>::xs_bytes(K_S, pad, split); break;
-      case 2: xs = SmemLayout<2>::xs_bytes(K_S, pad, split); break;
-      case 4: xs = SmemLayout<4>::xs_bytes(K_S, pad, split); break;
-      default: xs = SmemLayout<8>::xs_bytes(K_S, pad, split); break;
-    }
-    if (xs > kXBudget) continue;
-    const long long items = (long long)d * p.tiles;
-    const long long g = items < G ? items : G;
-    const long long per = (items + g - 1) / g;
-    const double eff = (double)items / ((double)G * (double)per);
-    if (eff > best + 0.01) {
-      best = eff;
-      best_ks = K_S;
-    }
-  }
-  if (best_ks == 0) return false;
-  p.K_S = best_ks;
-  p.KS = K / best_ks;
-  p.items = p.KS * p.tiles;
-  p.grid = p.items < G ? p.items : G;
-  switch (p.nt) {
-    case 1: p.smem = SmemLayout<1>::total(p.K_S, pad, split); break;
-    case 2: p.smem = SmemLayout<2>::total(p.K_S, pad, split); break;
-    case 4: p.smem = SmemLayout<4>::total(p.K_S, pad, split); break;
-    default: p.smem = SmemLayout<8>::total(p.K_S, pad, split); break;
-  }
-  *plan = p;
+  const int nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
+  auto xs = [&](int K_S) { return xs_bytes_nt(nt, M, K_S, pad, split); };
+  if (!ws_make_plan(N, K, M, num_sms * ctas_per_sm, blk_k, kProducers, kXBudget, xs, plan)) return false;
+  // As deep a weight ring as the rest of shared memory allows (up to kMaxStages).
+  const size_t fixed = fixed_nt(plan->nt, M, plan->K_S, pad, split);
+  const size_t stage = SmemLayout<1>::stage_bytes(plan->chunk_k, esize, i8) + 16;
+  if ((size_t)max_smem <= fixed) return false;
+  size_t s = ((size_t)max_smem - fixed) / stage;
+  if (s > (size_t)kMaxStages) s = kMaxStages;
+  if (s < 2) return false;
+  plan->stages = (int)s;
+  plan->smem = fixed + s * stage;
   return true;
 }
 

@@ -20,16 +20,27 @@ enum class Region : int {
   FfnDown = 3    // R4b: FFN-down GEMV, bias, residual (+ next LayerNorm statistics)
 };
 
-// Work split of one skinny GEMM y[M][N] = x[M][K] W[N][K]^T (see gemv.cu).
+// Work split of one skinny GEMM y[M][N] = x[M][K] W[N][K]^T (see gemv_impl.cuh).
+// A unit is 16 weight rows x one K slice; a chunk is 8 warp steps of a unit.
+// Every CTA owns q whole units (data-parallel part); the leftover units'
+// chunks are spread evenly over all CTAs, whose partial sums are combined by
+// the last contributor of each row tile.
 struct GemvPlan {
-  int KS = 1;       // number of K slices
-  int K_S = 0;      // slice length (multiple of 8 * step_k)
-  int tiles = 0;    // N / 16 row tiles
-  int items = 0;    // KS * tiles work items
-  int grid = 0;     // CTAs
-  int nt = 1;       // n-tiles of 8 batch rows (1, 2, 4, 8)
-  int nblk = 2;     // k-blocks per warp step (2, or 1 for narrow K)
-  size_t smem = 0;  // dynamic shared memory bytes
+  int KS = 1;        // number of K slices
+  int K_S = 0;       // slice length
+  int tiles = 0;     // N / 16 row tiles
+  int units = 0;     // KS * tiles, slice-major (u = s * tiles + t)
+  int C = 0;         // chunks per unit
+  int chunk_k = 0;   // k per chunk (8 warps x one warp step)
+  int q = 0;         // whole units per CTA
+  int U_dp = 0;      // q * grid
+  long long R = 0;   // leftover chunks spread over the grid
+  int maxc = 1;      // most CTAs contributing to one leftover unit
+  int grid = 0;      // CTAs
+  int nt = 1;        // n-tiles of 8 batch rows (1, 2, 4, 8)
+  int nblk = 2;      // k-blocks per warp step (2, or 1 for narrow K)
+  int stages = 0;    // depth of the shared-memory weight ring (chunks in flight)
+  size_t smem = 0;   // dynamic shared memory bytes
 };
 
 struct RegionArgs {
@@ -39,7 +50,7 @@ struct RegionArgs {
   int N = 0, K = 0, M = 0;         // M = B * T rows
   int B = 1, T = 1;
   GemvPlan plan;
-  float* partials = nullptr;       // [KS][N][M] split-K partial sums
+  float* partials = nullptr;       // [tiles][KS * maxc][16][M] partial sums
   int* counters = nullptr;         // [tiles] arrival counters (self-resetting)
   const void* bias = nullptr;      // [N] act dtype
   // prologue
@@ -83,7 +94,7 @@ struct AttnArgs {
 
 // Chooses the work split for one GEMV; returns false if no valid split exists.
 bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int ctas_per_sm,
-                    GemvPlan* plan);
+                    int max_smem, GemvPlan* plan);
 cudaError_t launch_region(Region r, WKind wk, ActKind ak, const RegionArgs& a,
                           cudaStream_t st, bool pdl);
 // Sets the dynamic shared-memory limit of every region kernel (call once per

@@ -1,0 +1,154 @@
+// Work split of the skinny-GEMM region kernels, shared by the host planner,
+// the device kernels and the CPU replay test (tests/work_split_check.cu).
+//
+// Page cited as [P1]: "DeepSpeed Inference 内核优化深度解析：多 GPU 自适应并行、
+// 算子融合推理内核与 MoQ 量化支持", §3 intro (a skinny GEMM scheduled so that ops
+// fuse at its reduction boundary) and §3.1 (CTAs meet only through global
+// memory at the reduction boundary).
+//
+// y[M][N] = x[M][K] W[N][K]^T is cut into units of 16 weight rows x one K
+// slice (slice-major: u = s * tiles + t) and every unit into C chunks of
+// chunk_k = 8 warps x one warp step along K.  With G CTAs:
+//   * CTA c owns the q whole units [c q, (c+1) q) ("data-parallel" units);
+//   * the R = (units - q G) C chunks of the leftover units are split into G
+//     contiguous ranges [c R / G, (c+1) R / G), processed first.
+// A row tile whose result is spread over several CTAs or K slices is summed
+// by its last contributor, in fixed order (slice, then CTA), so results are
+// deterministic.
+#pragma once
+
+#include <stddef.h>
+
+#include "internal.h"
+
+#if defined(__CUDACC__)
+#define DS_HD __host__ __device__ __forceinline__
+#else
+#define DS_HD inline
+#endif
+
+namespace ds {
+
+// The CTA whose leftover range holds leftover chunk i.
+DS_HD int ws_cta_of(long long i, long long R, int G) { return (int)(((i + 1) * (long long)G - 1) / R); }
+
+// Number of CTAs contributing to unit u (every CTA owns >= 1 leftover chunk
+// whenever R > 0, so the contributors of a leftover unit are consecutive).
+DS_HD int ws_unit_contrib(int u, const GemvPlan& P, int G) {
+  if (u < P.U_dp) return 1;
+  const long long first = (long long)(u - P.U_dp) * P.C;
+  return ws_cta_of(first + P.C - 1, P.R, G) - ws_cta_of(first, P.R, G) + 1;
+}
+
+// Partial-sum contributions that complete row tile t (all K slices).
+DS_HD int ws_tile_target(int t, const GemvPlan& P, int G) {
+  int n = 0;
+  for (int s = 0; s < P.KS; ++s) n += ws_unit_contrib(s * P.tiles + t, P, G);
+  return n;
+}
+
+// Position in a CTA's chunk sequence: leftover chunks first, then whole units.
+struct Cursor {
+  int s, t, kc;  // slice, row tile, chunk within the unit
+  int rem_left;  // leftover chunks still to come, including this one
+};
+
+DS_HD void ws_cursor_init(Cursor& q, const GemvPlan& P, long long ra, long long rb, int dp_b) {
+  if (rb > ra) {
+    const long long u = P.U_dp + ra / P.C;
+    q.kc = (int)(ra % P.C);
+    q.s = (int)(u / P.tiles);
+    q.t = (int)(u - (long long)q.s * P.tiles);
+    q.rem_left = (int)(rb - ra);
+  } else {
+    q.rem_left = 0;
+    q.s = dp_b / P.tiles;
+    q.t = dp_b - q.s * P.tiles;
+    q.kc = 0;
+  }
+}
+
+DS_HD void ws_cursor_next(Cursor& q, const GemvPlan& P, int dp_b) {
+  if (q.rem_left > 0) {
+    if (--q.rem_left == 0) {
+      q.s = dp_b / P.tiles;
+      q.t = dp_b - q.s * P.tiles;
+      q.kc = 0;
+      return;
+    }
+  }
+  if (++q.kc == P.C) {
+    q.kc = 0;
+    if (++q.t == P.tiles) {
+      q.t = 0;
+      ++q.s;
+    }
+  }
+}
+
+// True when the chunk at cursor q is the last of its segment (a segment is a
+// run of one CTA's chunks inside one unit); j is the chunk's index in the CTA.
+DS_HD bool ws_segment_ends(const Cursor& q, const GemvPlan& P, int j, int nchunks) {
+  return q.kc == P.C - 1 || q.rem_left == 1 || j == nchunks - 1;
+}
+
+// The epilogue side's view of the leftover segments: starting at leftover
+// chunk i of CTA cta, the segment's unit, its end and the CTA's slot among
+// the unit's contributors.
+DS_HD void ws_leftover_segment(const GemvPlan& P, long long i, long long rb, int cta, int G, int* u,
+                               long long* end, int* j_slot) {
+  const long long uo = i / P.C;
+  *end = (uo + 1) * P.C < rb ? (uo + 1) * P.C : rb;
+  *u = (int)(P.U_dp + uo);
+  *j_slot = cta - ws_cta_of(uo * P.C, P.R, G);
+}
+
+// Host planner: the longest K slice whose staged x fits `x_budget` bytes, then
+// q whole units per CTA and the leftover units' chunks spread evenly.
+// xs_bytes(K_S) gives the staged-x bytes for a slice length.
+template <typename XsBytes>
+inline bool ws_make_plan(int N, int K, int M, int num_ctas, int blk_k, int warps, size_t x_budget,
+                         XsBytes xs_bytes, GemvPlan* plan) {
+  if (N <= 0 || K <= 0 || M < 1 || M > 64 || (N % 16) != 0 || num_ctas < 1) return false;
+  GemvPlan p;
+  p.nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
+  p.nblk = (K % (warps * 2 * blk_k) == 0) ? 2 : 1;
+  p.chunk_k = warps * p.nblk * blk_k;
+  if (K % p.chunk_k != 0) return false;
+  p.tiles = N / 16;
+  const int nck = K / p.chunk_k;
+  p.K_S = 0;
+  for (int d = 1; d <= nck; ++d) {
+    if (nck % d != 0) continue;
+    if (xs_bytes(K / d) <= x_budget) {
+      p.K_S = K / d;
+      break;
+    }
+  }
+  if (p.K_S == 0) return false;
+  p.KS = K / p.K_S;
+  p.C = p.K_S / p.chunk_k;
+  p.units = p.KS * p.tiles;
+  const long long total = (long long)p.units * p.C;
+  long long G = num_ctas;
+  if (G > total) G = total;
+  p.grid = (int)G;
+  p.q = p.units / p.grid;
+  // Every CTA must own at least one leftover chunk when there are any (so the
+  // CTAs sharing a leftover unit are consecutive, with no empty ranges in
+  // between): with fewer leftover chunks than CTAs, hand one whole unit per
+  // CTA back to the leftover pool.
+  const long long left = (long long)(p.units - p.q * p.grid) * p.C;
+  if (p.q > 0 && left > 0 && left < p.grid) p.q -= 1;
+  p.U_dp = p.q * p.grid;
+  p.R = (long long)(p.units - p.U_dp) * p.C;
+  p.maxc = 1;
+  for (int u = p.U_dp; u < p.units; ++u) {
+    const int n = ws_unit_contrib(u, p, p.grid);
+    if (n > p.maxc) p.maxc = n;
+  }
+  *plan = p;
+  return true;
+}
+
+}  // namespace ds

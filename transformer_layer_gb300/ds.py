@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_PKG, "libdslayer.so")
 DS_OK, DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED, DS_ERR_CUDA, DS_ERR_WORKSPACE, DS_ERR_DEVICE = range(6)
 DS_F16, DS_BF16, DS_I8 = 0, 1, 2
 DS_DEVFLAG_CACHE_OVERFLOW = 0x1
+DS_DEVFLAG_WAIT_TIMEOUT = 0x2
 
 # Every exported symbol of include/ds_layer.h, with (restype, argtypes).
 _vp = C.c_void_p
