@@ -130,6 +130,26 @@ DS_API ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out
                            const int32_t* past_len, void* workspace, size_t ws_bytes,
                            void* stream);
 
+/* ds_layer_forward for callers that cannot allocate device memory (plugins in
+ * frameworks that own and pre-reserve all GPU memory, latency-critical loops
+ * that must not risk the device-wide synchronisation of an allocation,
+ * real-time hosts that forbid allocation after start-up).  The pages have no
+ * counterpart: this is a property of the library, not of the method.
+ * Runs the same five kernels, with the workspace taken from a 16 MiB static
+ * device array inside the library (every GPU that loads the library holds
+ * it until the process exits); nothing is allocated or freed.
+ *   - Returns DS_ERR_UNSUPPORTED when ds_layer_workspace_bytes(layer, batch,
+ *     new_tokens) exceeds 16 MiB, and the argument errors of ds_layer_forward.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make it before any
+ *     stream capture.
+ *   - All calls share the array: calls that overlap on the GPU race.  Each
+ *     call clears the array's status word and counters first, so device
+ *     status flags of this entry point are not reported. */
+DS_API ds_status ds_layer_forward_noalloc(ds_layer* layer, const void* x_in, void* x_out, int batch,
+                                          int new_tokens, void* k_cache, void* v_cache, int max_len,
+                                          const int32_t* past_len, void* stream);
+
 /* A stack of layers that share one config.  The layer handles stay owned by
  * the caller and must outlive the stack. */
 DS_API ds_status ds_stack_create(ds_layer* const* layers, int n_layers, ds_stack** out);

@@ -480,6 +480,23 @@ ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out, int b
   return DS_OK;
 }
 
+}  // extern "C"
+
+namespace ds {
+void set_last_error(const char* msg) { g_err = msg; }
+
+// Bytes at the start of a workspace that must be zero before a call (status
+// word and arrival counters); 0 for invalid arguments.
+size_t layer_workspace_zero_prefix(const ds_layer* layer, int batch, int new_tokens) {
+  if (layer == nullptr || batch < 1 || new_tokens < 1 || (long long)batch * new_tokens > 64) return 0;
+  Plans p;
+  if (!make_plans(*layer, batch * new_tokens, batch, &p)) return 0;
+  return ws_layout(*layer, batch, new_tokens, p).q;
+}
+}  // namespace ds
+
+extern "C" {
+
 ds_status ds_stack_create(ds_layer* const* layers, int n_layers, ds_stack** out) {
   if (out == nullptr) return fail(DS_ERR_INVALID_ARG, "out is null");
   *out = nullptr;

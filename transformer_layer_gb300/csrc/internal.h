@@ -106,6 +106,16 @@ size_t attn_smem_bytes(int head_dim, int chunk_cap);
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl);
 cudaError_t prepare_attention_kernels(int max_smem);
 
+}  // namespace ds
+
+struct ds_layer;
+namespace ds {
+// Leading workspace bytes (status word + arrival counters) that must be zero
+// before a ds_layer_forward call with this batch shape; 0 if invalid.
+size_t layer_workspace_zero_prefix(const ds_layer* layer, int batch, int new_tokens);
+// Sets the detail string returned by ds_last_error() on this thread.
+void set_last_error(const char* msg);
+
 cudaError_t launch_quantize_int8(const void* w, int n, int k, int8_t* codes, void* scales,
                                  cudaStream_t st);
 

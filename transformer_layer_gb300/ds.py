@@ -28,6 +28,7 @@ _SIGS = {
     "ds_workspace_init": (C.c_int, [_vp, C.c_size_t, _vp]),
     "ds_layer_forward": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, _vp, C.c_int, _vp, _vp,
                                    C.c_size_t, _vp]),
+    "ds_layer_forward_noalloc": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, _vp, C.c_int, _vp, _vp]),
     "ds_stack_create": (C.c_int, [C.POINTER(_vp), C.c_int, C.POINTER(_vp)]),
     "ds_stack_destroy": (C.c_int, [_vp]),
     "ds_stack_workspace_bytes": (C.c_size_t, [_vp, C.c_int]),
@@ -140,6 +141,14 @@ def ds_layer_forward(layer, x_in, x_out, batch, new_tokens, k_cache, v_cache, ma
     _check(load().ds_layer_forward(layer, _ptr(x_in), _ptr(x_out), batch, new_tokens, _ptr(k_cache),
                                    _ptr(v_cache), max_len, _ptr(past_len), _ptr(ws), ws_bytes,
                                    _stream(stream)), "ds_layer_forward")
+
+
+def ds_layer_forward_noalloc(layer, x_in, x_out, batch, new_tokens, k_cache, v_cache, max_len, past_len,
+                             stream=None):
+    """The layer forward on the library's static workspace (no allocation)."""
+    _check(load().ds_layer_forward_noalloc(layer, _ptr(x_in), _ptr(x_out), batch, new_tokens, _ptr(k_cache),
+                                           _ptr(v_cache), max_len, _ptr(past_len), _stream(stream)),
+           "ds_layer_forward_noalloc")
 
 
 def ds_stack_create(layers):
