@@ -1,11 +1,12 @@
 // Region 2: decode attention over the KV cache with scale, causal mask and
-// softmax fused (split-KV, combined at the reduction boundary).
+// softmax fused; the key splits of one head are merged on chip.
 //
 // Pages cited:
 //   [P1] "DeepSpeed Inference 内核优化深度解析：多 GPU 自适应并行、算子融合推理内核
 //        与 MoQ 量化支持", §3.2 region 2: transform and attention merged, the
 //        head-split layout read through index arithmetic ("implicit matrix
-//        transformation") instead of being materialised.
+//        transformation") instead of being materialised; §3.3: shared memory
+//        between reductions, warp-level reductions of partial results.
 //   [P3] "DeepSpeed MoE 大规模稀疏模型推理实战指南：并行切分、PR-MoE 优化与
 //        init_inference 全解析", table "推理配置参数详解": triangular_masking,
 //        the causal mask.
@@ -13,14 +14,17 @@
 // What it computes, per sequence b, new token t and head h:
 //   s_j = q . k_j / sqrt(d) for j <= past_len[b] + t;  p = softmax(s);  o = sum_j p_j v_j.
 //
-// GB300 design (not the pages'): at batch 1 a layer has only nh (20-40) heads,
-// far fewer than 152 SMs, so each (b, h) is split over `nsplit` CTAs along the
-// keys.  Each CTA computes its keys' scores (16-byte loads, a key's d values
-// spread over d/8 lanes and reduced with warp shuffles), the local max and sum
-// (log2 domain) and the unnormalised p.V; the last CTA of each (b, h) to
-// arrive (atomic counter, no waiting) merges the splits with the usual
-// log-sum-exp rescaling.  Before griddepcontrol.wait a CTA asks the TMA unit to
-// prefetch into L2 the cache rows that the previous kernel does not write.
+// GB300 design (not the pages'): a layer has only nh (20-40) heads at batch
+// 1, far fewer than 152 SMs, so each (b, h) is split along the keys over a
+// thread-block cluster of `nsplit` (<= 8) CTAs.  A CTA loads the K and V rows
+// of its keys together (16-byte loads; a key's d values spread over d/8 lanes
+// and reduced with warp shuffles) and keeps a running max / sum / p.V per lane
+// group (online softmax, log2 domain), so there is one pass over the keys and
+// no score buffer.  The groups of a CTA merge in shared memory, and the CTAs
+// of the cluster merge through distributed shared memory in rank 0: no
+// global partials, no atomics.  Before griddepcontrol.wait a CTA asks the TMA
+// unit to prefetch into L2 the cache rows that the previous kernel does not
+// write.
 #include <math.h>
 
 #include "common.cuh"
@@ -29,26 +33,43 @@
 namespace ds {
 
 constexpr int kAttnThreads = 128;
+constexpr int kAttnMaxSplit = 8;  // portable cluster size
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
+                   : "memory");
+}
+// Reads a float from the shared memory of CTA `rank` of this cluster, at the
+// same offset as `local` in this CTA.
+__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
+  uint32_t addr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(addr) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 
 template <typename ACT, int D>
 __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs a) {
   constexpr int LPK = D / 8;               // lanes per key (16 B each)
-  constexpr int KPI = kAttnThreads / LPK;  // keys per CTA pass
+  constexpr int KPI = kAttnThreads / LPK;  // key groups per CTA (keys per pass)
+  constexpr int NB = 8;                    // passes whose K and V loads are in flight together
   extern __shared__ __align__(16) float sm[];
-  float* sc = sm;                         // [chunk_cap] scores, then probabilities
-  float* ored = sc + a.chunk_cap;         // [KPI][D]
-  float* red = ored + KPI * D;            // [32] block-reduction / merge scratch
-  int* flag = reinterpret_cast<int*>(red + 32);
+  float* og = sm;                // [KPI][D] per-group unnormalised p.V
+  float* mg = og + KPI * D;      // [KPI] per-group running max (log2 domain)
+  float* lg = mg + KPI;          // [KPI] per-group running sum
+  float* part = lg + KPI;        // [T][D + 2] this CTA's (O[D], M, L) per token
 
-  const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;  // sp = rank in the cluster
+  const int nsplit = gridDim.x;
+  const int tid = threadIdx.x;
   const int kq = tid % LPK, kr = tid / LPK;
 
   const int past = a.past_len[b];
   int S_all = past + a.T;
   if (S_all > a.max_len) S_all = a.max_len;
   if (S_all < 1) S_all = 1;
-  const int chunk = (S_all + a.nsplit - 1) / a.nsplit;
+  const int chunk = (S_all + nsplit - 1) / nsplit;
   const int lo = sp * chunk;
   const int hi = min(S_all, lo + chunk);
   const size_t head_row0 = ((size_t)b * a.heads + h) * a.max_len;
@@ -68,15 +89,6 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   for (int t = 0; t < a.T; ++t) {
     const int St = min(past + t + 1, S_all);
     const int n_keys = max(0, min(hi, St) - lo);
-    float* dst = a.part + (((size_t)(b * a.T + t) * a.heads + h) * a.nsplit + sp) * (D + 2);
-    if (n_keys == 0) {
-      if (tid < D) dst[tid] = 0.f;
-      if (tid == 0) {
-        dst[D] = -INFINITY;
-        dst[D + 1] = 0.f;
-      }
-      continue;
-    }
     float qv[8];
     {
       const float* qp = a.q + (size_t)(b * a.T + t) * a.H + h * D + kq * 8;
@@ -87,122 +99,124 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
 #pragma unroll
       for (int i = 0; i < 8; ++i) qv[i] *= a.scale_log2;
     }
-    // scores (log2 domain)
-    float mloc = -INFINITY;
-    const int passes = (n_keys + KPI - 1) / KPI;
-#pragma unroll 8
-    for (int ps = 0; ps < passes; ++ps) {
-      const int j = ps * KPI + kr;
-      float s = 0.f;
-      if (j < n_keys) {
-        const uint4 u = *reinterpret_cast<const uint4*>(Kc + (size_t)(lo + j) * D + kq * 8);
-        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = Act<ACT>::unpack2(uw[i]);
-          s += f.x * qv[2 * i] + f.y * qv[2 * i + 1];
-        }
-      }
-#pragma unroll
-      for (int o = LPK / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (j < n_keys) {
-        if (kq == 0) sc[j] = s;
-        mloc = fmaxf(mloc, s);
-      }
-    }
-    mloc = warp_max(mloc);
-    if (lane == 0) red[warp] = mloc;
-    __syncthreads();
-    const float m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    float lsum = 0.f;
-    for (int j = tid; j < n_keys; j += kAttnThreads) {
-      const float p = exp2f(sc[j] - m);
-      sc[j] = p;
-      lsum += p;
-    }
-    lsum = warp_sum(lsum);
-    __syncthreads();  // red reads done, probabilities visible
-    if (lane == 0) red[4 + warp] = lsum;
-    // o = sum_j p_j v_j
+    float m = -INFINITY, l = 0.f;
     float o8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int ps = 0; ps < passes; ++ps) {
-      const int j = ps * KPI + kr;
-      if (j < n_keys) {
-        const float p = sc[j];
-        const uint4 u = *reinterpret_cast<const uint4*>(Vc + (size_t)(lo + j) * D + kq * 8);
-        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+    for (int base = 0; base < n_keys; base += NB * KPI) {
+      uint4 kk[NB], vv[NB];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = Act<ACT>::unpack2(uw[i]);
-          o8[2 * i] += p * f.x;
-          o8[2 * i + 1] += p * f.y;
+      for (int i = 0; i < NB; ++i) {
+        const int j = base + i * KPI + kr;
+        if (j < n_keys) {
+          kk[i] = *reinterpret_cast<const uint4*>(Kc + (size_t)(lo + j) * D + kq * 8);
+          vv[i] = *reinterpret_cast<const uint4*>(Vc + (size_t)(lo + j) * D + kq * 8);
+        } else {
+          kk[i] = make_uint4(0u, 0u, 0u, 0u);
+          vv[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-    }
+      float s[NB];
+      float bm = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ored[kr * D + kq * 8 + i] = o8[i];
+      for (int i = 0; i < NB; ++i) {
+        const uint32_t kw[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
+        float d = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float2 f = Act<ACT>::unpack2(kw[w]);
+          d += f.x * qv[2 * w] + f.y * qv[2 * w + 1];
+        }
+#pragma unroll
+        for (int o = LPK / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        s[i] = (base + i * KPI + kr < n_keys) ? d : -INFINITY;
+        bm = fmaxf(bm, s[i]);
+      }
+      const float m_new = fmaxf(m, bm);
+      const float scale = (m_new == -INFINITY) ? 1.f : exp2f(m - m_new);
+      l *= scale;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o8[i] *= scale;
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        const float p = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_new);
+        l += p;
+        const uint32_t vw[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float2 f = Act<ACT>::unpack2(vw[w]);
+          o8[2 * w] += p * f.x;
+          o8[2 * w + 1] += p * f.y;
+        }
+      }
+      m = m_new;
+    }
+    // Merge the key groups of this CTA.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) og[kr * D + kq * 8 + i] = o8[i];
+    if (kq == 0) {
+      mg[kr] = m;
+      lg[kr] = l;
+    }
     __syncthreads();
     if (tid < D) {
-      float o = 0.f;
+      float M = -INFINITY;
 #pragma unroll
-      for (int r = 0; r < KPI; ++r) o += ored[r * D + tid];
-      dst[tid] = o;
+      for (int r = 0; r < KPI; ++r) M = fmaxf(M, mg[r]);
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < KPI; ++r) {
+          const float w = exp2f(mg[r] - M);
+          L += w * lg[r];
+          O += w * og[r * D + tid];
+        }
+      }
+      part[t * (D + 2) + tid] = O;
+      if (tid == 0) {
+        part[t * (D + 2) + D] = M;
+        part[t * (D + 2) + D + 1] = L;
+      }
     }
-    if (tid == 0) {
-      dst[D] = m;
-      dst[D + 1] = red[4] + red[5] + red[6] + red[7];
-    }
-    __syncthreads();  // sc / ored / red reused by the next token
+    __syncthreads();
   }
 
-  // Merge the splits of (b, h): the last CTA to arrive does it.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&a.counters[b * a.heads + h], 1);
-    *flag = (prev == a.nsplit - 1);
-  }
-  __syncthreads();
-  if (*flag) {
-    __threadfence();
-    float* wsm = red;  // [nsplit] merge weights (nsplit <= 32)
+  // Merge the CTAs of the cluster in rank 0 (distributed shared memory).
+  cluster_sync_all();
+  if (sp == 0) {
     for (int t = 0; t < a.T; ++t) {
-      const float* base = a.part + ((size_t)(b * a.T + t) * a.heads + h) * a.nsplit * (D + 2);
-      if (warp == 0) {
-        const float ms = lane < a.nsplit ? ld_cg(base + lane * (D + 2) + D) : -INFINITY;
-        const float ls = lane < a.nsplit ? ld_cg(base + lane * (D + 2) + D + 1) : 0.f;
-        const float mx = warp_max(ms);
-        const float w = lane < a.nsplit ? exp2f(ms - mx) : 0.f;
-        const float lsum = warp_sum(w * ls);
-        if (lane < a.nsplit) wsm[lane] = w / lsum;
-      }
-      __syncthreads();
       if (tid < D) {
-        float O = 0.f;
-#pragma unroll 8
-        for (int s2 = 0; s2 < a.nsplit; ++s2) O += wsm[s2] * ld_cg(base + s2 * (D + 2) + tid);
-        a.out[(size_t)(b * a.T + t) * a.H + h * D + tid] = O;
+        const float* pt = part + t * (D + 2);
+        float Mr[kAttnMaxSplit];
+        float M = -INFINITY;
+        for (int r = 0; r < nsplit; ++r) {
+          Mr[r] = ld_cluster(pt + D, (uint32_t)r);
+          M = fmaxf(M, Mr[r]);
+        }
+        float L = 0.f, O = 0.f;
+        for (int r = 0; r < nsplit; ++r) {
+          const float w = (Mr[r] == -INFINITY) ? 0.f : exp2f(Mr[r] - M);
+          L += w * ld_cluster(pt + D + 1, (uint32_t)r);
+          O += w * ld_cluster(pt + tid, (uint32_t)r);
+        }
+        a.out[(size_t)(b * a.T + t) * a.H + h * D + tid] = O / L;
       }
-      __syncthreads();
     }
-    if (tid == 0) a.counters[b * a.heads + h] = 0;
   }
+  cluster_sync_all();  // rank 0 has read every CTA's shared memory
 }
 
 int attn_nsplit(int B, int heads, int max_len, int num_sms) {
   const int bh = B * heads;
   int ns = (2 * num_sms + bh - 1) / bh;
   if (ns < 1) ns = 1;
-  if (ns > 32) ns = 32;
+  if (ns > kAttnMaxSplit) ns = kAttnMaxSplit;
   const int cap = (max_len + 15) / 16;  // at least ~16 keys per split
   if (ns > cap) ns = cap < 1 ? 1 : cap;
   return ns;
 }
 
-size_t attn_smem_bytes(int head_dim, int chunk_cap) {
+size_t attn_smem_bytes(int head_dim, int tokens) {
   const int kpi = kAttnThreads / (head_dim / 8);
-  return sizeof(float) * ((size_t)chunk_cap + (size_t)kpi * head_dim + 32) + 16;
+  return sizeof(float) * ((size_t)kpi * head_dim + 2 * kpi + (size_t)tokens * (head_dim + 2));
 }
 
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl) {
@@ -211,11 +225,15 @@ cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, boo
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = a.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl ? 2 : 1;
   if (ak == ActKind::F16) {
     if (a.head_dim == 64) return cudaLaunchKernelEx(&cfg, attn_decode_kernel<__half, 64>, a);
     if (a.head_dim == 128) return cudaLaunchKernelEx(&cfg, attn_decode_kernel<__half, 128>, a);
@@ -228,8 +246,8 @@ cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, boo
 
 cudaError_t prepare_attention_kernels(int max_smem) {
   cudaError_t e = cudaSuccess;
-#define DS_PREP_ATTN(T, D)                                                                   \
-  if (e == cudaSuccess)                                                                      \
+#define DS_PREP_ATTN(T, D)                                                                            \
+  if (e == cudaSuccess)                                                                               \
     e = cudaFuncSetAttribute(attn_decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                              max_smem)
   DS_PREP_ATTN(__half, 64);

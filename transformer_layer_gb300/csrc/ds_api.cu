@@ -97,7 +97,6 @@ namespace {
 
 struct Plans {
   GemvPlan qkv, o, up, down;
-  int nsplit_max = 1;
 };
 
 bool make_plans(const ds_layer& L, int M, int B, Plans* p) {
@@ -108,15 +107,13 @@ bool make_plans(const ds_layer& L, int M, int B, Plans* p) {
   if (!gemv_make_plan(wk, ak, H, H, M, L.sms, L.ctas_per_sm, L.max_smem, &p->o)) return false;
   if (!gemv_make_plan(wk, ak, F, H, M, L.sms, L.ctas_per_sm, L.max_smem, &p->up)) return false;
   if (!gemv_make_plan(wk, ak, H, F, M, L.sms, L.ctas_per_sm, L.max_smem, &p->down)) return false;
-  p->nsplit_max = attn_nsplit(B, L.cfg.heads, 1 << 30, L.sms);
   return true;
 }
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t status, cnt_gemv, cnt_attn, q, o, x1, g, stats_a, stats_b, partials, attn_part, act,
-      total;
+  size_t status, cnt_gemv, q, o, x1, g, stats_a, stats_b, partials, act, total;
 };
 
 // Workspace regions, each 256-byte aligned.  Counters first so that a
@@ -134,7 +131,6 @@ WsLayout ws_layout(const ds_layer& L, int B, int T, const Plans& p) {
   w.status = take(256);
   const size_t tiles_max = (size_t)std::max(3 * H, F) / 16;
   w.cnt_gemv = take(tiles_max * sizeof(int));
-  w.cnt_attn = take((size_t)B * nh * sizeof(int));
   w.q = take(M * H * 4);
   w.o = take(M * H * 4);
   w.x1 = take(M * H * 4);
@@ -146,7 +142,6 @@ WsLayout ws_layout(const ds_layer& L, int B, int T, const Plans& p) {
   for (int i = 0; i < 4; ++i)
     part = std::max(part, (size_t)ps[i]->tiles * ps[i]->KS * ps[i]->maxc * 16 * M * 4);
   w.partials = take(part);
-  w.attn_part = take(M * nh * (size_t)p.nsplit_max * (d + 2) * 4);
   w.act = take(2 * M * H * 2);
   w.total = off;
   return w;
@@ -178,8 +173,7 @@ ds_status validate_config(const ds_layer_config* c) {
 struct Bufs {
   unsigned* status;
   int* cnt_gemv;
-  int* cnt_attn;
-  float *q, *o, *x1, *g, *stats_a, *stats_b, *partials, *attn_part;
+  float *q, *o, *x1, *g, *stats_a, *stats_b, *partials;
   char* act;
 };
 
@@ -188,7 +182,6 @@ Bufs bufs_of(void* ws, const WsLayout& w) {
   Bufs r;
   r.status = reinterpret_cast<unsigned*>(b + w.status);
   r.cnt_gemv = reinterpret_cast<int*>(b + w.cnt_gemv);
-  r.cnt_attn = reinterpret_cast<int*>(b + w.cnt_attn);
   r.q = reinterpret_cast<float*>(b + w.q);
   r.o = reinterpret_cast<float*>(b + w.o);
   r.x1 = reinterpret_cast<float*>(b + w.x1);
@@ -196,7 +189,6 @@ Bufs bufs_of(void* ws, const WsLayout& w) {
   r.stats_a = reinterpret_cast<float*>(b + w.stats_a);
   r.stats_b = reinterpret_cast<float*>(b + w.stats_b);
   r.partials = reinterpret_cast<float*>(b + w.partials);
-  r.attn_part = reinterpret_cast<float*>(b + w.attn_part);
   r.act = b + w.act;
   return r;
 }
@@ -270,13 +262,9 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   ra.max_len = max_len;
   ra.H = H;
   ra.nsplit = attn_nsplit(B, nh, max_len, L.sms);
-  ra.chunk_cap = (max_len + ra.nsplit - 1) / ra.nsplit;
   ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  ra.smem = attn_smem_bytes(d, ra.chunk_cap);
-  ra.part = bf.attn_part;
-  ra.counters = bf.cnt_attn;
+  ra.smem = attn_smem_bytes(d, T);
   ra.out = bf.o;
-  ra.status = bf.status;
   if ((e = record(es, st)) != cudaSuccess) return e;
   if ((e = launch_attention(ak, ra, st, pdl)) != cudaSuccess) return e;
   if ((e = record(es, st)) != cudaSuccess) return e;
@@ -350,11 +338,9 @@ ds_status check_forward_args(const void* x_in, const void* x_out, int batch, int
   return DS_OK;
 }
 
-ds_status check_attn_smem(const ds_layer& L, int B, int max_len) {
-  const int ns = attn_nsplit(B, L.cfg.heads, max_len, L.sms);
-  const int cap = (max_len + ns - 1) / ns;
-  if (attn_smem_bytes(L.cfg.hidden / L.cfg.heads, cap) > (size_t)L.max_smem)
-    return fail(DS_ERR_UNSUPPORTED, "max_len too large for the attention kernel's shared memory");
+ds_status check_attn_smem(const ds_layer& L, int T) {
+  if (attn_smem_bytes(L.cfg.hidden / L.cfg.heads, T) > (size_t)L.max_smem)
+    return fail(DS_ERR_UNSUPPORTED, "too many new tokens for the attention kernel's shared memory");
   return DS_OK;
 }
 
@@ -465,7 +451,7 @@ ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out, int b
   ds_status s = check_forward_args(x_in, x_out, batch, new_tokens, k_cache, v_cache, max_len,
                                    past_len, workspace);
   if (s != DS_OK) return s;
-  if ((s = check_attn_smem(*layer, batch, max_len)) != DS_OK) return s;
+  if ((s = check_attn_smem(*layer, new_tokens)) != DS_OK) return s;
   Plans p;
   if (!make_plans(*layer, batch * new_tokens, batch, &p))
     return fail(DS_ERR_UNSUPPORTED, "no GEMV work split for this shape");
@@ -561,7 +547,7 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
     if (s != DS_OK) return s;
   }
   const ds_layer& L0 = *stack->layers[0];
-  ds_status s = check_attn_smem(L0, batch, max_len);
+  ds_status s = check_attn_smem(L0, 1);
   if (s != DS_OK) return s;
   Plans p;
   if (!make_plans(L0, batch, batch, &p)) return fail(DS_ERR_UNSUPPORTED, "no GEMV work split for this shape");

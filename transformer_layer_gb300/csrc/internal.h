@@ -82,14 +82,10 @@ struct AttnArgs {
   const void* v_cache = nullptr;
   const int32_t* past_len = nullptr;
   int B = 1, T = 1, heads = 0, head_dim = 0, max_len = 0, H = 0;
-  int nsplit = 1;
-  int chunk_cap = 0;                // keys per split the smem was sized for
+  int nsplit = 1;                   // CTAs per (b, h), one thread-block cluster (<= 8)
   float scale_log2 = 0.f;           // log2(e) / sqrt(head_dim)
   size_t smem = 0;
-  float* part = nullptr;            // [B*T][nh][nsplit][d + 2]
-  int* counters = nullptr;          // [B][nh]
   float* out = nullptr;             // [B*T][H] fp32
-  unsigned* status = nullptr;
 };
 
 // Chooses the work split for one GEMV; returns false if no valid split exists.
@@ -102,7 +98,7 @@ cudaError_t launch_region(Region r, WKind wk, ActKind ak, const RegionArgs& a,
 cudaError_t prepare_region_kernels(int max_smem);
 
 int attn_nsplit(int B, int heads, int max_len, int num_sms);
-size_t attn_smem_bytes(int head_dim, int chunk_cap);
+size_t attn_smem_bytes(int head_dim, int tokens);
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl);
 cudaError_t prepare_attention_kernels(int max_smem);
 
