@@ -24,17 +24,19 @@ static int fail(const char* what, int N, int K, int M, int G, int a, int b) {
   return 1;
 }
 
-static int check(int N, int K, int M, int G0, bool i8, bool split) {
+static int check(int N, int K, int M, int G0, bool i8, bool split, bool fixed = false) {
   const int blk_k = i8 ? 64 : 32, pad = i8 ? 8 : 32;
   auto xs = [&](int K_S) { return (size_t)(split ? 2 : 1) * M * (K_S + pad) * 2; };
   GemvPlan P;
-  if (!ws_make_plan(N, K, M, G0, blk_k, 8, 80 * 1024, xs, &P)) return 0;  // shape not supported
+  if (!ws_make_plan(N, K, M, G0, blk_k, 8, 80 * 1024, xs, &P, fixed)) return 0;  // shape not supported
   const int G = P.grid, C = P.C, tiles = P.tiles;
-  if (P.R > 0 && P.R < G) return fail("fewer leftover chunks than CTAs", N, K, M, G, (int)P.R, G);
+  if (fixed && G != G0) return fail("fixed grid not kept", N, K, M, G, G0, 0);
+  if (!fixed && P.R > 0 && P.R < G) return fail("fewer leftover chunks than CTAs", N, K, M, G, (int)P.R, G);
   std::map<std::tuple<int, int, int>, int> cover;
   std::map<int, std::vector<std::pair<int, int>>> parts;  // tile -> (slice, slot)
   for (int cta = 0; cta < G; ++cta) {
-    const long long ra = (long long)cta * P.R / G, rb = (long long)(cta + 1) * P.R / G;
+    long long ra, rb;
+    ws_left_range(P, cta, G, &ra, &rb);
     const int dp_b = cta * P.q;
     const int nch = (int)(rb - ra) + P.q * C;
     // streaming warps
@@ -106,6 +108,8 @@ int main() {
             bad |= check(H, H, M, G, i8, split);
             bad |= check(F, H, M, G, i8, split);
             bad |= check(H, F, M, G, i8, split);
+            bad |= check(3 * H, H, M, G, i8, split, true);   // persistent step kernel: grid fixed
+            bad |= check(H, F, M, G, i8, split, true);
           }
   // Pseudo-random shapes and grid sizes.
   unsigned x = 12345u;
@@ -117,6 +121,7 @@ int main() {
     const int M = 1 + rnd(64);
     const int G = 1 + rnd(400);
     bad |= check(N, K, M, G, i8, rnd(2));
+    bad |= check(N, K, M, G, i8, rnd(2), true);
   }
   if (!bad) std::printf("ok\n");
   return bad;

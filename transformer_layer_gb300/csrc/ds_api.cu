@@ -12,6 +12,7 @@
 // workspace layout, the per-GEMV work split, the launch chain with
 // programmatic dependent launch, CUDA-graph capture/replay of a stack step,
 // and per-region event timing in profile mode.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
@@ -43,7 +44,8 @@ bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr
 struct DevInfo {
   bool ready = false;
   int sms = 0;
-  int max_smem = 0;
+  int max_smem = 0;     // opt-in shared memory of one block
+  int smem_per_sm = 0;  // shared memory of one SM (shared by its resident blocks)
 };
 std::mutex g_dev_mu;
 DevInfo g_dev[64];
@@ -61,10 +63,14 @@ ds_status device_info(int* dev_out, DevInfo* out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
     e = cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(max smem)");
+    e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem per SM)");
     e = prepare_region_kernels(d.max_smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(region kernels)");
     e = prepare_attention_kernels(d.max_smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention kernel)");
+    e = prepare_step_kernels(d.max_smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(step kernel)");
     d.ready = true;
   }
   *dev_out = dev;
@@ -79,6 +85,15 @@ int ctas_per_sm_knob() {
   return (v >= 1 && v <= 4) ? v : 1;
 }
 
+// A stack step runs as the chain of region kernels (graph-captured, PDL
+// overlapped); DS_STEP_KERNEL=1 selects the persistent step kernel instead
+// where it can run (one cooperative launch per step; measured slower on
+// GB300, kept for comparison).
+bool step_kernel_knob() {
+  const char* s = std::getenv("DS_STEP_KERNEL");
+  return s != nullptr && std::atoi(s) != 0;
+}
+
 WKind wkind(ds_dtype d) { return d == DS_I8 ? WKind::I8 : (d == DS_BF16 ? WKind::BF16 : WKind::F16); }
 ActKind akind(ds_dtype d) { return d == DS_BF16 ? ActKind::BF16 : ActKind::F16; }
 
@@ -90,30 +105,52 @@ struct ds_layer {
   int device = 0;
   int sms = 0;
   int max_smem = 0;
+  int smem_per_sm = 0;
   int ctas_per_sm = 1;
+  // TMA tensor maps in device memory, kTensorMapBytes each: weights of QKV,
+  // O-proj, FFN-up, FFN-down, then (int8) their scales in the same order, one
+  // map per k-blocks-per-step choice (1, 2, 4): a map's box is one chunk.
+  unsigned char* tmaps = nullptr;
+  static int nblk_index(int nblk) { return nblk == 4 ? 2 : (nblk == 2 ? 1 : 0); }
+  const void* tmap_w(int r, int nblk) const { return tmaps + (size_t)(3 * r + nblk_index(nblk)) * kTensorMapBytes; }
+  const void* tmap_s(int r, int nblk) const {
+    return cfg.weight_dtype == DS_I8 ? tmaps + (size_t)(12 + 3 * r + nblk_index(nblk)) * kTensorMapBytes : nullptr;
+  }
 };
 
 namespace {
 
 struct Plans {
-  GemvPlan qkv, o, up, down;
+  GemvPlan qkv, o, up, down;  // region kernels (ds_layer_forward, profile mode)
+  GemvPlan step[4];           // persistent step kernel: one CTA per SM for every phase
+  bool step_ok = false;
 };
 
 bool make_plans(const ds_layer& L, int M, int B, Plans* p) {
+  (void)B;
   const int H = L.cfg.hidden, F = L.cfg.ffn;
   const WKind wk = wkind(L.cfg.weight_dtype);
   const ActKind ak = akind(L.cfg.act_dtype);
-  if (!gemv_make_plan(wk, ak, 3 * H, H, M, L.sms, L.ctas_per_sm, L.max_smem, &p->qkv)) return false;
-  if (!gemv_make_plan(wk, ak, H, H, M, L.sms, L.ctas_per_sm, L.max_smem, &p->o)) return false;
-  if (!gemv_make_plan(wk, ak, F, H, M, L.sms, L.ctas_per_sm, L.max_smem, &p->up)) return false;
-  if (!gemv_make_plan(wk, ak, H, F, M, L.sms, L.ctas_per_sm, L.max_smem, &p->down)) return false;
+  // Several CTAs per SM share its shared memory (1 KB of it reserved per CTA).
+  const int cps = L.ctas_per_sm;
+  const int smem = cps == 1 ? L.max_smem : std::min(L.max_smem, L.smem_per_sm / cps - 1024);
+  if (!gemv_make_plan(wk, ak, 3 * H, H, M, L.sms, cps, smem, &p->qkv)) return false;
+  if (!gemv_make_plan(wk, ak, H, H, M, L.sms, cps, smem, &p->o)) return false;
+  if (!gemv_make_plan(wk, ak, F, H, M, L.sms, cps, smem, &p->up)) return false;
+  if (!gemv_make_plan(wk, ak, H, F, M, L.sms, cps, smem, &p->down)) return false;
+  const int NK[4][2] = {{3 * H, H}, {H, H}, {F, H}, {H, F}};
+  p->step_ok = true;
+  for (int i = 0; i < 4; ++i)
+    if (!gemv_make_plan(wk, ak, NK[i][0], NK[i][1], M, L.sms, 1, L.max_smem, &p->step[i], true))
+      p->step_ok = false;
   return true;
 }
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t status, cnt_gemv, q, o, x1, g, stats_a, stats_b, partials, act, total;
+  size_t status, cnt_gemv, grid_bar, attn_cnt, q, o, x1, g, stats_a, stats_b, partials, attn_part, act,
+      total;
 };
 
 // Workspace regions, each 256-byte aligned.  Counters first so that a
@@ -131,6 +168,8 @@ WsLayout ws_layout(const ds_layer& L, int B, int T, const Plans& p) {
   w.status = take(256);
   const size_t tiles_max = (size_t)std::max(3 * H, F) / 16;
   w.cnt_gemv = take(tiles_max * sizeof(int));
+  w.grid_bar = take(sizeof(unsigned));
+  w.attn_cnt = take((size_t)B * nh * sizeof(int));
   w.q = take(M * H * 4);
   w.o = take(M * H * 4);
   w.x1 = take(M * H * 4);
@@ -139,9 +178,13 @@ WsLayout ws_layout(const ds_layer& L, int B, int T, const Plans& p) {
   w.stats_b = take((size_t)(H / 16) * M * 2 * 4);
   size_t part = 0;
   const GemvPlan* ps[4] = {&p.qkv, &p.o, &p.up, &p.down};
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 4; ++i) {
     part = std::max(part, (size_t)ps[i]->tiles * ps[i]->KS * ps[i]->maxc * 16 * M * 4);
+    const GemvPlan& q = p.step[i];
+    if (p.step_ok) part = std::max(part, (size_t)q.tiles * q.KS * q.maxc * 16 * M * 4);
+  }
   w.partials = take(part);
+  w.attn_part = take((size_t)B * nh * step_attn_nsplit(B, nh, 1 << 30, L.sms) * (d + 2) * 4);
   w.act = take(2 * M * H * 2);
   w.total = off;
   return w;
@@ -173,7 +216,9 @@ ds_status validate_config(const ds_layer_config* c) {
 struct Bufs {
   unsigned* status;
   int* cnt_gemv;
-  float *q, *o, *x1, *g, *stats_a, *stats_b, *partials;
+  unsigned* grid_bar;
+  int* attn_cnt;
+  float *q, *o, *x1, *g, *stats_a, *stats_b, *partials, *attn_part;
   char* act;
 };
 
@@ -182,6 +227,9 @@ Bufs bufs_of(void* ws, const WsLayout& w) {
   Bufs r;
   r.status = reinterpret_cast<unsigned*>(b + w.status);
   r.cnt_gemv = reinterpret_cast<int*>(b + w.cnt_gemv);
+  r.grid_bar = reinterpret_cast<unsigned*>(b + w.grid_bar);
+  r.attn_cnt = reinterpret_cast<int*>(b + w.attn_cnt);
+  r.attn_part = reinterpret_cast<float*>(b + w.attn_part);
   r.q = reinterpret_cast<float*>(b + w.q);
   r.o = reinterpret_cast<float*>(b + w.o);
   r.x1 = reinterpret_cast<float*>(b + w.x1);
@@ -209,7 +257,8 @@ cudaError_t record(EventSink* es, cudaStream_t st) {
 cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, const void* x_in,
                           void* x_out, int B, int T, void* kc, void* vc, int max_len,
                           const int32_t* past_len, const float* stats_in, float* stats_out,
-                          int32_t* seq_inc, cudaStream_t st, bool pdl, EventSink* es) {
+                          int32_t* seq_inc, const ds_layer* next, cudaStream_t st, bool pdl,
+                          EventSink* es) {
   const ds_layer_config& c = L.cfg;
   const int H = c.hidden, F = c.ffn, nh = c.heads, d = H / nh, M = B * T;
   const WKind wk = wkind(c.weight_dtype);
@@ -229,7 +278,12 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   // R1: LayerNorm1 + QKV + bias + KV append
   RegionArgs r1 = base;
   r1.W = L.w.w_qkv;
+  r1.tmap_w = L.tmap_w(0, P.qkv.nblk);
+  r1.tmap_s = L.tmap_s(0, P.qkv.nblk);
   r1.Wscale = static_cast<const __half*>(L.w.s_qkv);
+  r1.next_tmap_w = L.tmap_w(1, P.o.nblk);
+  r1.next_tmap_s = L.tmap_s(1, P.o.nblk);
+  r1.next_plan = P.o;
   r1.N = 3 * H;
   r1.K = H;
   r1.plan = P.qkv;
@@ -272,7 +326,12 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   // R3: O-proj + bias + residual + LayerNorm2 statistics
   RegionArgs r3 = base;
   r3.W = L.w.w_o;
+  r3.tmap_w = L.tmap_w(1, P.o.nblk);
+  r3.tmap_s = L.tmap_s(1, P.o.nblk);
   r3.Wscale = static_cast<const __half*>(L.w.s_o);
+  r3.next_tmap_w = L.tmap_w(2, P.up.nblk);
+  r3.next_tmap_s = L.tmap_s(2, P.up.nblk);
+  r3.next_plan = P.up;
   r3.N = H;
   r3.K = H;
   r3.plan = P.o;
@@ -288,7 +347,12 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   // R4a: LayerNorm2 + FFN-up + bias + GeLU
   RegionArgs r4 = base;
   r4.W = L.w.w_fc1;
+  r4.tmap_w = L.tmap_w(2, P.up.nblk);
+  r4.tmap_s = L.tmap_s(2, P.up.nblk);
   r4.Wscale = static_cast<const __half*>(L.w.s_fc1);
+  r4.next_tmap_w = L.tmap_w(3, P.down.nblk);
+  r4.next_tmap_s = L.tmap_s(3, P.down.nblk);
+  r4.next_plan = P.down;
   r4.N = F;
   r4.K = H;
   r4.plan = P.up;
@@ -305,7 +369,14 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   // R4b: FFN-down + bias + residual (+ next LayerNorm statistics)
   RegionArgs r5 = base;
   r5.W = L.w.w_fc2;
+  r5.tmap_w = L.tmap_w(3, P.down.nblk);
+  r5.tmap_s = L.tmap_s(3, P.down.nblk);
   r5.Wscale = static_cast<const __half*>(L.w.s_fc2);
+  if (next != nullptr) {
+    r5.next_tmap_w = next->tmap_w(0, P.qkv.nblk);
+    r5.next_tmap_s = next->tmap_s(0, P.qkv.nblk);
+    r5.next_plan = P.qkv;
+  }
   r5.N = H;
   r5.K = F;
   r5.plan = P.down;
@@ -341,6 +412,42 @@ ds_status check_forward_args(const void* x_in, const void* x_out, int batch, int
 ds_status check_attn_smem(const ds_layer& L, int T) {
   if (attn_smem_bytes(L.cfg.hidden / L.cfg.heads, T) > (size_t)L.max_smem)
     return fail(DS_ERR_UNSUPPORTED, "too many new tokens for the attention kernel's shared memory");
+  return DS_OK;
+}
+
+// Encodes the layer's TMA tensor maps on the host and copies them to device
+// memory owned by the layer (freed by ds_layer_destroy).
+ds_status make_tensor_maps(ds_layer* L) {
+  const ds_layer_config& c = L->cfg;
+  const int H = c.hidden, F = c.ffn;
+  const size_t esz = (c.weight_dtype == DS_I8) ? 1 : 2;
+  const void* W[4] = {L->w.w_qkv, L->w.w_o, L->w.w_fc1, L->w.w_fc2};
+  const void* Sc[4] = {L->w.s_qkv, L->w.s_o, L->w.s_fc1, L->w.s_fc2};
+  const int rows[4] = {3 * H, H, F, H};
+  const int cols[4] = {H, H, H, F};
+  const bool i8 = (c.weight_dtype == DS_I8);
+  const int nmaps = i8 ? 24 : 12;
+  std::vector<unsigned char> host((size_t)nmaps * kTensorMapBytes, 0);
+  const int blk_k = i8 ? 64 : 32;  // k per 16-byte lane load
+  for (int r = 0; r < 4; ++r) {
+    // a chunk is 8 warps x nb blocks of blk_k weights (8 nb blk_k esz bytes per row)
+    for (int i = 0, nb = 1; i < 3; ++i, nb *= 2) {
+      if (cols[r] % (8 * nb * blk_k) != 0) continue;  // no chunk of this width
+      if (!encode_weight_map(host.data() + (size_t)(3 * r + i) * kTensorMapBytes, W[r], rows[r],
+                             (size_t)cols[r] * esz, (int)(8 * nb * blk_k * esz)))
+        return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+      if (i8 && !encode_scale_map(host.data() + (size_t)(12 + 3 * r + i) * kTensorMapBytes, Sc[r], rows[r],
+                                  cols[r] / 64, 8 * nb))
+        return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a scale matrix");
+    }
+  }
+  int cur = 0;
+  cudaGetDevice(&cur);
+  cudaError_t e = cudaSetDevice(L->device);
+  if (e == cudaSuccess) e = cudaMalloc(&L->tmaps, host.size());
+  if (e == cudaSuccess) e = cudaMemcpy(L->tmaps, host.data(), host.size(), cudaMemcpyHostToDevice);
+  cudaSetDevice(cur);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor map upload");
   return DS_OK;
 }
 
@@ -415,17 +522,30 @@ ds_status ds_layer_create(const ds_layer_config* cfg, const ds_layer_weights* w,
   L->device = dev;
   L->sms = di.sms;
   L->max_smem = di.max_smem;
+  L->smem_per_sm = di.smem_per_sm;
   L->ctas_per_sm = ctas_per_sm_knob();
   Plans p;
   if (!make_plans(*L, 1, 1, &p)) {
     delete L;
     return fail(DS_ERR_UNSUPPORTED, "no GEMV work split for this shape");
   }
+  s = make_tensor_maps(L);
+  if (s != DS_OK) {
+    delete L;
+    return s;
+  }
   *out = L;
   return DS_OK;
 }
 
 ds_status ds_layer_destroy(ds_layer* layer) {
+  if (layer != nullptr && layer->tmaps != nullptr) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(layer->device);
+    cudaFree(layer->tmaps);
+    cudaSetDevice(cur);
+  }
   delete layer;
   return DS_OK;
 }
@@ -459,7 +579,7 @@ ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out, int b
   if (ws_bytes < wl.total) return fail(DS_ERR_WORKSPACE, "workspace smaller than ds_layer_workspace_bytes()");
   const Bufs bf = bufs_of(workspace, wl);
   cudaError_t e = enqueue_layer(*layer, p, bf, x_in, x_out, batch, new_tokens, k_cache, v_cache,
-                                max_len, past_len, nullptr, nullptr, nullptr,
+                                max_len, past_len, nullptr, nullptr, nullptr, nullptr,
                                 static_cast<cudaStream_t>(stream), true, nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "region kernel launch");
   g_launches += 5;
@@ -516,6 +636,75 @@ size_t ds_stack_workspace_bytes(const ds_stack* stack, int batch) {
 
 namespace {
 
+// Arguments of the persistent step kernel; false when it cannot run this
+// configuration (too many layers, no ring geometry, or not co-resident).
+bool build_step_args(const ds_stack* S, const Plans& p, const Bufs& bf, const void* x_in, void* x_out, int B,
+                     void* const* kc, void* const* vc, int max_len, int32_t* seq, StepArgs* a) {
+  const int L = (int)S->layers.size();
+  if (!p.step_ok || L > kStepMaxLayers || !step_kernel_knob()) return false;
+  const ds_layer& L0 = *S->layers[0];
+  const ds_layer_config& c = L0.cfg;
+  const WKind wk = wkind(c.weight_dtype);
+  const ActKind ak = akind(c.act_dtype);
+  a->L = L;
+  a->B = B;
+  a->H = c.hidden;
+  a->F = c.ffn;
+  a->heads = c.heads;
+  a->head_dim = c.hidden / c.heads;
+  a->max_len = max_len;
+  a->eps = c.ln_eps;
+  a->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a->head_dim));
+  a->nsplit = step_attn_nsplit(B, c.heads, max_len, L0.sms);
+  for (int i = 0; i < 4; ++i) a->plan[i] = p.step[i];
+  if (!step_geometry(wk, ak, B, L0.max_smem, a)) return false;
+  if (step_blocks_per_sm(wk, ak, a->plan[0].nt, step_smem_bytes(a->plan[0].nt, a->stages, a->SB, a->xs_cap)) < 1)
+    return false;
+  a->x_in = x_in;
+  a->x_out = x_out;
+  a->seq = seq;
+  a->status = bf.status;
+  a->counters = bf.cnt_gemv;
+  a->grid_bar = bf.grid_bar;
+  a->attn_cnt = bf.attn_cnt;
+  a->q = bf.q;
+  a->o = bf.o;
+  a->x1 = bf.x1;
+  a->g = bf.g;
+  a->stats_a = bf.stats_a;
+  a->stats_b = bf.stats_b;
+  a->partials = bf.partials;
+  a->attn_part = bf.attn_part;
+  a->act = bf.act;
+  for (int l = 0; l < L; ++l) {
+    const ds_layer_weights& w = S->layers[l]->w;
+    StepLayer& y = a->layer[l];
+    y.w[0] = w.w_qkv;
+    y.w[1] = w.w_o;
+    y.w[2] = w.w_fc1;
+    y.w[3] = w.w_fc2;
+    y.sc[0] = static_cast<const __half*>(w.s_qkv);
+    y.sc[1] = static_cast<const __half*>(w.s_o);
+    y.sc[2] = static_cast<const __half*>(w.s_fc1);
+    y.sc[3] = static_cast<const __half*>(w.s_fc2);
+    y.bias[0] = w.b_qkv;
+    y.bias[1] = w.b_o;
+    y.bias[2] = w.b_fc1;
+    y.bias[3] = w.b_fc2;
+    y.ln1_g = w.ln1_g;
+    y.ln1_b = w.ln1_b;
+    y.ln2_g = w.ln2_g;
+    y.ln2_b = w.ln2_b;
+    y.kc = kc[l];
+    y.vc = vc[l];
+    for (int r = 0; r < 4; ++r) {
+      y.tmap_w[r] = S->layers[l]->tmap_w(r, p.step[r].nblk);
+      y.tmap_s[r] = S->layers[l]->tmap_s(r, p.step[r].nblk);
+    }
+  }
+  return true;
+}
+
 cudaError_t enqueue_stack(ds_stack* S, const Plans& p, const Bufs& bf, const void* x_in, void* x_out,
                           int B, void* const* kc, void* const* vc, int max_len, int32_t* seq,
                           cudaStream_t st, bool pdl, EventSink* es) {
@@ -527,7 +716,8 @@ cudaError_t enqueue_stack(ds_stack* S, const Plans& p, const Bufs& bf, const voi
     const float* sin = (l == 0) ? nullptr : bf.stats_b;
     float* sout = (l == L - 1) ? nullptr : bf.stats_b;
     cudaError_t e = enqueue_layer(*S->layers[l], p, bf, xi, xo, B, 1, kc[l], vc[l], max_len, seq, sin,
-                                  sout, (l == L - 1) ? seq : nullptr, st, pdl, es);
+                                  sout, (l == L - 1) ? seq : nullptr, (l + 1 < L) ? S->layers[l + 1] : nullptr,
+                                  st, pdl, es);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -583,16 +773,29 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
     return DS_OK;
   }
 
+  // Default path: one persistent, cooperative launch for the whole step;
+  // otherwise the chain of region kernels.
+  static thread_local StepArgs step_args;  // ~10 KB: kept off the call stack
+  const bool use_step = build_step_args(stack, p, bf, x_in, x_out, batch, k_caches, v_caches, max_len,
+                                        seq_len, &step_args);
+  const WKind swk = wkind(L0.cfg.weight_dtype);
+  const ActKind sak = akind(L0.cfg.act_dtype);
+  auto enqueue = [&]() -> cudaError_t {
+    if (use_step) return launch_step(swk, sak, step_args, L0.sms, st);
+    return enqueue_stack(stack, p, bf, x_in, x_out, batch, k_caches, v_caches, max_len, seq_len, st, true,
+                         nullptr);
+  };
+  const int launched = use_step ? 1 : kernels;
+
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (st != nullptr) {
     cudaError_t e = cudaStreamIsCapturing(st, &cs);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
   }
   if (st == nullptr || cs != cudaStreamCaptureStatusNone) {
-    cudaError_t e = enqueue_stack(stack, p, bf, x_in, x_out, batch, k_caches, v_caches, max_len,
-                                  seq_len, st, true, nullptr);
-    if (e != cudaSuccess) return cuda_fail(e, "region kernel launch");
-    g_launches += kernels;
+    cudaError_t e = enqueue();
+    if (e != cudaSuccess) return cuda_fail(e, use_step ? "step kernel launch" : "region kernel launch");
+    g_launches += launched;
     return DS_OK;
   }
 
@@ -613,8 +816,7 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
     stack->have_graph = false;
     cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamBeginCapture");
-    cudaError_t el = enqueue_stack(stack, p, bf, x_in, x_out, batch, k_caches, v_caches, max_len,
-                                   seq_len, st, true, nullptr);
+    cudaError_t el = enqueue();
     cudaGraph_t graph = nullptr;
     e = cudaStreamEndCapture(st, &graph);
     if (el != cudaSuccess) {
@@ -630,7 +832,7 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
     }
     stack->key = key;
     stack->have_graph = true;
-    stack->graph_kernels = kernels;
+    stack->graph_kernels = launched;
   }
   cudaError_t e = cudaGraphLaunch(stack->exec, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");

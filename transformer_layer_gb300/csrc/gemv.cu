@@ -34,7 +34,7 @@ static size_t fixed_nt(int nt, int M, int K_S, int pad, bool split) {
 }
 
 bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int ctas_per_sm,
-                    int max_smem, GemvPlan* plan) {
+                    int max_smem, GemvPlan* plan, bool fixed_grid) {
   const bool i8 = (wk == WKind::I8);
   const int blk_k = i8 ? 64 : 32;
   const int pad = i8 ? 8 : 32;
@@ -42,16 +42,17 @@ bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int 
   const bool split = (ak == ActKind::BF16);
   const int nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
   auto xs = [&](int K_S) { return xs_bytes_nt(nt, M, K_S, pad, split); };
-  if (!ws_make_plan(N, K, M, num_sms * ctas_per_sm, blk_k, kProducers, kXBudget, xs, plan)) return false;
+  if (!ws_make_plan(N, K, M, num_sms * ctas_per_sm, blk_k, kProducers, kXBudget, xs, plan, fixed_grid))
+    return false;
   // As deep a weight ring as the rest of shared memory allows (up to kMaxStages).
   const size_t fixed = fixed_nt(plan->nt, M, plan->K_S, pad, split);
   const size_t stage = SmemLayout<1>::stage_bytes(plan->chunk_k, esize, i8) + 16;
-  if ((size_t)max_smem <= fixed) return false;
-  size_t s = ((size_t)max_smem - fixed) / stage;
+  if ((size_t)max_smem <= fixed + 1024) return false;
+  size_t s = ((size_t)max_smem - fixed - 1024) / stage;
   if (s > (size_t)kMaxStages) s = kMaxStages;
   if (s < 2) return false;
   plan->stages = (int)s;
-  plan->smem = fixed + s * stage;
+  plan->smem = 1024 + fixed + s * stage;  // + alignment of the ring to 1024 bytes
   return true;
 }
 

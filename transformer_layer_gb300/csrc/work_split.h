@@ -1,5 +1,5 @@
 // Work split of the skinny-GEMM region kernels, shared by the host planner,
-// the device kernels and the CPU replay test (tests/work_split_check.cu).
+// the device kernels and the CPU replay test (tests/work_split_check.cpp).
 //
 // Page cited as [P1]: "DeepSpeed Inference 内核优化深度解析：多 GPU 自适应并行、
 // 算子融合推理内核与 MoQ 量化支持", §3 intro (a skinny GEMM scheduled so that ops
@@ -29,13 +29,29 @@
 
 namespace ds {
 
-// The CTA whose leftover range holds leftover chunk i.
-DS_HD int ws_cta_of(long long i, long long R, int G) { return (int)(((i + 1) * (long long)G - 1) / R); }
+// a / b for a >= 0, b > 0: the 32-bit divide whenever both fit (always, for
+// the shapes this library takes), which is far shorter code on the GPU.
+DS_HD long long ws_div(long long a, long long b) {
+  if ((((unsigned long long)a | (unsigned long long)b) >> 32) == 0) return (long long)((unsigned)a / (unsigned)b);
+  return a / b;
+}
 
-// Number of CTAs contributing to unit u (every CTA owns >= 1 leftover chunk
-// whenever R > 0, so the contributors of a leftover unit are consecutive).
+// The CTA whose leftover range holds leftover chunk i.
+DS_HD int ws_cta_of(long long i, long long R, int G) { return (int)ws_div((i + 1) * (long long)G - 1, R); }
+
+// CTA cta's range [ra, rb) of leftover chunks.
+DS_HD void ws_left_range(const GemvPlan& P, int cta, int G, long long* ra, long long* rb) {
+  *ra = ws_div((long long)cta * P.R, G);
+  *rb = ws_div((long long)(cta + 1) * P.R, G);
+}
+
+// Number of CTAs contributing to unit u.  With at least as many leftover
+// chunks as CTAs every CTA owns >= 1 of them and a unit's contributors are
+// consecutive CTAs; with fewer (a fixed grid larger than the work) every CTA
+// owns at most one, so each chunk of a unit has its own CTA.
 DS_HD int ws_unit_contrib(int u, const GemvPlan& P, int G) {
   if (u < P.U_dp) return 1;
+  if (P.R < G) return P.C;
   const long long first = (long long)(u - P.U_dp) * P.C;
   return ws_cta_of(first + P.C - 1, P.R, G) - ws_cta_of(first, P.R, G) + 1;
 }
@@ -55,8 +71,9 @@ struct Cursor {
 
 DS_HD void ws_cursor_init(Cursor& q, const GemvPlan& P, long long ra, long long rb, int dp_b) {
   if (rb > ra) {
-    const long long u = P.U_dp + ra / P.C;
-    q.kc = (int)(ra % P.C);
+    const long long uq = ws_div(ra, P.C);
+    const long long u = P.U_dp + uq;
+    q.kc = (int)(ra - uq * P.C);
     q.s = (int)(u / P.tiles);
     q.t = (int)(u - (long long)q.s * P.tiles);
     q.rem_left = (int)(rb - ra);
@@ -97,32 +114,39 @@ DS_HD bool ws_segment_ends(const Cursor& q, const GemvPlan& P, int j, int nchunk
 // the unit's contributors.
 DS_HD void ws_leftover_segment(const GemvPlan& P, long long i, long long rb, int cta, int G, int* u,
                                long long* end, int* j_slot) {
-  const long long uo = i / P.C;
+  const long long uo = ws_div(i, P.C);
   *end = (uo + 1) * P.C < rb ? (uo + 1) * P.C : rb;
   *u = (int)(P.U_dp + uo);
-  *j_slot = cta - ws_cta_of(uo * P.C, P.R, G);
+  *j_slot = (P.R < G) ? (int)(i - uo * P.C) : cta - ws_cta_of(uo * P.C, P.R, G);
 }
 
 // Host planner: the longest K slice whose staged x fits `x_budget` bytes, then
 // q whole units per CTA and the leftover units' chunks spread evenly.
 // xs_bytes(K_S) gives the staged-x bytes for a slice length.
+// fixed_grid: use exactly num_ctas CTAs even when there is less work (the
+// persistent step kernel has one CTA per SM for every phase); CTAs may then
+// own no chunk of this GEMV.
 template <typename XsBytes>
 inline bool ws_make_plan(int N, int K, int M, int num_ctas, int blk_k, int warps, size_t x_budget,
-                         XsBytes xs_bytes, GemvPlan* plan) {
+                         XsBytes xs_bytes, GemvPlan* plan, bool fixed_grid = false) {
   if (N <= 0 || K <= 0 || M < 1 || M > 64 || (N % 16) != 0 || num_ctas < 1) return false;
   GemvPlan p;
   p.nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
-  p.nblk = (K % (warps * 2 * blk_k) == 0) ? 2 : 1;
-  p.chunk_k = warps * p.nblk * blk_k;
-  if (K % p.chunk_k != 0) return false;
+  // k-blocks per warp step: as many as K allows, up to 4 (more bytes per
+  // ring handshake), then the longest K slice whose staged x fits the budget.
   p.tiles = N / 16;
-  const int nck = K / p.chunk_k;
   p.K_S = 0;
-  for (int d = 1; d <= nck; ++d) {
-    if (nck % d != 0) continue;
-    if (xs_bytes(K / d) <= x_budget) {
-      p.K_S = K / d;
-      break;
+  for (int nb = 4; nb >= 1 && p.K_S == 0; nb /= 2) {
+    if (K % (warps * nb * blk_k) != 0) continue;
+    p.nblk = nb;
+    p.chunk_k = warps * nb * blk_k;
+    const int nck = K / p.chunk_k;
+    for (int d = 1; d <= nck; ++d) {
+      if (nck % d != 0) continue;
+      if (xs_bytes(K / d) <= x_budget) {
+        p.K_S = K / d;
+        break;
+      }
     }
   }
   if (p.K_S == 0) return false;
@@ -131,7 +155,7 @@ inline bool ws_make_plan(int N, int K, int M, int num_ctas, int blk_k, int warps
   p.units = p.KS * p.tiles;
   const long long total = (long long)p.units * p.C;
   long long G = num_ctas;
-  if (G > total) G = total;
+  if (G > total && !fixed_grid) G = total;
   p.grid = (int)G;
   p.q = p.units / p.grid;
   // Every CTA must own at least one leftover chunk when there are any (so the
