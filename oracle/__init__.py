@@ -10,8 +10,7 @@ states what one pre-LN GPT-style layer computes, region by region, as the page
 "DeepSpeed Inference 内核优化深度解析：多 GPU 自适应并行、算子融合推理内核与
 MoQ 量化支持" describes it (§3 "面向 Transformer 块的定制化推理内核", §3.2
 "一个 Transformer 层中的四大融合区域", and §5.2 for the int8 weights).  The
-pages print no formula, so each function names the reading it takes; the
-readings are listed once more in the design doc of the repository.
+pages print no formula, so each function names the reading it takes.
 
 Modules
 -------
