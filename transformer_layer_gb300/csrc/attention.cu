@@ -16,15 +16,17 @@
 //
 // GB300 design (not the pages'): a layer has only nh (20-40) heads at batch
 // 1, far fewer than 152 SMs, so each (b, h) is split along the keys over a
-// thread-block cluster of `nsplit` (<= 8) CTAs.  A CTA loads the K and V rows
-// of its keys together (16-byte loads; a key's d values spread over d/8 lanes
-// and reduced with warp shuffles) and keeps a running max / sum / p.V per lane
-// group (online softmax, log2 domain), so there is one pass over the keys and
-// no score buffer.  The groups of a CTA merge in shared memory, and the CTAs
-// of the cluster merge through distributed shared memory in rank 0: no
-// global partials, no atomics.  Before griddepcontrol.wait a CTA asks the TMA
-// unit to prefetch into L2 the cache rows that the previous kernel does not
-// write.
+// thread-block cluster of `nsplit` (<= 8) CTAs.  Before griddepcontrol.wait a
+// CTA copies the cached K and V rows of its keys that the previous kernel
+// does not write (positions < past_len) into shared memory with two TMA bulk
+// copies, so that once the QKV kernel completes only q and the new rows come
+// from global memory.  A key's d values are spread over d/8 lanes (16-byte
+// loads) and reduced with warp shuffles; each lane group keeps a running
+// max / sum / p.V (online softmax, log2 domain): one pass over the keys, no
+// score buffer.  The groups of a CTA merge in shared memory; every CTA of the
+// cluster then stores its (O, M, L) into rank 0's shared memory (distributed
+// shared memory), and rank 0 merges them locally: no global partials, no
+// atomics, no remote loads.
 #include <math.h>
 
 #include "common.cuh"
@@ -39,32 +41,48 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
                    : "memory");
 }
-// Reads a float from the shared memory of CTA `rank` of this cluster, at the
+
+// Stores a float into the shared memory of CTA `rank` of this cluster, at the
 // same offset as `local` in this CTA.
-__device__ __forceinline__ float ld_cluster(const float* local, uint32_t rank) {
+__device__ __forceinline__ void st_cluster(float* local, uint32_t rank, float v) {
   uint32_t addr;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(addr) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(v) : "memory");
 }
+
+// Shared-memory carve-up (floats, then the staged K and V rows, then one
+// mbarrier): og [KPI][D] per-group p.V, mg / lg [KPI] per-group max and sum,
+// part [D + 2] this CTA's (O, M, L), mrg [8][D + 2] the cluster's partials
+// (used in rank 0), Ks / Vs [stage_keys][D].
+__host__ __device__ inline size_t attn_floats(int D) {
+  const int kpi = kAttnThreads / (D / 8);
+  return (size_t)kpi * D + 2 * kpi + (size_t)(1 + kAttnMaxSplit) * (D + 2);
+}
+__host__ __device__ inline size_t attn_stage_offset(int D) { return (attn_floats(D) * 4 + 127) & ~(size_t)127; }
 
 template <typename ACT, int D>
 __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs a) {
   constexpr int LPK = D / 8;               // lanes per key (16 B each)
   constexpr int KPI = kAttnThreads / LPK;  // key groups per CTA (keys per pass)
   constexpr int NB = 8;                    // passes whose K and V loads are in flight together
-  extern __shared__ __align__(16) float sm[];
-  float* og = sm;                // [KPI][D] per-group unnormalised p.V
-  float* mg = og + KPI * D;      // [KPI] per-group running max (log2 domain)
-  float* lg = mg + KPI;          // [KPI] per-group running sum
-  float* part = lg + KPI;        // [T][D + 2] this CTA's (O[D], M, L) per token
+  extern __shared__ __align__(128) float sm[];
+  float* og = sm;
+  float* mg = og + KPI * D;
+  float* lg = mg + KPI;
+  float* part = lg + KPI;
+  float* mrg = part + (D + 2);
+  ACT* Ks = reinterpret_cast<ACT*>(reinterpret_cast<unsigned char*>(sm) + attn_stage_offset(D));
+  ACT* Vs = Ks + (size_t)a.stage_keys * D;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Vs + (size_t)a.stage_keys * D);
 
   const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;  // sp = rank in the cluster
   const int nsplit = gridDim.x;
   const int tid = threadIdx.x;
   const int kq = tid % LPK, kr = tid / LPK;
 
+  // past_len is only changed by the last kernel of a stack step, which has
+  // completed before this step's first kernel starts (that one is launched
+  // without programmatic overlap), so it may be read before the wait.
   const int past = a.past_len[b];
   int S_all = past + a.T;
   if (S_all > a.max_len) S_all = a.max_len;
@@ -75,16 +93,30 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   const size_t head_row0 = ((size_t)b * a.heads + h) * a.max_len;
   const ACT* Kc = static_cast<const ACT*>(a.k_cache) + head_row0 * D;
   const ACT* Vc = static_cast<const ACT*>(a.v_cache) + head_row0 * D;
+  // Keys [lo, lo + n_st) are cached rows nobody writes during this step.
+  const int n_st = max(0, min(min(hi, past) - lo, a.stage_keys));
 
   if (tid == 0) {
+    mbar_init(smem_u32(bar), 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (tid == 0 && n_st > 0) {
+    const uint32_t bytes = (uint32_t)(n_st * D * sizeof(ACT));
+    const uint64_t pol = l2_evict_first_policy();
+    mbar_arrive_expect_tx(smem_u32(bar), 2 * bytes);
+    bulk_g2s(smem_u32(Ks), Kc + (size_t)lo * D, bytes, smem_u32(bar), pol);
+    bulk_g2s(smem_u32(Vs), Vc + (size_t)lo * D, bytes, smem_u32(bar), pol);
+    // rows past the staging budget: into L2
     const int pe = min(hi, past);
-    if (pe > lo) {
-      prefetch_l2_bulk(Kc + (size_t)lo * D, (uint32_t)((pe - lo) * D * sizeof(ACT)));
-      prefetch_l2_bulk(Vc + (size_t)lo * D, (uint32_t)((pe - lo) * D * sizeof(ACT)));
+    if (pe > lo + n_st) {
+      prefetch_l2_bulk(Kc + (size_t)(lo + n_st) * D, (uint32_t)((pe - lo - n_st) * D * sizeof(ACT)));
+      prefetch_l2_bulk(Vc + (size_t)(lo + n_st) * D, (uint32_t)((pe - lo - n_st) * D * sizeof(ACT)));
     }
   }
   pdl_wait();
   pdl_launch_dependents();
+  if (n_st > 0) mbar_wait(smem_u32(bar), 0, a.status);
 
   for (int t = 0; t < a.T; ++t) {
     const int St = min(past + t + 1, S_all);
@@ -107,8 +139,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
       for (int i = 0; i < NB; ++i) {
         const int j = base + i * KPI + kr;
         if (j < n_keys) {
-          kk[i] = *reinterpret_cast<const uint4*>(Kc + (size_t)(lo + j) * D + kq * 8);
-          vv[i] = *reinterpret_cast<const uint4*>(Vc + (size_t)(lo + j) * D + kq * 8);
+          // staged rows from shared memory, the rest (new rows) from global
+          const ACT* kp = (j < n_st) ? Ks + (size_t)j * D : Kc + (size_t)(lo + j) * D;
+          const ACT* vp = (j < n_st) ? Vs + (size_t)j * D : Vc + (size_t)(lo + j) * D;
+          kk[i] = *reinterpret_cast<const uint4*>(kp + kq * 8);
+          vv[i] = *reinterpret_cast<const uint4*>(vp + kq * 8);
         } else {
           kk[i] = make_uint4(0u, 0u, 0u, 0u);
           vv[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -149,7 +184,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
       }
       m = m_new;
     }
-    // Merge the key groups of this CTA.
+    // Merge the key groups of this CTA, then push (O, M, L) to rank 0.
 #pragma unroll
     for (int i = 0; i < 8; ++i) og[kr * D + kq * 8 + i] = o8[i];
     if (kq == 0) {
@@ -170,38 +205,28 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
           O += w * og[r * D + tid];
         }
       }
-      part[t * (D + 2) + tid] = O;
+      float* slot = mrg + sp * (D + 2);
+      st_cluster(slot + tid, 0, O);
       if (tid == 0) {
-        part[t * (D + 2) + D] = M;
-        part[t * (D + 2) + D + 1] = L;
+        st_cluster(slot + D, 0, M);
+        st_cluster(slot + D + 1, 0, L);
       }
     }
-    __syncthreads();
-  }
-
-  // Merge the CTAs of the cluster in rank 0 (distributed shared memory).
-  cluster_sync_all();
-  if (sp == 0) {
-    for (int t = 0; t < a.T; ++t) {
-      if (tid < D) {
-        const float* pt = part + t * (D + 2);
-        float Mr[kAttnMaxSplit];
-        float M = -INFINITY;
-        for (int r = 0; r < nsplit; ++r) {
-          Mr[r] = ld_cluster(pt + D, (uint32_t)r);
-          M = fmaxf(M, Mr[r]);
-        }
-        float L = 0.f, O = 0.f;
-        for (int r = 0; r < nsplit; ++r) {
-          const float w = (Mr[r] == -INFINITY) ? 0.f : exp2f(Mr[r] - M);
-          L += w * ld_cluster(pt + D + 1, (uint32_t)r);
-          O += w * ld_cluster(pt + tid, (uint32_t)r);
-        }
-        a.out[(size_t)(b * a.T + t) * a.H + h * D + tid] = O / L;
+    cluster_sync_all();  // every CTA's partial is in rank 0; og/mg/lg free again
+    if (sp == 0 && tid < D) {
+      float M = -INFINITY;
+      for (int r = 0; r < nsplit; ++r) M = fmaxf(M, mrg[r * (D + 2) + D]);
+      float L = 0.f, O = 0.f;
+      for (int r = 0; r < nsplit; ++r) {
+        const float mr = mrg[r * (D + 2) + D];
+        const float w = (mr == -INFINITY) ? 0.f : exp2f(mr - M);
+        L += w * mrg[r * (D + 2) + D + 1];
+        O += w * mrg[r * (D + 2) + tid];
       }
+      a.out[(size_t)(b * a.T + t) * a.H + h * D + tid] = O / L;
     }
+    if (t + 1 < a.T) cluster_sync_all();  // rank 0 has read the partials before they are overwritten
   }
-  cluster_sync_all();  // rank 0 has read every CTA's shared memory
 }
 
 int attn_nsplit(int B, int heads, int max_len, int num_sms) {
@@ -214,9 +239,14 @@ int attn_nsplit(int B, int heads, int max_len, int num_sms) {
   return ns;
 }
 
-size_t attn_smem_bytes(int head_dim, int tokens) {
-  const int kpi = kAttnThreads / (head_dim / 8);
-  return sizeof(float) * ((size_t)kpi * head_dim + 2 * kpi + (size_t)tokens * (head_dim + 2));
+int attn_stage_keys(int head_dim, int max_len, int nsplit) {
+  const int per_split = (max_len + nsplit - 1) / nsplit;
+  const int budget = (48 * 1024) / (2 * head_dim * 2);  // K and V rows of 16-bit values
+  return per_split < budget ? per_split : budget;
+}
+
+size_t attn_smem_bytes(int head_dim, int stage_keys) {
+  return attn_stage_offset(head_dim) + (size_t)2 * stage_keys * head_dim * 2 + 16;
 }
 
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl) {

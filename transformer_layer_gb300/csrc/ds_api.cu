@@ -257,8 +257,8 @@ cudaError_t record(EventSink* es, cudaStream_t st) {
 cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, const void* x_in,
                           void* x_out, int B, int T, void* kc, void* vc, int max_len,
                           const int32_t* past_len, const float* stats_in, float* stats_out,
-                          int32_t* seq_inc, const ds_layer* next, cudaStream_t st, bool pdl,
-                          EventSink* es) {
+                          int32_t* seq_inc, const ds_layer* next, bool first, cudaStream_t st,
+                          bool pdl, EventSink* es) {
   const ds_layer_config& c = L.cfg;
   const int H = c.hidden, F = c.ffn, nh = c.heads, d = H / nh, M = B * T;
   const WKind wk = wkind(c.weight_dtype);
@@ -300,7 +300,9 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   r1.max_len = max_len;
   r1.past_len = past_len;
   if ((e = record(es, st)) != cudaSuccess) return e;
-  if ((e = launch_region(Region::LnQkv, wk, ak, r1, st, pdl)) != cudaSuccess) return e;
+  // The first kernel of an enqueue waits for everything before it (no
+  // programmatic overlap): later kernels may then read past_len early.
+  if ((e = launch_region(Region::LnQkv, wk, ak, r1, st, pdl && !first)) != cudaSuccess) return e;
   if ((e = record(es, st)) != cudaSuccess) return e;
 
   // R2: attention
@@ -317,8 +319,10 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   ra.H = H;
   ra.nsplit = attn_nsplit(B, nh, max_len, L.sms);
   ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  ra.smem = attn_smem_bytes(d, T);
+  ra.stage_keys = attn_stage_keys(d, max_len, ra.nsplit);
+  ra.smem = attn_smem_bytes(d, ra.stage_keys);
   ra.out = bf.o;
+  ra.status = bf.status;
   if ((e = record(es, st)) != cudaSuccess) return e;
   if ((e = launch_attention(ak, ra, st, pdl)) != cudaSuccess) return e;
   if ((e = record(es, st)) != cudaSuccess) return e;
@@ -410,8 +414,10 @@ ds_status check_forward_args(const void* x_in, const void* x_out, int batch, int
 }
 
 ds_status check_attn_smem(const ds_layer& L, int T) {
-  if (attn_smem_bytes(L.cfg.hidden / L.cfg.heads, T) > (size_t)L.max_smem)
-    return fail(DS_ERR_UNSUPPORTED, "too many new tokens for the attention kernel's shared memory");
+  (void)T;  // tokens are processed one after another: shared memory does not grow with T
+  const int d = L.cfg.hidden / L.cfg.heads;
+  if (attn_smem_bytes(d, attn_stage_keys(d, 1 << 30, 1)) > (size_t)L.max_smem)
+    return fail(DS_ERR_UNSUPPORTED, "attention kernel's shared memory exceeds the device limit");
   return DS_OK;
 }
 
@@ -579,7 +585,7 @@ ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out, int b
   if (ws_bytes < wl.total) return fail(DS_ERR_WORKSPACE, "workspace smaller than ds_layer_workspace_bytes()");
   const Bufs bf = bufs_of(workspace, wl);
   cudaError_t e = enqueue_layer(*layer, p, bf, x_in, x_out, batch, new_tokens, k_cache, v_cache,
-                                max_len, past_len, nullptr, nullptr, nullptr, nullptr,
+                                max_len, past_len, nullptr, nullptr, nullptr, nullptr, true,
                                 static_cast<cudaStream_t>(stream), true, nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "region kernel launch");
   g_launches += 5;
@@ -717,7 +723,7 @@ cudaError_t enqueue_stack(ds_stack* S, const Plans& p, const Bufs& bf, const voi
     float* sout = (l == L - 1) ? nullptr : bf.stats_b;
     cudaError_t e = enqueue_layer(*S->layers[l], p, bf, xi, xo, B, 1, kc[l], vc[l], max_len, seq, sin,
                                   sout, (l == L - 1) ? seq : nullptr, (l + 1 < L) ? S->layers[l + 1] : nullptr,
-                                  st, pdl, es);
+                                  l == 0, st, pdl, es);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

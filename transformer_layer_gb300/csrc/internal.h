@@ -103,8 +103,10 @@ struct AttnArgs {
   int B = 1, T = 1, heads = 0, head_dim = 0, max_len = 0, H = 0;
   int nsplit = 1;                   // CTAs per (b, h), one thread-block cluster (<= 8)
   float scale_log2 = 0.f;           // log2(e) / sqrt(head_dim)
+  int stage_keys = 0;               // cached keys per split copied to shared memory up front
   size_t smem = 0;
   float* out = nullptr;             // [B*T][H] fp32
+  unsigned* status = nullptr;       // workspace status word (wait-timeout flag)
 };
 
 // ---------------------------------------------------------------- step kernel
@@ -169,7 +171,10 @@ cudaError_t launch_region(Region r, WKind wk, ActKind ak, const RegionArgs& a,
 cudaError_t prepare_region_kernels(int max_smem);
 
 int attn_nsplit(int B, int heads, int max_len, int num_sms);
-size_t attn_smem_bytes(int head_dim, int tokens);
+// Shared memory of the attention kernel, and the cached keys per split it
+// stages there (all of a split's keys when they fit a 48 KB budget).
+size_t attn_smem_bytes(int head_dim, int stage_keys);
+int attn_stage_keys(int head_dim, int max_len, int nsplit);
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl);
 cudaError_t prepare_attention_kernels(int max_smem);
 
