@@ -31,7 +31,7 @@ static int check(int N, int K, int M, int G0, bool i8, bool split, bool fixed = 
   if (!ws_make_plan(N, K, M, G0, blk_k, 8, 80 * 1024, xs, &P, fixed)) return 0;  // shape not supported
   const int G = P.grid, C = P.C, tiles = P.tiles;
   if (fixed && G != G0) return fail("fixed grid not kept", N, K, M, G, G0, 0);
-  if (!fixed && P.R > 0 && P.R < G) return fail("fewer leftover chunks than CTAs", N, K, M, G, (int)P.R, G);
+  if (!fixed && !P.whole && P.R > 0 && P.R < G) return fail("fewer leftover chunks than CTAs", N, K, M, G, (int)P.R, G);
   std::map<std::tuple<int, int, int>, int> cover;
   std::map<int, std::vector<std::pair<int, int>>> parts;  // tile -> (slice, slot)
   for (int cta = 0; cta < G; ++cta) {

@@ -39,8 +39,14 @@ DS_HD long long ws_div(long long a, long long b) {
 // The CTA whose leftover range holds leftover chunk i.
 DS_HD int ws_cta_of(long long i, long long R, int G) { return (int)ws_div((i + 1) * (long long)G - 1, R); }
 
-// CTA cta's range [ra, rb) of leftover chunks.
+// CTA cta's range [ra, rb) of leftover chunks (whole units when P.whole).
 DS_HD void ws_left_range(const GemvPlan& P, int cta, int G, long long* ra, long long* rb) {
+  if (P.whole) {
+    const long long lu = ws_div(P.R, P.C);  // leftover units
+    *ra = ws_div((long long)cta * lu, G) * P.C;
+    *rb = ws_div((long long)(cta + 1) * lu, G) * P.C;
+    return;
+  }
   *ra = ws_div((long long)cta * P.R, G);
   *rb = ws_div((long long)(cta + 1) * P.R, G);
 }
@@ -50,7 +56,7 @@ DS_HD void ws_left_range(const GemvPlan& P, int cta, int G, long long* ra, long 
 // consecutive CTAs; with fewer (a fixed grid larger than the work) every CTA
 // owns at most one, so each chunk of a unit has its own CTA.
 DS_HD int ws_unit_contrib(int u, const GemvPlan& P, int G) {
-  if (u < P.U_dp) return 1;
+  if (u < P.U_dp || P.whole) return 1;
   if (P.R < G) return P.C;
   const long long first = (long long)(u - P.U_dp) * P.C;
   return ws_cta_of(first + P.C - 1, P.R, G) - ws_cta_of(first, P.R, G) + 1;
@@ -117,7 +123,7 @@ DS_HD void ws_leftover_segment(const GemvPlan& P, long long i, long long rb, int
   const long long uo = ws_div(i, P.C);
   *end = (uo + 1) * P.C < rb ? (uo + 1) * P.C : rb;
   *u = (int)(P.U_dp + uo);
-  *j_slot = (P.R < G) ? (int)(i - uo * P.C) : cta - ws_cta_of(uo * P.C, P.R, G);
+  *j_slot = P.whole ? 0 : (P.R < G) ? (int)(i - uo * P.C) : cta - ws_cta_of(uo * P.C, P.R, G);
 }
 
 // Host planner: the longest K slice whose staged x fits `x_budget` bytes, then
@@ -158,12 +164,25 @@ inline bool ws_make_plan(int N, int K, int M, int num_ctas, int blk_k, int warps
   if (G > total && !fixed_grid) G = total;
   p.grid = (int)G;
   p.q = p.units / p.grid;
+  p.whole = 0;
+  // Leftover units go whole to CTAs when that lengthens the busiest CTA by at
+  // most 3 chunks: a split-K fix-up costs global round trips (several us under
+  // the weight stream) that the short kernels cannot hide.
+  if (!fixed_grid) {
+    const long long lu = p.units - (long long)p.q * p.grid;
+    const long long whole_max = ((long long)p.q + (lu > 0 ? 1 : 0)) * p.C;
+    long long qs = p.q;
+    if (qs > 0 && lu * p.C > 0 && lu * p.C < p.grid) qs -= 1;
+    const long long rs = (p.units - qs * p.grid) * p.C;
+    const long long split_max = qs * p.C + (rs + p.grid - 1) / p.grid;
+    if (lu > 0 && whole_max - split_max <= 3) p.whole = 1;
+  }
   // Every CTA must own at least one leftover chunk when there are any (so the
   // CTAs sharing a leftover unit are consecutive, with no empty ranges in
   // between): with fewer leftover chunks than CTAs, hand one whole unit per
   // CTA back to the leftover pool.
   const long long left = (long long)(p.units - p.q * p.grid) * p.C;
-  if (p.q > 0 && left > 0 && left < p.grid) p.q -= 1;
+  if (!p.whole && p.q > 0 && left > 0 && left < p.grid) p.q -= 1;
   p.U_dp = p.q * p.grid;
   p.R = (long long)(p.units - p.U_dp) * p.C;
   p.maxc = 1;
