@@ -110,6 +110,41 @@ def test_full_width_layer_f16(H, nh, F, B):
         L.close()
 
 
+@pytest.mark.parametrize("act,B", [(torch.float16, 2), (torch.float16, 8), (torch.float16, 16),
+                                   (torch.float16, 32), (torch.float16, 64), (torch.bfloat16, 1),
+                                   (torch.bfloat16, 8), (torch.bfloat16, 64)])
+def test_skinny_gemm_sweep_layer(act, B):
+    """The batch-row sweep on one 4096-hidden layer (QKV, O-proj, FFN-up and
+    FFN-down with their fused epilogues): one to eight MMA column tiles, fp16
+    and bf16 (hi/lo operand split), every output element checked."""
+    H, nh, F = 4096, 32, 16384
+    L = DeviceLayer(H, nh, F, seed=1004, act_dtype=act, weight_dtype=act)
+    try:
+        past = [16 + (37 * b) % 600 for b in range(B)]
+        res = run_layer(L, B, 1, past, max_len=640, seed=11)
+        check_layer(L, res, B, 1, past, f"sweep {act} B={B}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("B", [1, 16])
+def test_int8_13b_shaped_layer(B):
+    """A 13B-shaped layer (hidden 5120, 40 heads, FFN 20480) with MoQ int8
+    group-64 weights quantised on the device, 1024 cached positions, batch 1
+    and 16: codes and scales bit-exact, layer output within tolerance."""
+    H, nh, F = 5120, 40, 20480
+    L = DeviceLayer(H, nh, F, seed=1005, weight_dtype=torch.int8)
+    try:
+        q, sc = oracle.quantize_int8(L.p["w_o"].cpu().numpy(), 64)
+        assert np.array_equal(L.codes["w_o"].cpu().numpy(), q)
+        assert np.array_equal(L.scales["w_o"].cpu().numpy().view(np.uint16), sc.view(np.uint16))
+        past = [1024 - 3 * b for b in range(B)]
+        res = run_layer(L, B, 1, past, max_len=1088, seed=12)
+        check_layer(L, res, B, 1, past, f"int8 13B B={B}")
+    finally:
+        L.close()
+
+
 def test_zero_weight_layer_is_identity():
     L = DeviceLayer(256, 4, 1024, seed=5)
     try:
