@@ -41,6 +41,15 @@ METRIC = "decode tokens/sec at batch 1 (7B-shaped fp16 stack); % of HBM roofline
 FALLBACK_HBM_GBS = 6800.0
 CYCLE = 64  # decode positions per pass over the cache
 
+# Stack shapes: hidden, heads, FFN, depth, cached positions, weight bytes per
+# weight (int8: one code byte + a 2-byte fp16 scale per group of 64).
+MODELS = {
+    "7b": dict(H=4096, nh=32, F=16384, layers=32, past=512, wbytes=2.0, wname="fp16",
+               title="7B-shaped GPT-style stack"),
+    "13b-int8": dict(H=5120, nh=40, F=20480, layers=40, past=1024, wbytes=1.0 + 2.0 / 64, wname="int8",
+                     title="13B-shaped GPT-style stack, MoQ int8 group-64 weights"),
+}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -49,20 +58,25 @@ def parse():
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--batch", type=int, default=1)
-    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--layers", type=int, default=None, help="default: the model's depth")
+    ap.add_argument("--model", default="7b", choices=sorted(MODELS),
+                    help="7b: the headline fp16 stack; 13b-int8: the MoQ int8 stack (no CPU baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=4)
     return ap.parse_args()
 
 
-def workload_config(B, layers):
+def workload_config(B, layers, model="7b"):
+    m = MODELS[model]
+    H, nh, F, past = m["H"], m["nh"], m["F"], m["past"]
+    gb = layers * layer_bytes(H, F, m["wbytes"]) / 1e9
     return {
-        "workload": f"7B-shaped GPT-style stack: {layers} pre-LN layers, hidden 4096, 32 heads "
-                    f"(head_dim 128), FFN 16384, GeLU(tanh), fp16 weights; batch {B}; KV cache "
-                    f"512 cached positions + 64 decode positions",
-        "batch": B, "layers": layers, "hidden": 4096, "heads": 32, "ffn": 16384,
-        "past": 512, "decode_positions": CYCLE,
-        "l2": "inputs larger than L2: 12.9 GB of weights streamed per step (L2 is 129 MB)",
+        "workload": f"{m['title']}: {layers} pre-LN layers, hidden {H}, {nh} heads "
+                    f"(head_dim {H // nh}), FFN {F}, GeLU(tanh), {m['wname']} weights; batch {B}; KV cache "
+                    f"{past} cached positions + {CYCLE} decode positions",
+        "batch": B, "layers": layers, "hidden": H, "heads": nh, "ffn": F,
+        "past": past, "decode_positions": CYCLE,
+        "l2": f"inputs larger than L2: {gb:.1f} GB of weights streamed per step (L2 is 129 MB)",
         "parallelism": "replicas",
     }
 
@@ -155,31 +169,31 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def layer_bytes(H, F):
+def layer_bytes(H, F, wbytes=2.0):
     n_w = 3 * H * H + H * H + F * H + H * F
     n_small = 3 * H + H + F + H + 4 * H
-    return 2 * n_w + 2 * n_small
+    return wbytes * n_w + 2 * n_small
 
 
-def step_bytes(H, F, layers, B, past, steps):
+def step_bytes(H, F, layers, B, past, steps, wbytes=2.0):
     """Average algorithmic bytes of one decode step over positions past..past+CYCLE-1:
     weights + biases + LN params, K/V read (S = past + 1 + i keys), K/V write."""
     kv = 0.0
     for i in range(steps):
         S = past + 1 + (i % CYCLE)
         kv += B * layers * 2 * S * H * 2 + B * layers * 2 * H * 2
-    return layers * layer_bytes(H, F) + kv / steps
+    return layers * layer_bytes(H, F, wbytes) + kv / steps
 
 
-def region_bytes(H, F, B, past):
+def region_bytes(H, F, B, past, wbytes=2.0):
     """Algorithmic bytes of one launch of each region kernel (weights + vectors in/out)."""
     S = past + 1 + CYCLE // 2
     return {
-        "ln_qkv": 3 * H * H * 2 + 3 * H * 2 + 4 * H + B * (H * 2 + H * 4 + 2 * H * 2),
+        "ln_qkv": 3 * H * H * wbytes + 3 * H * 2 + 4 * H + B * (H * 2 + H * 4 + 2 * H * 2),
         "attention": B * (2 * S * H * 2 + H * 4 + H * 4),
-        "oproj_res": H * H * 2 + 2 * H + B * (H * 4 + H * 2 + H * 4),
-        "ffn_up": F * H * 2 + 2 * F + 4 * H + B * (H * 4 + F * 4),
-        "ffn_down": H * F * 2 + 2 * H + B * (F * 4 + H * 4 + H * 2),
+        "oproj_res": H * H * wbytes + 2 * H + B * (H * 4 + H * 2 + H * 4),
+        "ffn_up": F * H * wbytes + 2 * F + 4 * H + B * (H * 4 + F * 4),
+        "ffn_down": H * F * wbytes + 2 * H + B * (F * 4 + H * 4 + H * 2),
     }
 
 
@@ -220,8 +234,9 @@ def run_reference(args):
     import numpy as np
     import oracle
     from transformer_layer_gb300 import inputs
-    B, layers = args.batch, args.layers
-    H, F, nh, d, past = 4096, 16384, 32, 128, 512
+    B = args.batch
+    layers = args.layers if args.layers is not None else MODELS["7b"]["layers"]
+    H, F, nh, d, past = 4096, 16384, 32, 128, 512   # the oracle arm times the 7B-shaped layer
     p = {k: v.numpy() for k, v in inputs.layer_params(H, F, 1002, 0, device="cpu").items()}
     kc, vc = inputs.kv_cache(B, nh, past + CYCLE, d, 1002, device="cpu")
     K0, V0 = kc.numpy(), vc.numpy()
@@ -275,8 +290,12 @@ def main():
     __graft_entry__.build()
     from transformer_layer_gb300 import ds, inputs
 
-    B, L = args.batch, args.layers
-    H, nh, F, d, past = 4096, 32, 16384, 128, 512
+    m = MODELS[args.model]
+    B = args.batch
+    L = args.layers if args.layers is not None else m["layers"]
+    H, nh, F, past, wbytes = m["H"], m["nh"], m["F"], m["past"], m["wbytes"]
+    d = H // nh
+    int8 = m["wname"] == "int8"
     max_len = past + CYCLE
     seed = 1002 + rank
     stream = torch.cuda.Stream(device=dev)
@@ -285,8 +304,16 @@ def main():
     layers, params, kcs, vcs = [], [], [], []
     for l in range(L):
         p = inputs.layer_params(H, F, seed, l, device=dev)
+        if int8:   # MoQ group-64 codes and fp16 scales, quantised on the device
+            for k, sk in (("w_qkv", "s_qkv"), ("w_o", "s_o"), ("w_fc1", "s_fc1"), ("w_fc2", "s_fc2")):
+                w = p[k]
+                q = torch.empty(w.shape, dtype=torch.int8, device=dev)
+                sc = torch.empty((w.shape[0], w.shape[1] // 64), dtype=torch.float16, device=dev)
+                ds.ds_quantize_int8(w, q, sc)
+                p[k], p[sk] = q, sc
+            torch.cuda.synchronize(dev)
         params.append(p)
-        layers.append(ds.ds_layer_create(H, nh, F, p, torch.float16, torch.float16))
+        layers.append(ds.ds_layer_create(H, nh, F, p, torch.float16, torch.int8 if int8 else torch.float16))
         k, v = inputs.kv_cache(B, nh, max_len, d, seed, l, device=dev)
         kcs.append(k)
         vcs.append(v)
@@ -370,30 +397,32 @@ def main():
     ds.ds_stack_set_profiling(stack, False)
 
     peak, peak_kind = load_peak()
-    rbytes = region_bytes(H, F, B, past)
+    rbytes = region_bytes(H, F, B, past, wbytes)
     shares = {r: us[i] for i, r in enumerate(REGIONS)}
     dom = max(("ffn_up", "ffn_down", "ln_qkv", "oproj_res"), key=lambda r: shares[r])
     dom_us = shares[dom]
     achieved = rbytes[dom] / (dom_us * 1e-6) / 1e9
-    sbytes = step_bytes(H, F, L, B, past, args.steps)
+    sbytes = step_bytes(H, F, L, B, past, args.steps, wbytes)
     step_gbs = sbytes / (ms_max / args.steps / 1000.0) / 1e9
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.model == "7b":
         v, cores, sample = cpu_baseline_sample(B, layers=L)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if args.model == "7b" else
+                  f"decode tokens/sec at batch {B} ({m['title']}); % of HBM roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded: weights N(0,0.02), biases N(0,0.01), LN gamma 1+N(0,0.1), "
                 "beta N(0,0.1), KV cache and inputs N(0,1))",
-        "config": workload_config(B, L),
+        "config": workload_config(B, L, args.model),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} HBM copy",
                      "bytes_per_launch": rbytes[dom], "us_per_launch": dom_us,
-                     "traffic": ncu_traffic(dom)},
+                     "traffic": ncu_traffic(dom) if args.model == "7b" and B == 1 else None},
         "step_roofline": {"bytes_per_step": sbytes, "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                           "frac": step_gbs / peak, "peak_source": f"{peak_kind} HBM copy"},
         "region_us": {r: shares[r] for r in REGIONS},
