@@ -48,6 +48,8 @@ MODELS = {
                title="7B-shaped GPT-style stack"),
     "13b-int8": dict(H=5120, nh=40, F=20480, layers=40, past=1024, wbytes=1.0 + 2.0 / 64, wname="int8",
                      title="13B-shaped GPT-style stack, MoQ int8 group-64 weights"),
+    "neo-2.7b": dict(H=2560, nh=20, F=10240, layers=32, past=128, wbytes=2.0, wname="fp16",
+                     title="GPT-Neo-2.7B-shaped stack"),
 }
 
 
@@ -60,7 +62,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--layers", type=int, default=None, help="default: the model's depth")
     ap.add_argument("--model", default="7b", choices=sorted(MODELS),
-                    help="7b: the headline fp16 stack; 13b-int8: the MoQ int8 stack (no CPU baseline)")
+                    help="7b: the headline fp16 stack; 13b-int8: the MoQ int8 stack; neo-2.7b: the "
+                         "GPT-Neo-2.7B-shaped fp16 stack (the last two without CPU baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=4)
     return ap.parse_args()
