@@ -64,18 +64,21 @@ def parse():
     ap.add_argument("--model", default="7b", choices=sorted(MODELS),
                     help="7b: the headline fp16 stack; 13b-int8: the MoQ int8 stack; neo-2.7b: the "
                          "GPT-Neo-2.7B-shaped fp16 stack (the last two without CPU baseline)")
+    ap.add_argument("--bf16", action="store_true",
+                    help="bf16 weights and activations (fp16 stacks only); default fp16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=4)
     return ap.parse_args()
 
 
-def workload_config(B, layers, model="7b"):
+def workload_config(B, layers, model="7b", wname=None):
     m = MODELS[model]
+    wname = wname or m["wname"]
     H, nh, F, past = m["H"], m["nh"], m["F"], m["past"]
     gb = layers * layer_bytes(H, F, m["wbytes"]) / 1e9
     return {
         "workload": f"{m['title']}: {layers} pre-LN layers, hidden {H}, {nh} heads "
-                    f"(head_dim {H // nh}), FFN {F}, GeLU(tanh), {m['wname']} weights; batch {B}; KV cache "
+                    f"(head_dim {H // nh}), FFN {F}, GeLU(tanh), {wname} weights; batch {B}; KV cache "
                     f"{past} cached positions + {CYCLE} decode positions",
         "batch": B, "layers": layers, "hidden": H, "heads": nh, "ffn": F,
         "past": past, "decode_positions": CYCLE,
@@ -299,6 +302,10 @@ def main():
     H, nh, F, past, wbytes = m["H"], m["nh"], m["F"], m["past"], m["wbytes"]
     d = H // nh
     int8 = m["wname"] == "int8"
+    if args.bf16 and int8:
+        raise SystemExit("--bf16 applies to the fp16 stacks")
+    act = torch.bfloat16 if args.bf16 else torch.float16
+    wname = "bf16" if args.bf16 else m["wname"]
     max_len = past + CYCLE
     seed = 1002 + rank
     stream = torch.cuda.Stream(device=dev)
@@ -306,7 +313,7 @@ def main():
     # ---- weights, caches, workspace (all resident in HBM before timing)
     layers, params, kcs, vcs = [], [], [], []
     for l in range(L):
-        p = inputs.layer_params(H, F, seed, l, device=dev)
+        p = inputs.layer_params(H, F, seed, l, dtype=act, device=dev)
         if int8:   # MoQ group-64 codes and fp16 scales, quantised on the device
             for k, sk in (("w_qkv", "s_qkv"), ("w_o", "s_o"), ("w_fc1", "s_fc1"), ("w_fc2", "s_fc2")):
                 w = p[k]
@@ -316,8 +323,8 @@ def main():
                 p[k], p[sk] = q, sc
             torch.cuda.synchronize(dev)
         params.append(p)
-        layers.append(ds.ds_layer_create(H, nh, F, p, torch.float16, torch.int8 if int8 else torch.float16))
-        k, v = inputs.kv_cache(B, nh, max_len, d, seed, l, device=dev)
+        layers.append(ds.ds_layer_create(H, nh, F, p, act, torch.int8 if int8 else act))
+        k, v = inputs.kv_cache(B, nh, max_len, d, seed, l, dtype=act, device=dev)
         kcs.append(k)
         vcs.append(v)
     stack = ds.ds_stack_create(layers)
@@ -327,8 +334,8 @@ def main():
     seq = torch.full((B,), past, dtype=torch.int32, device=dev)
     seq0 = seq.clone()
     n_x = 8
-    xs = [inputs.hidden(B, 1, H, seed, step=i, device=dev).reshape(B, H) for i in range(n_x)]
-    out = torch.empty(B, H, dtype=torch.float16, device=dev)
+    xs = [inputs.hidden(B, 1, H, seed, step=i, dtype=act, device=dev).reshape(B, H) for i in range(n_x)]
+    out = torch.empty(B, H, dtype=act, device=dev)
     torch.cuda.synchronize(dev)
 
     def step(i):
@@ -369,7 +376,7 @@ def main():
 
     # ---- end to end through the host-buffer entry point
     xh = [x.cpu().pin_memory() for x in xs]
-    yh = torch.empty(B, H, dtype=torch.float16).pin_memory()
+    yh = torch.empty(B, H, dtype=act).pin_memory()
     xd, yd = torch.empty_like(xs[0]), torch.empty_like(out)
     seq.copy_(seq0)
     torch.cuda.synchronize(dev)
@@ -409,23 +416,23 @@ def main():
     step_gbs = sbytes / (ms_max / args.steps / 1000.0) / 1e9
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.model == "7b":
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.model == "7b" and not args.bf16:
         v, cores, sample = cpu_baseline_sample(B, layers=L)
         cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
 
     line = {
-        "metric": METRIC if args.model == "7b" else
-                  f"decode tokens/sec at batch {B} ({m['title']}); % of HBM roofline",
+        "metric": METRIC if (args.model == "7b" and not args.bf16) else
+                  f"decode tokens/sec at batch {B} ({m['title']}, {wname}); % of HBM roofline",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if args.bf16 else "f16",
         "data": "synthetic (seeded: weights N(0,0.02), biases N(0,0.01), LN gamma 1+N(0,0.1), "
                 "beta N(0,0.1), KV cache and inputs N(0,1))",
-        "config": workload_config(B, L, args.model),
+        "config": workload_config(B, L, args.model, wname),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} HBM copy",
                      "bytes_per_launch": rbytes[dom], "us_per_launch": dom_us,
-                     "traffic": ncu_traffic(dom) if args.model == "7b" and B == 1 else None},
+                     "traffic": ncu_traffic(dom) if args.model == "7b" and B == 1 and not args.bf16 else None},
         "step_roofline": {"bytes_per_step": sbytes, "achieved": step_gbs, "peak": peak, "unit": "GB/s",
                           "frac": step_gbs / peak, "peak_source": f"{peak_kind} HBM copy"},
         "region_us": {r: shares[r] for r in REGIONS},
