@@ -232,6 +232,21 @@ def cpu_baseline_sample(B, budget_s=10.0, layers=32):
     return B / (per_layer * layers), cores, sample
 
 
+def max_over_ranks(x, world, device="cpu"):
+    """The largest value of x over the ranks (every rank receives it)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step, steps, world, seconds):
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank_step * steps * world / seconds
+
+
 def run_reference(args):
     """--impl reference: the float64 CPU oracle on this host's cores (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
@@ -368,11 +383,8 @@ def main():
     clocks = sampler.stop()
     launches = ds.ds_launch_count() - launches0
     ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = B * args.steps * world / (ms_max / 1000.0)
+    ms_max = max_over_ranks(ms, world, dev)
+    value = job_throughput(B, args.steps, world, ms_max / 1000.0)
 
     # ---- end to end through the host-buffer entry point
     xh = [x.cpu().pin_memory() for x in xs]
@@ -390,10 +402,7 @@ def main():
         ds.ds_stack_decode_host(stack, xh[i % n_x], yh, xd, yd, B, kcs, vcs, max_len, seq, ws, nbytes,
                                 stream)
     e2e_s = time.perf_counter() - t0
-    te = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = B * e2e_steps * world / float(te.item())
+    e2e_value = job_throughput(B, e2e_steps, world, max_over_ranks(e2e_s, world, dev))
 
     # ---- per-region kernel times (profile mode: no graph, no PDL; each kernel alone)
     ds.ds_stack_set_profiling(stack, True)
