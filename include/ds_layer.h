@@ -164,9 +164,12 @@ DS_API size_t ds_stack_workspace_bytes(const ds_stack* stack, int batch);
  *            is written at seq_len[b], and the step adds 1 to every entry on
  *            the device after the last layer has read it.
  * The launch sequence (5 kernels per layer, chained with programmatic
- * dependent launch) is captured into a CUDA graph on the first call with a
- * given argument set and replayed afterwards; when `stream` is the legacy
- * default stream or is already capturing, the kernels are launched directly. */
+ * dependent launch; the first kernel waits for all earlier work on `stream`)
+ * is captured into a CUDA graph on the first call with a given argument set
+ * and replayed afterwards; when `stream` is the legacy default stream or is
+ * already capturing, the kernels are launched directly.  With the environment
+ * variable DS_STEP_KERNEL=1 the step runs instead as one persistent,
+ * cooperative kernel where it can (same results within tolerance; slower). */
 DS_API ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, int batch,
                                void* const* k_caches, void* const* v_caches, int max_len,
                                int32_t* seq_len, void* workspace, size_t ws_bytes,
