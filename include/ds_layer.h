@@ -82,7 +82,7 @@ typedef struct {
   float ln_eps;        /* LayerNorm epsilon (1e-5 in every shipped workload)  */
   ds_dtype act_dtype;  /* DS_F16 or DS_BF16: hidden states, caches, biases, LN */
   ds_dtype weight_dtype; /* DS_F16 / DS_BF16 (must equal act_dtype) or DS_I8    */
-  int quant_group;     /* DS_I8 only: group length along K; must be 64        */
+  int quant_group;     /* DS_I8 only: group length along K, 64 or 128          */
 } ds_layer_config;
 
 /* Device pointers to one layer's parameters.  Vectors are in act_dtype.
@@ -197,7 +197,7 @@ DS_API ds_status ds_stack_set_profiling(ds_stack* stack, int enabled);
 DS_API ds_status ds_stack_region_times(ds_stack* stack, float us_out[5], int launches_out[5]);
 
 /* MoQ-style quantisation of a float16 weight matrix w_f16 [n][k] ([P1] §5.2):
- * per group of `group` (= 64) consecutive weights along k, scale
+ * per group of `group` (32, 64 or 128) consecutive weights along k, scale
  * s = fp16_rne(float32(max|w|) / 127) and code q = clamp(rne(w / s), -127, 127)
  * (IEEE float32 division); s = 0 and q = 0 for an all-zero group.
  * codes [n][k] int8 and scales_f16 [n][k/group] are written on `stream`. */

@@ -47,8 +47,9 @@ class DeviceLayer:
     the device with ds_quantize_int8 when weight_dtype is torch.int8)."""
 
     def __init__(self, hidden, heads, ffn, seed, layer=0, act_dtype=torch.float16,
-                 weight_dtype=torch.float16, device="cuda"):
+                 weight_dtype=torch.float16, device="cuda", quant_group=64):
         self.hidden, self.heads, self.ffn = hidden, heads, ffn
+        self.quant_group = quant_group
         self.act_dtype, self.weight_dtype = act_dtype, weight_dtype
         src_dtype = torch.float16 if weight_dtype == torch.int8 else act_dtype
         self.p = inputs.layer_params(hidden, ffn, seed, layer, dtype=src_dtype, device=device)
@@ -61,20 +62,22 @@ class DeviceLayer:
             for k, sk in (("w_qkv", "s_qkv"), ("w_o", "s_o"), ("w_fc1", "s_fc1"), ("w_fc2", "s_fc2")):
                 w = self.p[k]
                 q = torch.empty(w.shape, dtype=torch.int8, device=device)
-                s = torch.empty((w.shape[0], w.shape[1] // 64), dtype=torch.float16, device=device)
-                ds.ds_quantize_int8(w, q, s)
+                s = torch.empty((w.shape[0], w.shape[1] // quant_group), dtype=torch.float16, device=device)
+                ds.ds_quantize_int8(w, q, s, group=quant_group)
                 self.dev[k] = q
                 self.dev[sk] = s
                 self.codes[k], self.scales[k] = q, s
         torch.cuda.synchronize()
-        self.handle = ds.ds_layer_create(hidden, heads, ffn, self.dev, act_dtype, weight_dtype)
+        self.handle = ds.ds_layer_create(hidden, heads, ffn, self.dev, act_dtype, weight_dtype,
+                                         quant_group=quant_group)
 
     def oracle_params(self):
         """float64 copies of the weights the device uses (q * s for int8)."""
         out = {}
         for k, v in self.p.items():
             if self.weight_dtype == torch.int8 and k in self.codes:
-                out[k] = oracle.dequantize_int8(self.codes[k].cpu().numpy(), self.scales[k].cpu().numpy())
+                out[k] = oracle.dequantize_int8(self.codes[k].cpu().numpy(), self.scales[k].cpu().numpy(),
+                                                self.quant_group)
             else:
                 out[k] = to64(v)
         return out

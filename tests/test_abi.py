@@ -67,7 +67,9 @@ def _create(lib, **kw):
     (dict(ln_eps=0.0), ds.DS_ERR_INVALID_ARG),
     (dict(act_dtype=ds.DS_I8), ds.DS_ERR_INVALID_ARG),
     (dict(weight_dtype=ds.DS_BF16), ds.DS_ERR_UNSUPPORTED),
-    (dict(weight_dtype=ds.DS_I8, quant_group=32), ds.DS_ERR_UNSUPPORTED),
+    (dict(weight_dtype=ds.DS_I8, hidden=512, heads=4, ffn=1024, quant_group=96), ds.DS_ERR_UNSUPPORTED),
+    (dict(weight_dtype=ds.DS_I8, hidden=512, heads=4, ffn=1024, quant_group=32), ds.DS_ERR_UNSUPPORTED),
+    (dict(weight_dtype=ds.DS_I8, hidden=512, heads=4, ffn=1024, quant_group=128), ds.DS_ERR_UNSUPPORTED),
     (dict(weight_dtype=ds.DS_I8), ds.DS_ERR_UNSUPPORTED),  # int8 needs hidden % 512 == 0
     (dict(ffn=1000), ds.DS_ERR_UNSUPPORTED),
 ])
@@ -92,7 +94,7 @@ def test_null_arguments(lib):
         ds.DS_ERR_INVALID_ARG
     assert lib.ds_stack_decode_step(None, None, None, 1, None, None, 1, None, None, 0, None) == \
         ds.DS_ERR_INVALID_ARG
-    assert lib.ds_quantize_int8(C.c_void_p(4096), 4, 128, 32, C.c_void_p(4096), C.c_void_p(4096),
+    assert lib.ds_quantize_int8(C.c_void_p(4096), 4, 192, 96, C.c_void_p(4096), C.c_void_p(4096),
                                 None) == ds.DS_ERR_UNSUPPORTED
     assert lib.ds_quantize_int8(None, 4, 128, 64, None, None, None) == ds.DS_ERR_INVALID_ARG
     assert lib.ds_stack_set_profiling(None, 1) == ds.DS_ERR_INVALID_ARG

@@ -145,6 +145,39 @@ def test_int8_13b_shaped_layer(B):
         L.close()
 
 
+@pytest.mark.parametrize("group,act,B", [(128, torch.float16, 1), (128, torch.bfloat16, 6),
+                                         (128, torch.float16, 16)])
+def test_int8_group_lengths(group, act, B):
+    """A MoQ grouping other than 64 along K (groups of 128 codes): device codes
+    and scales bit-exact with the oracle's quantiser at that group length, and
+    the layer within tolerance of the oracle using q * s."""
+    H, nh, F = 1024, 8, 4096
+    L = DeviceLayer(H, nh, F, seed=1006, act_dtype=act, weight_dtype=torch.int8, quant_group=group)
+    try:
+        for k in ("w_qkv", "w_fc2"):
+            q, s = oracle.quantize_int8(L.p[k].cpu().numpy(), group)
+            assert np.array_equal(L.codes[k].cpu().numpy(), q)
+            assert np.array_equal(L.scales[k].cpu().numpy().view(np.uint16), s.view(np.uint16))
+        past = [40 + 11 * b for b in range(B)]
+        res = run_layer(L, B, 1, past, max_len=256, seed=13)
+        check_layer(L, res, B, 1, past, f"int8 g{group} {act} B={B}")
+    finally:
+        L.close()
+
+
+def test_quantizer_group32_bit_exact():
+    """ds_quantize_int8 with groups of 32 (the layer takes 64 and 128): codes
+    and scales bit-exact with the oracle's quantiser."""
+    w = inputs.layer_params(1024, 4096, 1007, device="cuda")["w_fc1"]
+    q = torch.empty(w.shape, dtype=torch.int8, device="cuda")
+    s = torch.empty((w.shape[0], w.shape[1] // 32), dtype=torch.float16, device="cuda")
+    ds.ds_quantize_int8(w, q, s, group=32)
+    torch.cuda.synchronize()
+    q0, s0 = oracle.quantize_int8(w.cpu().numpy(), 32)
+    assert np.array_equal(q.cpu().numpy(), q0)
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), s0.view(np.uint16))
+
+
 def test_zero_weight_layer_is_identity():
     L = DeviceLayer(256, 4, 1024, seed=5)
     try:

@@ -138,10 +138,16 @@ bool make_plans(const ds_layer& L, int M, int B, Plans* p) {
   if (!gemv_make_plan(wk, ak, H, H, M, L.sms, cps, smem, &p->o)) return false;
   if (!gemv_make_plan(wk, ak, F, H, M, L.sms, cps, smem, &p->up)) return false;
   if (!gemv_make_plan(wk, ak, H, F, M, L.sms, cps, smem, &p->down)) return false;
+  if (wk == WKind::I8) {  // the scale box of a chunk must hold at least 8 groups
+    const GemvPlan* pl[4] = {&p->qkv, &p->o, &p->up, &p->down};
+    for (const GemvPlan* q : pl)
+      if (q->chunk_k / L.cfg.quant_group < 8) return false;
+  }
   const int NK[4][2] = {{3 * H, H}, {H, H}, {F, H}, {H, F}};
   p->step_ok = true;
   for (int i = 0; i < 4; ++i)
-    if (!gemv_make_plan(wk, ak, NK[i][0], NK[i][1], M, L.sms, 1, L.max_smem, &p->step[i], true))
+    if (!gemv_make_plan(wk, ak, NK[i][0], NK[i][1], M, L.sms, 1, L.max_smem, &p->step[i], true) ||
+        (wk == WKind::I8 && p->step[i].chunk_k / L.cfg.quant_group < 8))
       p->step_ok = false;
   return true;
 }
@@ -201,9 +207,15 @@ ds_status validate_config(const ds_layer_config* c) {
   if (c->act_dtype != DS_F16 && c->act_dtype != DS_BF16)
     return fail(DS_ERR_INVALID_ARG, "act_dtype must be DS_F16 or DS_BF16");
   if (c->weight_dtype == DS_I8) {
-    if (c->quant_group != 64) return fail(DS_ERR_UNSUPPORTED, "quant_group must be 64");
-    if (c->hidden % 512 != 0 || c->ffn % 512 != 0)
-      return fail(DS_ERR_UNSUPPORTED, "int8 weights need hidden and ffn multiples of 512");
+    // One MMA sums 16 codes spread over a 64-code block, so a scale must be
+    // uniform over each block: groups of 64 or 128 (32 would need the scale
+    // applied before the MMA).
+    if (c->quant_group != 64 && c->quant_group != 128)
+      return fail(DS_ERR_UNSUPPORTED, "quant_group must be 64 or 128 for the layer (32 only for ds_quantize_int8)");
+    // a weight chunk (8 warps x blocks of 64 codes) spans at least 8 scale groups
+    const int kmul = c->quant_group == 128 ? 1024 : 512;
+    if (c->hidden % kmul != 0 || c->ffn % kmul != 0)
+      return fail(DS_ERR_UNSUPPORTED, "int8 weights need hidden and ffn multiples of 512 (1024 for quant_group 128)");
   } else if (c->weight_dtype == c->act_dtype) {
     if (c->hidden % 256 != 0 || c->ffn % 256 != 0)
       return fail(DS_ERR_UNSUPPORTED, "hidden and ffn must be multiples of 256");
@@ -273,6 +285,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   base.counters = bf.cnt_gemv;
   base.eps = c.ln_eps;
   base.status = bf.status;
+  base.qgroup = c.quant_group;
   base.H = H;
 
   // R1: LayerNorm1 + QKV + bias + KV append
@@ -442,8 +455,10 @@ ds_status make_tensor_maps(ds_layer* L) {
       if (!encode_weight_map(host.data() + (size_t)(3 * r + i) * kTensorMapBytes, W[r], rows[r],
                              (size_t)cols[r] * esz, (int)(8 * nb * blk_k * esz)))
         return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
-      if (i8 && !encode_scale_map(host.data() + (size_t)(12 + 3 * r + i) * kTensorMapBytes, Sc[r], rows[r],
-                                  cols[r] / 64, 8 * nb))
+      // the scale box (8 nb 64 / quant_group groups) must be 16 bytes or more
+      if (i8 && 8 * nb * 64 / c.quant_group >= 8 &&
+          !encode_scale_map(host.data() + (size_t)(12 + 3 * r + i) * kTensorMapBytes, Sc[r], rows[r],
+                            cols[r] / c.quant_group, 8 * nb * 64 / c.quant_group))
         return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a scale matrix");
     }
   }
@@ -618,7 +633,8 @@ ds_status ds_stack_create(ds_layer* const* layers, int n_layers, ds_stack** out)
     const ds_layer_config& a = layers[0]->cfg;
     const ds_layer_config& b = layers[i]->cfg;
     if (a.hidden != b.hidden || a.heads != b.heads || a.ffn != b.ffn || a.act_dtype != b.act_dtype ||
-        a.weight_dtype != b.weight_dtype || a.ln_eps != b.ln_eps || layers[i]->device != layers[0]->device)
+        a.weight_dtype != b.weight_dtype || a.ln_eps != b.ln_eps || layers[i]->device != layers[0]->device ||
+        (a.weight_dtype == DS_I8 && a.quant_group != b.quant_group))
       return fail(DS_ERR_INVALID_ARG, "all layers of a stack must share one config and device");
   }
   ds_stack* S = new ds_stack();
@@ -660,6 +676,7 @@ bool build_step_args(const ds_stack* S, const Plans& p, const Bufs& bf, const vo
   a->head_dim = c.hidden / c.heads;
   a->max_len = max_len;
   a->eps = c.ln_eps;
+  a->qgroup = c.quant_group;
   a->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a->head_dim));
   a->nsplit = step_attn_nsplit(B, c.heads, max_len, L0.sms);
   for (int i = 0; i < 4; ++i) a->plan[i] = p.step[i];
@@ -891,9 +908,13 @@ ds_status ds_quantize_int8(const void* w_f16, int n, int k, int group, int8_t* c
   if ((reinterpret_cast<uintptr_t>(w_f16) & 3u) != 0 || (reinterpret_cast<uintptr_t>(codes) & 1u) != 0 ||
       (reinterpret_cast<uintptr_t>(scales_f16) & 1u) != 0)
     return fail(DS_ERR_INVALID_ARG, "misaligned pointer");
-  if (group != 64) return fail(DS_ERR_UNSUPPORTED, "group must be 64");
-  if (n < 1 || k < 64 || k % 64 != 0) return fail(DS_ERR_INVALID_ARG, "n >= 1 and k a positive multiple of 64 required");
-  cudaError_t e = launch_quantize_int8(w_f16, n, k, codes, scales_f16, static_cast<cudaStream_t>(stream));
+  if (group != 32 && group != 64 && group != 128) return fail(DS_ERR_UNSUPPORTED, "group must be 32, 64 or 128");
+  if ((reinterpret_cast<uintptr_t>(w_f16) & (size_t)(group / 16 - 1)) != 0 ||
+      (reinterpret_cast<uintptr_t>(codes) & (size_t)(group / 32 - 1)) != 0)
+    return fail(DS_ERR_INVALID_ARG, "misaligned pointer for this group length");
+  if (n < 1 || k < group || k % group != 0)
+    return fail(DS_ERR_INVALID_ARG, "n >= 1 and k a positive multiple of group required");
+  cudaError_t e = launch_quantize_int8(w_f16, n, k, group, codes, scales_f16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize_int8 launch");
   g_launches += 1;
   return DS_OK;

@@ -97,7 +97,7 @@ template <int NT> struct SmemLayout {
   // rstd [64] and the full / empty mbarriers of the ring.
   static __host__ __device__ size_t chunk_bytes(int chunk_k, int esize) { return (size_t)16 * chunk_k * esize; }
   static __host__ __device__ size_t scale_bytes(int chunk_k, bool i8) {
-    return i8 ? (size_t)16 * (chunk_k / 64) * 2 : 0;
+    return i8 ? (size_t)16 * (chunk_k / 32) * 2 : 0;  // room for the finest grouping (32)
   }
   static __host__ __device__ size_t stage_bytes(int chunk_k, int esize, bool i8) {
     return (chunk_bytes(chunk_k, esize) + scale_bytes(chunk_k, i8) + 1023) & ~(size_t)1023;
@@ -243,7 +243,7 @@ __device__ void gemv_tma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
   const int dp_b = cta * P.q;
   const int nchunks = (int)(rb - ra) + P.q * C;
   (void)nchunks; (void)K; (void)S; (void)SB; (void)ring; (void)M; (void)K_S;
-  const uint32_t tx = (uint32_t)(RB + (kI8 ? 16 * (P.chunk_k / 64) * 2 : 0));
+  const uint32_t tx = (uint32_t)(RB + (kI8 ? 16 * (P.chunk_k / a.qgroup) * 2 : 0));
   (void)tw;
   // Lanes 0 .. kIssueLanes-1 each issue every kIssueLanes-th chunk: one
   // issuing thread cannot keep a CTA's copies in flight at HBM rate (it spends
@@ -267,7 +267,7 @@ __device__ void gemv_tma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
       const uint32_t stage = smem_u32(ring + (size_t)st * SB);
       mbar_arrive_expect_tx(sm.full_bar(st), tx);
       tma_load_3d(stage, a.tmap_w, 0, row0, kg * ESZ / kSwizzleBytes, sm.full_bar(st), pol);
-      if constexpr (kI8) tma_load_2d(stage + (uint32_t)RB, a.tmap_s, kg / 64, row0, sm.full_bar(st), pol);
+      if constexpr (kI8) tma_load_2d(stage + (uint32_t)RB, a.tmap_s, kg / a.qgroup, row0, sm.full_bar(st), pol);
       for (int i = 0; i < kIssueLanes; ++i) ws_cursor_next(q, P, dp_b);
     }
     __syncwarp();
@@ -281,7 +281,7 @@ __device__ void gemv_tma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
 // scales) that CTA blockIdx.x streams in the GEMV of plan P.
 template <WKind WK>
 __device__ void gemv_l2_prefetch_phase(const void* tmap_w, const void* tmap_s, const GemvPlan& P,
-                                       int max_chunks) {
+                                       int max_chunks, int qgroup) {
   constexpr int ESZ = (WK == WKind::I8) ? 1 : 2;
   const int cta = blockIdx.x, G = P.grid;
   if ((threadIdx.x & 31) != 0 || cta >= G) return;
@@ -295,7 +295,7 @@ __device__ void gemv_l2_prefetch_phase(const void* tmap_w, const void* tmap_s, c
   for (int j = 0; j < nchunks; ++j) {
     const int kg = q.s * P.K_S + q.kc * P.chunk_k;
     tma_prefetch_3d(tmap_w, 0, q.t * 16, kg * ESZ / kSwizzleBytes);
-    if (WK == WKind::I8) tma_prefetch_2d(tmap_s, kg / 64, q.t * 16);
+    if (WK == WKind::I8) tma_prefetch_2d(tmap_s, kg / qgroup, q.t * 16);
     ws_cursor_next(q, P, dp_b);
   }
 }
@@ -350,8 +350,11 @@ __device__ void gemv_mma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
   unsigned lofs[kMaxBlk];
 #pragma unroll
   for (int blk = 0; blk < kMaxBlk; ++blk) lofs[blk] = rl_offset(wr, o_step + 64 * blk);
-  const int gpc = P.chunk_k / 64;  // int8: scale groups per chunk row
-  const int sofs = wr * gpc + warp * step_k / 64;
+  // int8: scale groups per chunk row, and the group of block blk (groups of
+  // 64 or 128 codes: uniform over the block, whose codes one MMA sums)
+  const int gpc = P.chunk_k / a.qgroup;
+  const int sofs = wr * gpc;
+  const int sg0 = warp * step_k + 16 * c;
   auto load = [&](int st, Slot& sl) {
     const unsigned char* stage = ring + (size_t)st * SB;
 #pragma unroll
@@ -367,8 +370,9 @@ __device__ void gemv_mma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
 #pragma unroll
       for (int blk = 0; blk < kMaxBlk; ++blk) {
         if (blk < P.nblk) {
-          sl.sc[blk] = sc[blk];
-          sl.sc[kMaxBlk + blk] = sc[8 * gpc + blk];
+          const int gi = (sg0 + 64 * blk) / a.qgroup;
+          sl.sc[blk] = sc[gi];
+          sl.sc[kMaxBlk + blk] = sc[8 * gpc + gi];
         }
       }
     }
@@ -909,7 +913,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) region_gemv_kernel(const Regi
     // wait for it: the ring fills while the previous kernel is still finishing.
     RingPos rp;
     gemv_tma_phase<R, WK, ACT, NT>(a, a.plan, sm, rp, warp - kTmaWarp0, l2_evict_first_policy());
-    if (a.next_tmap_w != nullptr) gemv_l2_prefetch_phase<WK>(a.next_tmap_w, a.next_tmap_s, a.next_plan, kL2Lookahead);
+    if (a.next_tmap_w != nullptr)
+      gemv_l2_prefetch_phase<WK>(a.next_tmap_w, a.next_tmap_s, a.next_plan, kL2Lookahead, a.qgroup);
     pdl_launch_dependents();
   } else {
     pdl_wait();

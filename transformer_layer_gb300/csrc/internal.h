@@ -60,6 +60,7 @@ struct RegionArgs {
   const __half* Wscale = nullptr;  // int8: fp16 scales [N][K/64]
   const void* tmap_w = nullptr;    // device address of W's tensor map (64-byte aligned)
   const void* tmap_s = nullptr;    // int8: device address of the scales' tensor map
+  int qgroup = 64;                 // int8: scale group length along K (32, 64 or 128)
   int N = 0, K = 0, M = 0;         // M = B * T rows
   int B = 1, T = 1;
   GemvPlan plan;
@@ -133,6 +134,7 @@ struct StepLayer {
 
 struct StepArgs {
   int L = 0, B = 1, H = 0, F = 0, heads = 0, head_dim = 0, max_len = 0;
+  int qgroup = 64;          // int8 scale group length
   float eps = 1e-5f, scale_log2 = 0.f;
   int nsplit = 1;           // attention key splits per (b, h)
   GemvPlan plan[4];         // QKV, O-proj, FFN-up, FFN-down
@@ -189,7 +191,7 @@ size_t layer_workspace_zero_prefix(const ds_layer* layer, int batch, int new_tok
 // Sets the detail string returned by ds_last_error() on this thread.
 void set_last_error(const char* msg);
 
-cudaError_t launch_quantize_int8(const void* w, int n, int k, int8_t* codes, void* scales,
+cudaError_t launch_quantize_int8(const void* w, int n, int k, int group, int8_t* codes, void* scales,
                                  cudaStream_t st);
 
 }  // namespace ds
