@@ -1,6 +1,6 @@
 """GPU parity of the stack decode step (graph replay, device-side seq_len).
 
-Each decode step is judged layer by layer, teacher-forced: the oracle gets
+Each decode step is checked layer by layer, teacher-forced: the oracle gets
 the device's input to that layer and the cache contents the device had before
 the step, and its float64 result is compared with the device's layer output
 and new cache entries.  Free-running drift of the whole stack is bounded
@@ -73,7 +73,7 @@ def prefix_outputs(S, x, stream):
                                               (torch.float16, True)])
 def test_stack_steps_graph_vs_oracle(act, step_kernel, monkeypatch):
     """Four graph-replayed decode steps of a 3-layer stack, run as the chain of
-    region kernels or (DS_STEP_KERNEL=1) by the persistent step kernel.  Each layer is judged
+    region kernels or (DS_STEP_KERNEL=1) by the persistent step kernel.  Each layer is checked
     against the oracle fed that layer's device input and the device cache
     contents before the step (teacher-forced, layer by layer); the step output
     must equal the last prefix's output bit for bit; the free-running drift of
