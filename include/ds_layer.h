@@ -83,12 +83,17 @@ typedef struct {
   ds_dtype act_dtype;  /* DS_F16 or DS_BF16: hidden states, caches, biases, LN */
   ds_dtype weight_dtype; /* DS_F16 / DS_BF16 (must equal act_dtype) or DS_I8    */
   int quant_group;     /* DS_I8 only: group length along K, 64 or 128          */
+  int mlp_extra_grouping; /* DS_I8 only: 0, or 1 = the FFN matrices w_fc1 and
+                           * w_fc2 use groups of quant_group / 2 (twice as many
+                           * groups as w_qkv and w_o; quant_group must then be 128) */
 } ds_layer_config;
 
 /* Device pointers to one layer's parameters.  Vectors are in act_dtype.
  * Matrices are [out][in]: w_qkv [3H][H], w_o [H][H], w_fc1 [F][H], w_fc2 [H][F],
  * in weight_dtype (int8 codes for DS_I8).  For DS_I8, s_* hold the float16
- * group scales [out][in / quant_group]; they are ignored otherwise. */
+ * group scales [out][in / g]: g = quant_group for s_qkv and s_o, and for s_fc1
+ * and s_fc2 quant_group / 2 with mlp_extra_grouping, else quant_group.  They
+ * are ignored for other weight dtypes. */
 typedef struct {
   const void *ln1_g, *ln1_b, *w_qkv, *b_qkv, *w_o, *b_o;
   const void *ln2_g, *ln2_b, *w_fc1, *b_fc1, *w_fc2, *b_fc2;

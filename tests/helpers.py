@@ -44,12 +44,18 @@ def to64(t):
 
 class DeviceLayer:
     """One layer's device weights + library handle (int8 weights quantised on
-    the device with ds_quantize_int8 when weight_dtype is torch.int8)."""
+    the device with ds_quantize_int8 when weight_dtype is torch.int8).
+
+    int8 group lengths along K: ``quant_group`` for w_qkv and w_o; with
+    ``mlp_extra_grouping`` the FFN matrices w_fc1 and w_fc2 are split into
+    twice as many groups (quant_group / 2)."""
 
     def __init__(self, hidden, heads, ffn, seed, layer=0, act_dtype=torch.float16,
-                 weight_dtype=torch.float16, device="cuda", quant_group=64):
+                 weight_dtype=torch.float16, device="cuda", quant_group=64, mlp_extra_grouping=0):
         self.hidden, self.heads, self.ffn = hidden, heads, ffn
-        self.quant_group = quant_group
+        self.quant_group, self.mlp_extra_grouping = quant_group, mlp_extra_grouping
+        self.groups = {k: (quant_group // 2 if mlp_extra_grouping and k in ("w_fc1", "w_fc2") else quant_group)
+                       for k in ("w_qkv", "w_o", "w_fc1", "w_fc2")}
         self.act_dtype, self.weight_dtype = act_dtype, weight_dtype
         src_dtype = torch.float16 if weight_dtype == torch.int8 else act_dtype
         self.p = inputs.layer_params(hidden, ffn, seed, layer, dtype=src_dtype, device=device)
@@ -60,27 +66,37 @@ class DeviceLayer:
         self.codes, self.scales = {}, {}
         if weight_dtype == torch.int8:
             for k, sk in (("w_qkv", "s_qkv"), ("w_o", "s_o"), ("w_fc1", "s_fc1"), ("w_fc2", "s_fc2")):
-                w = self.p[k]
+                w, grp = self.p[k], self.groups[k]
                 q = torch.empty(w.shape, dtype=torch.int8, device=device)
-                s = torch.empty((w.shape[0], w.shape[1] // quant_group), dtype=torch.float16, device=device)
-                ds.ds_quantize_int8(w, q, s, group=quant_group)
+                s = torch.empty((w.shape[0], w.shape[1] // grp), dtype=torch.float16, device=device)
+                ds.ds_quantize_int8(w, q, s, group=grp)
                 self.dev[k] = q
                 self.dev[sk] = s
                 self.codes[k], self.scales[k] = q, s
         torch.cuda.synchronize()
         self.handle = ds.ds_layer_create(hidden, heads, ffn, self.dev, act_dtype, weight_dtype,
-                                         quant_group=quant_group)
+                                         quant_group=quant_group, mlp_extra_grouping=mlp_extra_grouping)
+        self._oracle = None
+
+    def oracle_quantized(self, k):
+        """The oracle's own (codes, scales) of int8 matrix k, quantised from the
+        same float16 weights the device quantiser read."""
+        return oracle.quantize_int8(self.p[k].cpu().numpy(), self.groups[k])
 
     def oracle_params(self):
-        """float64 copies of the weights the device uses (q * s for int8)."""
-        out = {}
-        for k, v in self.p.items():
-            if self.weight_dtype == torch.int8 and k in self.codes:
-                out[k] = oracle.dequantize_int8(self.codes[k].cpu().numpy(), self.scales[k].cpu().numpy(),
-                                                self.quant_group)
-            else:
-                out[k] = to64(v)
-        return out
+        """float64 parameters for the oracle: the float16 / bf16 values the device
+        uses, and for int8 weights q * s from the oracle's own quantiser (never
+        the device's codes)."""
+        if self._oracle is None:
+            out = {}
+            for k, v in self.p.items():
+                if self.weight_dtype == torch.int8 and k in self.groups:
+                    q, s = self.oracle_quantized(k)
+                    out[k] = oracle.dequantize_int8(q, s, self.groups[k])
+                else:
+                    out[k] = to64(v)
+            self._oracle = out
+        return self._oracle
 
     def close(self):
         ds.ds_layer_destroy(self.handle)

@@ -145,22 +145,27 @@ def test_int8_13b_shaped_layer(B):
         L.close()
 
 
+@pytest.mark.parametrize("extra", [0, 1])
 @pytest.mark.parametrize("group,act,B", [(128, torch.float16, 1), (128, torch.bfloat16, 6),
                                          (128, torch.float16, 16)])
-def test_int8_group_lengths(group, act, B):
-    """A MoQ grouping other than 64 along K (groups of 128 codes): device codes
-    and scales bit-exact with the oracle's quantiser at that group length, and
-    the layer within tolerance of the oracle using q * s."""
+def test_int8_group_lengths(group, act, B, extra):
+    """MoQ groupings other than 64 along K: groups of 128 codes in every matrix,
+    or (extra MLP grouping) 128 in w_qkv / w_o and twice as many groups, of 64,
+    in w_fc1 / w_fc2.  Device codes and scales bit-exact with the oracle's
+    quantiser at each matrix's group length, and the layer within tolerance of
+    the oracle using its own q * s."""
     H, nh, F = 1024, 8, 4096
-    L = DeviceLayer(H, nh, F, seed=1006, act_dtype=act, weight_dtype=torch.int8, quant_group=group)
+    L = DeviceLayer(H, nh, F, seed=1006, act_dtype=act, weight_dtype=torch.int8, quant_group=group,
+                    mlp_extra_grouping=extra)
     try:
-        for k in ("w_qkv", "w_fc2"):
-            q, s = oracle.quantize_int8(L.p[k].cpu().numpy(), group)
+        for k in ("w_qkv", "w_o", "w_fc1", "w_fc2"):
+            q, s = L.oracle_quantized(k)
+            assert s.shape[1] == L.p[k].shape[1] // (group // 2 if extra and k in ("w_fc1", "w_fc2") else group)
             assert np.array_equal(L.codes[k].cpu().numpy(), q)
             assert np.array_equal(L.scales[k].cpu().numpy().view(np.uint16), s.view(np.uint16))
         past = [40 + 11 * b for b in range(B)]
         res = run_layer(L, B, 1, past, max_len=256, seed=13)
-        check_layer(L, res, B, 1, past, f"int8 g{group} {act} B={B}")
+        check_layer(L, res, B, 1, past, f"int8 g{group} extra {extra} {act} B={B}")
     finally:
         L.close()
 

@@ -20,8 +20,10 @@ pytestmark = pytest.mark.gpu
 
 
 class DeviceStack:
-    def __init__(self, n_layers, H, nh, F, B, max_len, past, seed, act=torch.float16, wdt=torch.float16):
-        self.layers = [DeviceLayer(H, nh, F, seed, layer=l, act_dtype=act, weight_dtype=wdt)
+    def __init__(self, n_layers, H, nh, F, B, max_len, past, seed, act=torch.float16, wdt=torch.float16,
+                 quant_group=64, mlp_extra_grouping=0):
+        self.layers = [DeviceLayer(H, nh, F, seed, layer=l, act_dtype=act, weight_dtype=wdt,
+                                   quant_group=quant_group, mlp_extra_grouping=mlp_extra_grouping)
                        for l in range(n_layers)]
         self.handle = ds.ds_stack_create([l.handle for l in self.layers])
         d = H // nh
@@ -69,19 +71,25 @@ def prefix_outputs(S, x, stream):
     return outs
 
 
-@pytest.mark.parametrize("act,step_kernel", [(torch.float16, False), (torch.bfloat16, False),
-                                              (torch.float16, True)])
-def test_stack_steps_graph_vs_oracle(act, step_kernel, monkeypatch):
+@pytest.mark.parametrize("act,step_kernel,int8", [(torch.float16, False, False), (torch.bfloat16, False, False),
+                                                   (torch.float16, True, False), (torch.float16, False, True),
+                                                   (torch.bfloat16, True, True)])
+def test_stack_steps_graph_vs_oracle(act, step_kernel, int8, monkeypatch):
     """Four graph-replayed decode steps of a 3-layer stack, run as the chain of
     region kernels or (DS_STEP_KERNEL=1) by the persistent step kernel.  Each layer is checked
     against the oracle fed that layer's device input and the device cache
     contents before the step (teacher-forced, layer by layer); the step output
     must equal the last prefix's output bit for bit; the free-running drift of
-    the whole stack against the oracle is checked only loosely."""
+    the whole stack against the oracle is checked only loosely.  The int8 cases
+    take MoQ groups of 128 for w_qkv / w_o and, with the extra MLP grouping,
+    64 for the FFN matrices, so consecutive GEMVs differ in group length."""
     n_layers, H, nh, F, B, max_len = 3, 512, 8, 2048, 2, 40
+    quant = {}
+    if int8:
+        H, nh, quant = 1024, 8, dict(wdt=torch.int8, quant_group=128, mlp_extra_grouping=1)
     past = [7, 20]
     monkeypatch.setenv("DS_STEP_KERNEL", "1" if step_kernel else "0")
-    S = DeviceStack(n_layers, H, nh, F, B, max_len, past, seed=1100, act=act, wdt=act)
+    S = DeviceStack(n_layers, H, nh, F, B, max_len, past, seed=1100, act=act, **({"wdt": act} | quant))
     stream = torch.cuda.Stream()
     try:
         with torch.cuda.stream(stream):

@@ -116,6 +116,9 @@ struct ds_layer {
   const void* tmap_s(int r, int nblk) const {
     return cfg.weight_dtype == DS_I8 ? tmaps + (size_t)(12 + 3 * r + nblk_index(nblk)) * kTensorMapBytes : nullptr;
   }
+  // int8 scale group length of matrix r (0 QKV, 1 O-proj, 2 FFN-up, 3 FFN-down):
+  // the FFN matrices take half the length under mlp_extra_grouping.
+  int qgroup(int r) const { return (r >= 2 && cfg.mlp_extra_grouping == 1) ? cfg.quant_group / 2 : cfg.quant_group; }
 };
 
 namespace {
@@ -140,14 +143,14 @@ bool make_plans(const ds_layer& L, int M, int B, Plans* p) {
   if (!gemv_make_plan(wk, ak, H, F, M, L.sms, cps, smem, &p->down)) return false;
   if (wk == WKind::I8) {  // the scale box of a chunk must hold at least 8 groups
     const GemvPlan* pl[4] = {&p->qkv, &p->o, &p->up, &p->down};
-    for (const GemvPlan* q : pl)
-      if (q->chunk_k / L.cfg.quant_group < 8) return false;
+    for (int i = 0; i < 4; ++i)
+      if (pl[i]->chunk_k / L.qgroup(i) < 8) return false;
   }
   const int NK[4][2] = {{3 * H, H}, {H, H}, {F, H}, {H, F}};
   p->step_ok = true;
   for (int i = 0; i < 4; ++i)
     if (!gemv_make_plan(wk, ak, NK[i][0], NK[i][1], M, L.sms, 1, L.max_smem, &p->step[i], true) ||
-        (wk == WKind::I8 && p->step[i].chunk_k / L.cfg.quant_group < 8))
+        (wk == WKind::I8 && p->step[i].chunk_k / L.qgroup(i) < 8))
       p->step_ok = false;
   return true;
 }
@@ -212,10 +215,16 @@ ds_status validate_config(const ds_layer_config* c) {
     // applied before the MMA).
     if (c->quant_group != 64 && c->quant_group != 128)
       return fail(DS_ERR_UNSUPPORTED, "quant_group must be 64 or 128 for the layer (32 only for ds_quantize_int8)");
-    // a weight chunk (8 warps x blocks of 64 codes) spans at least 8 scale groups
-    const int kmul = c->quant_group == 128 ? 1024 : 512;
-    if (c->hidden % kmul != 0 || c->ffn % kmul != 0)
-      return fail(DS_ERR_UNSUPPORTED, "int8 weights need hidden and ffn multiples of 512 (1024 for quant_group 128)");
+    if (c->mlp_extra_grouping != 0 && c->mlp_extra_grouping != 1)
+      return fail(DS_ERR_INVALID_ARG, "mlp_extra_grouping must be 0 or 1");
+    const int g_mlp = c->mlp_extra_grouping == 1 ? c->quant_group / 2 : c->quant_group;
+    if (g_mlp < 64)
+      return fail(DS_ERR_UNSUPPORTED, "mlp_extra_grouping needs quant_group 128 (FFN groups of 64)");
+    // a weight chunk (8 warps x blocks of 64 codes) spans at least 8 scale
+    // groups: each matrix's K is a multiple of 8 groups and of 512
+    const int kmul_h = std::max(512, 8 * c->quant_group), kmul_f = std::max(512, 8 * g_mlp);
+    if (c->hidden % kmul_h != 0 || c->ffn % kmul_f != 0)
+      return fail(DS_ERR_UNSUPPORTED, "int8 weights need hidden and ffn multiples of 512 (of 1024 for groups of 128)");
   } else if (c->weight_dtype == c->act_dtype) {
     if (c->hidden % 256 != 0 || c->ffn % 256 != 0)
       return fail(DS_ERR_UNSUPPORTED, "hidden and ffn must be multiples of 256");
@@ -285,7 +294,6 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   base.counters = bf.cnt_gemv;
   base.eps = c.ln_eps;
   base.status = bf.status;
-  base.qgroup = c.quant_group;
   base.H = H;
 
   // R1: LayerNorm1 + QKV + bias + KV append
@@ -297,6 +305,8 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   r1.next_tmap_w = L.tmap_w(1, P.o.nblk);
   r1.next_tmap_s = L.tmap_s(1, P.o.nblk);
   r1.next_plan = P.o;
+  r1.qgroup = L.qgroup(0);
+  r1.next_qgroup = L.qgroup(1);
   r1.N = 3 * H;
   r1.K = H;
   r1.plan = P.qkv;
@@ -349,6 +359,8 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   r3.next_tmap_w = L.tmap_w(2, P.up.nblk);
   r3.next_tmap_s = L.tmap_s(2, P.up.nblk);
   r3.next_plan = P.up;
+  r3.qgroup = L.qgroup(1);
+  r3.next_qgroup = L.qgroup(2);
   r3.N = H;
   r3.K = H;
   r3.plan = P.o;
@@ -370,6 +382,8 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   r4.next_tmap_w = L.tmap_w(3, P.down.nblk);
   r4.next_tmap_s = L.tmap_s(3, P.down.nblk);
   r4.next_plan = P.down;
+  r4.qgroup = L.qgroup(2);
+  r4.next_qgroup = L.qgroup(3);
   r4.N = F;
   r4.K = H;
   r4.plan = P.up;
@@ -393,7 +407,9 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     r5.next_tmap_w = next->tmap_w(0, P.qkv.nblk);
     r5.next_tmap_s = next->tmap_s(0, P.qkv.nblk);
     r5.next_plan = P.qkv;
+    r5.next_qgroup = next->qgroup(0);
   }
+  r5.qgroup = L.qgroup(3);
   r5.N = H;
   r5.K = F;
   r5.plan = P.down;
@@ -455,10 +471,11 @@ ds_status make_tensor_maps(ds_layer* L) {
       if (!encode_weight_map(host.data() + (size_t)(3 * r + i) * kTensorMapBytes, W[r], rows[r],
                              (size_t)cols[r] * esz, (int)(8 * nb * blk_k * esz)))
         return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
-      // the scale box (8 nb 64 / quant_group groups) must be 16 bytes or more
-      if (i8 && 8 * nb * 64 / c.quant_group >= 8 &&
+      // the scale box (8 nb 64 / group groups) must be 16 bytes or more
+      const int grp = L->qgroup(r);
+      if (i8 && 8 * nb * 64 / grp >= 8 &&
           !encode_scale_map(host.data() + (size_t)(12 + 3 * r + i) * kTensorMapBytes, Sc[r], rows[r],
-                            cols[r] / c.quant_group, 8 * nb * 64 / c.quant_group))
+                            cols[r] / grp, 8 * nb * 64 / grp))
         return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a scale matrix");
     }
   }
@@ -539,6 +556,10 @@ ds_status ds_layer_create(const ds_layer_config* cfg, const ds_layer_weights* w,
   if (s != DS_OK) return s;
   ds_layer* L = new ds_layer();
   L->cfg = *cfg;
+  if (cfg->weight_dtype != DS_I8) {  // the int8 fields are ignored: keep them inert
+    L->cfg.quant_group = 64;
+    L->cfg.mlp_extra_grouping = 0;
+  }
   L->w = *w;
   L->device = dev;
   L->sms = di.sms;
@@ -634,7 +655,8 @@ ds_status ds_stack_create(ds_layer* const* layers, int n_layers, ds_stack** out)
     const ds_layer_config& b = layers[i]->cfg;
     if (a.hidden != b.hidden || a.heads != b.heads || a.ffn != b.ffn || a.act_dtype != b.act_dtype ||
         a.weight_dtype != b.weight_dtype || a.ln_eps != b.ln_eps || layers[i]->device != layers[0]->device ||
-        (a.weight_dtype == DS_I8 && a.quant_group != b.quant_group))
+        (a.weight_dtype == DS_I8 &&
+         (a.quant_group != b.quant_group || a.mlp_extra_grouping != b.mlp_extra_grouping)))
       return fail(DS_ERR_INVALID_ARG, "all layers of a stack must share one config and device");
   }
   ds_stack* S = new ds_stack();
@@ -676,7 +698,7 @@ bool build_step_args(const ds_stack* S, const Plans& p, const Bufs& bf, const vo
   a->head_dim = c.hidden / c.heads;
   a->max_len = max_len;
   a->eps = c.ln_eps;
-  a->qgroup = c.quant_group;
+  for (int i = 0; i < 4; ++i) a->qgroup[i] = L0.qgroup(i);
   a->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a->head_dim));
   a->nsplit = step_attn_nsplit(B, c.heads, max_len, L0.sms);
   for (int i = 0; i < 4; ++i) a->plan[i] = p.step[i];

@@ -914,7 +914,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) region_gemv_kernel(const Regi
     RingPos rp;
     gemv_tma_phase<R, WK, ACT, NT>(a, a.plan, sm, rp, warp - kTmaWarp0, l2_evict_first_policy());
     if (a.next_tmap_w != nullptr)
-      gemv_l2_prefetch_phase<WK>(a.next_tmap_w, a.next_tmap_s, a.next_plan, kL2Lookahead, a.qgroup);
+      gemv_l2_prefetch_phase<WK>(a.next_tmap_w, a.next_tmap_s, a.next_plan, kL2Lookahead, a.next_qgroup);
     pdl_launch_dependents();
   } else {
     pdl_wait();

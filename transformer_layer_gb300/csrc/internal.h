@@ -60,7 +60,7 @@ struct RegionArgs {
   const __half* Wscale = nullptr;  // int8: fp16 scales [N][K/64]
   const void* tmap_w = nullptr;    // device address of W's tensor map (64-byte aligned)
   const void* tmap_s = nullptr;    // int8: device address of the scales' tensor map
-  int qgroup = 64;                 // int8: scale group length along K (32, 64 or 128)
+  int qgroup = 64;                 // int8: scale group length along K (64 or 128)
   int N = 0, K = 0, M = 0;         // M = B * T rows
   int B = 1, T = 1;
   GemvPlan plan;
@@ -95,6 +95,7 @@ struct RegionArgs {
   const void* next_tmap_w = nullptr;
   const void* next_tmap_s = nullptr;
   GemvPlan next_plan;
+  int next_qgroup = 64;  // int8: that matrix's scale group length
 };
 
 struct AttnArgs {
@@ -134,7 +135,7 @@ struct StepLayer {
 
 struct StepArgs {
   int L = 0, B = 1, H = 0, F = 0, heads = 0, head_dim = 0, max_len = 0;
-  int qgroup = 64;          // int8 scale group length
+  int qgroup[4] = {64, 64, 64, 64};  // int8 scale group length of each phase's matrix
   float eps = 1e-5f, scale_log2 = 0.f;
   int nsplit = 1;           // attention key splits per (b, h)
   GemvPlan plan[4];         // QKV, O-proj, FFN-up, FFN-down

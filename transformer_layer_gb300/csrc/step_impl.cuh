@@ -103,7 +103,7 @@ __device__ __forceinline__ RegionArgs step_region_args(const StepArgs& s, int l,
   a.H = s.H;
   a.W = ly.w[r];
   a.Wscale = ly.sc[r];
-  a.qgroup = s.qgroup;
+  a.qgroup = s.qgroup[r];
   a.tmap_w = ly.tmap_w[r];
   a.tmap_s = ly.tmap_s[r];
   a.bias = ly.bias[r];
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
         const int nl = reg == 3 ? l + 1 : l, nreg = reg == 3 ? 0 : reg + 1;
         if (nl < s.L)
           gemv_l2_prefetch_phase<WK>(s.layer[nl].tmap_w[nreg], s.layer[nl].tmap_s[nreg], s.plan[nreg],
-                                     kStepL2Lookahead, s.qgroup);
+                                     kStepL2Lookahead, s.qgroup[nreg]);
       }
     }
   } else if (warp == kEpiWarp) {

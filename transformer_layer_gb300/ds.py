@@ -49,7 +49,8 @@ EXPORTED = tuple(_SIGS)
 
 class ds_layer_config(C.Structure):
     _fields_ = [("hidden", C.c_int), ("heads", C.c_int), ("ffn", C.c_int), ("ln_eps", C.c_float),
-                ("act_dtype", C.c_int), ("weight_dtype", C.c_int), ("quant_group", C.c_int)]
+                ("act_dtype", C.c_int), ("weight_dtype", C.c_int), ("quant_group", C.c_int),
+                ("mlp_extra_grouping", C.c_int)]
 
 
 _WNAMES = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "w_fc1", "b_fc1",
@@ -113,11 +114,11 @@ def _dtype_code(dt):
 
 # ---------------------------------------------------------------- thin wrappers
 def ds_layer_create(hidden, heads, ffn, weights: dict, act_dtype, weight_dtype, ln_eps=1e-5,
-                    quant_group=64):
+                    quant_group=64, mlp_extra_grouping=0):
     """weights: dict of device tensors keyed like ds_layer_weights' fields."""
     lib = load()
     cfg = ds_layer_config(hidden, heads, ffn, ln_eps, _dtype_code(act_dtype),
-                          _dtype_code(weight_dtype), quant_group)
+                          _dtype_code(weight_dtype), quant_group, int(mlp_extra_grouping))
     w = ds_layer_weights(*[_ptr(weights.get(n)) for n in _WNAMES])
     out = C.c_void_p()
     _check(lib.ds_layer_create(C.byref(cfg), C.byref(w), C.byref(out)), "ds_layer_create")
