@@ -294,6 +294,34 @@ def test_codes_match_exact_rational_rounding():
             assert int(q[n, k]) == want
 
 
+@pytest.mark.parametrize("group", [32, 64, 128])
+def test_group_lengths_brute_force(group):
+    """Each scale comes from the largest magnitude of its own run of ``group``
+    weights along K (checked by explicit loops over k ranges, in exact
+    rationals), every code from that scale, and dequantisation multiplies each
+    code by its own group's scale."""
+    rng = np.random.default_rng(17)
+    w = (rng.standard_normal((5, 512)) * 0.02).astype(np.float16)
+    w[1, 130] = np.float16(0.5)     # a lone large weight: only its own group's scale grows
+    q, s = oracle.quantize_int8(w, group)
+    assert s.shape == (5, 512 // group)
+    deq = oracle.dequantize_int8(q, s, group)
+    for n in range(5):
+        for j in range(512 // group):
+            ks = range(j * group, (j + 1) * group)
+            amax = max(abs(Fraction(float(w[n, k]))) for k in ks)
+            want_s = np.float16(_fp16_rne_of_fraction(amax / 127))
+            assert s[n, j].view(np.uint16) == want_s.view(np.uint16), (n, j)
+            sv = Fraction(float(s[n, j]))
+            for k in ks:
+                want = max(-127, min(127, round(Fraction(float(w[n, k])) / sv)))
+                assert int(q[n, k]) == want, (n, k)
+                assert Fraction(float(deq[n, k])) == want * sv
+    big = 130 // group
+    assert float(s[1, big]) == float(np.float16(np.float32(0.5) / np.float32(127)))
+    assert all(float(s[1, j]) < 1e-3 for j in range(512 // group) if j != big)
+
+
 def test_int8_invariants():
     rng = np.random.default_rng(15)
     w = (rng.standard_normal((32, 128)) * 0.02).astype(np.float16)
