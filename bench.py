@@ -42,12 +42,13 @@ FALLBACK_HBM_GBS = 6800.0
 CYCLE = 64  # decode positions per pass over the cache
 
 # Stack shapes: hidden, heads, FFN, depth, cached positions, weight bytes per
-# weight (int8: one code byte + a 2-byte fp16 scale per group of 64).
+# weight (int8: one code byte + a 2-byte fp16 scale per group; `--quant-group`
+# and `--mlp-extra-grouping` change the groups of the int8 stack).
 MODELS = {
     "7b": dict(H=4096, nh=32, F=16384, layers=32, past=512, wbytes=2.0, wname="fp16",
                title="7B-shaped GPT-style stack"),
     "13b-int8": dict(H=5120, nh=40, F=20480, layers=40, past=1024, wbytes=1.0 + 2.0 / 64, wname="int8",
-                     title="13B-shaped GPT-style stack, MoQ int8 group-64 weights"),
+                     title="13B-shaped GPT-style stack, MoQ int8 weights"),
     "neo-2.7b": dict(H=2560, nh=20, F=10240, layers=32, past=128, wbytes=2.0, wname="fp16",
                      title="GPT-Neo-2.7B-shaped stack"),
 }
@@ -66,16 +67,20 @@ def parse():
                          "GPT-Neo-2.7B-shaped fp16 stack (the last two without CPU baseline)")
     ap.add_argument("--bf16", action="store_true",
                     help="bf16 weights and activations (fp16 stacks only); default fp16")
+    ap.add_argument("--quant-group", type=int, default=64, choices=[64, 128],
+                    help="13b-int8: MoQ group length along K of the attention matrices")
+    ap.add_argument("--mlp-extra-grouping", action="store_true",
+                    help="13b-int8: FFN matrices in groups of half that length")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=4)
     return ap.parse_args()
 
 
-def workload_config(B, layers, model="7b", wname=None):
+def workload_config(B, layers, model="7b", wname=None, wbytes=None):
     m = MODELS[model]
     wname = wname or m["wname"]
     H, nh, F, past = m["H"], m["nh"], m["F"], m["past"]
-    gb = layers * layer_bytes(H, F, m["wbytes"]) / 1e9
+    gb = layers * layer_bytes(H, F, wbytes if wbytes is not None else m["wbytes"]) / 1e9
     return {
         "workload": f"{m['title']}: {layers} pre-LN layers, hidden {H}, {nh} heads "
                     f"(head_dim {H // nh}), FFN {F}, GeLU(tanh), {wname} weights; batch {B}; KV cache "
@@ -175,10 +180,15 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def _wb(wbytes):
+    """(attention matrices, FFN matrices) bytes per weight."""
+    return tuple(wbytes) if isinstance(wbytes, (tuple, list)) else (wbytes, wbytes)
+
+
 def layer_bytes(H, F, wbytes=2.0):
-    n_w = 3 * H * H + H * H + F * H + H * F
+    wa, wm = _wb(wbytes)
     n_small = 3 * H + H + F + H + 4 * H
-    return wbytes * n_w + 2 * n_small
+    return wa * 4 * H * H + wm * 2 * F * H + 2 * n_small
 
 
 def step_bytes(H, F, layers, B, past, steps, wbytes=2.0):
@@ -194,12 +204,13 @@ def step_bytes(H, F, layers, B, past, steps, wbytes=2.0):
 def region_bytes(H, F, B, past, wbytes=2.0):
     """Algorithmic bytes of one launch of each region kernel (weights + vectors in/out)."""
     S = past + 1 + CYCLE // 2
+    wa, wm = _wb(wbytes)
     return {
-        "ln_qkv": 3 * H * H * wbytes + 3 * H * 2 + 4 * H + B * (H * 2 + H * 4 + 2 * H * 2),
+        "ln_qkv": 3 * H * H * wa + 3 * H * 2 + 4 * H + B * (H * 2 + H * 4 + 2 * H * 2),
         "attention": B * (2 * S * H * 2 + H * 4 + H * 4),
-        "oproj_res": H * H * wbytes + 2 * H + B * (H * 4 + H * 2 + H * 4),
-        "ffn_up": F * H * wbytes + 2 * F + 4 * H + B * (H * 4 + F * 4),
-        "ffn_down": H * F * wbytes + 2 * H + B * (F * 4 + H * 4 + H * 2),
+        "oproj_res": H * H * wa + 2 * H + B * (H * 4 + H * 2 + H * 4),
+        "ffn_up": F * H * wm + 2 * F + 4 * H + B * (H * 4 + F * 4),
+        "ffn_down": H * F * wm + 2 * H + B * (F * 4 + H * 4 + H * 2),
     }
 
 
@@ -319,8 +330,18 @@ def main():
     int8 = m["wname"] == "int8"
     if args.bf16 and int8:
         raise SystemExit("--bf16 applies to the fp16 stacks")
+    ga = args.quant_group
+    gm = ga // 2 if args.mlp_extra_grouping else ga
+    if int8:
+        if gm < 64:
+            raise SystemExit("--mlp-extra-grouping needs --quant-group 128")
+        wbytes = (1.0 + 2.0 / ga, 1.0 + 2.0 / gm)
+    elif ga != 64 or args.mlp_extra_grouping:
+        raise SystemExit("--quant-group / --mlp-extra-grouping apply to the int8 stack")
     act = torch.bfloat16 if args.bf16 else torch.float16
     wname = "bf16" if args.bf16 else m["wname"]
+    if int8:
+        wname = f"int8 (MoQ groups of {ga}" + (f", FFN groups of {gm})" if gm != ga else ")")
     max_len = past + CYCLE
     seed = 1002 + rank
     stream = torch.cuda.Stream(device=dev)
@@ -329,16 +350,18 @@ def main():
     layers, params, kcs, vcs = [], [], [], []
     for l in range(L):
         p = inputs.layer_params(H, F, seed, l, dtype=act, device=dev)
-        if int8:   # MoQ group-64 codes and fp16 scales, quantised on the device
-            for k, sk in (("w_qkv", "s_qkv"), ("w_o", "s_o"), ("w_fc1", "s_fc1"), ("w_fc2", "s_fc2")):
+        if int8:   # MoQ codes and fp16 group scales, quantised on the device
+            for k, sk, g in (("w_qkv", "s_qkv", ga), ("w_o", "s_o", ga), ("w_fc1", "s_fc1", gm),
+                             ("w_fc2", "s_fc2", gm)):
                 w = p[k]
                 q = torch.empty(w.shape, dtype=torch.int8, device=dev)
-                sc = torch.empty((w.shape[0], w.shape[1] // 64), dtype=torch.float16, device=dev)
-                ds.ds_quantize_int8(w, q, sc)
+                sc = torch.empty((w.shape[0], w.shape[1] // g), dtype=torch.float16, device=dev)
+                ds.ds_quantize_int8(w, q, sc, group=g)
                 p[k], p[sk] = q, sc
             torch.cuda.synchronize(dev)
         params.append(p)
-        layers.append(ds.ds_layer_create(H, nh, F, p, act, torch.int8 if int8 else act))
+        layers.append(ds.ds_layer_create(H, nh, F, p, act, torch.int8 if int8 else act, quant_group=ga,
+                                         mlp_extra_grouping=int(args.mlp_extra_grouping)))
         k, v = inputs.kv_cache(B, nh, max_len, d, seed, l, dtype=act, device=dev)
         kcs.append(k)
         vcs.append(v)
@@ -437,7 +460,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if args.bf16 else "f16",
         "data": "synthetic (seeded: weights N(0,0.02), biases N(0,0.01), LN gamma 1+N(0,0.1), "
                 "beta N(0,0.1), KV cache and inputs N(0,1))",
-        "config": workload_config(B, L, args.model, wname),
+        "config": workload_config(B, L, args.model, wname, wbytes),
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_kind} HBM copy",
                      "bytes_per_launch": rbytes[dom], "us_per_launch": dom_us,
