@@ -34,7 +34,9 @@
  *     arrays [B][nh][max_len][d] in the activation dtype.
  *   - Every pointer must be 16-byte aligned (the workspace 256-byte aligned);
  *     d must be 64 or 128; H and F must be multiples of 256 for fp16/bf16
- *     weights and of 512 for int8 weights; B*T must be 1..64.
+ *     weights and of 512 for int8 weights, and of 1024 where a matrix with
+ *     that input width uses groups of 128 (H with quant_group 128; F with
+ *     quant_group 128 and no extra MLP grouping); B*T must be 1..64.
  *   - Calls are asynchronous on the given stream (never synchronising, except
  *     ds_stack_region_times, ds_workspace_status and ds_stack_decode_host,
  *     which say so).  A stream of 0 means the legacy default stream.
