@@ -111,3 +111,25 @@ def test_null_arguments(lib):
     assert lib.ds_quantize_int8(None, 4, 128, 64, None, None, None) == ds.DS_ERR_INVALID_ARG
     assert lib.ds_stack_set_profiling(None, 1) == ds.DS_ERR_INVALID_ARG
     assert lib.ds_workspace_init(None, 0, None) == ds.DS_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs a C compiler")
+@pytest.mark.parametrize("struct", ["ds_layer_config", "ds_layer_weights"])
+def test_binding_structs_match_the_header(struct, tmp_path):
+    """The ctypes mirrors of the header's structs have the C layout: a C program
+    compiled against include/ds_layer.h prints each field's offset and the
+    size, and they must equal ctypes' (a field missing from either side, or
+    out of order, fails)."""
+    cls = getattr(ds, struct)
+    fields = [name for name, _ in cls._fields_]
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "ds_layer.h"', "int main(void) {",
+             f'  printf("%zu\\n", sizeof({struct}));']
+    lines += [f'  printf("%zu\\n", offsetof({struct}, {f}));' for f in fields]
+    lines += ["  return 0;", "}"]
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [C.sizeof(cls)] + [getattr(cls, f).offset for f in fields]
+    assert got == want, (struct, fields, got, want)
