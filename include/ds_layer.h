@@ -67,7 +67,7 @@ extern "C" {
 typedef enum {
   DS_OK = 0,
   DS_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size or shape      */
-  DS_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement     */
+  DS_ERR_UNSUPPORTED = 2,   /* a valid request the library does not implement    */
   DS_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed        */
   DS_ERR_WORKSPACE = 4,     /* workspace smaller than ds_*_workspace_bytes()      */
   DS_ERR_DEVICE = 5         /* a device-side check failed (see ds_workspace_status) */
