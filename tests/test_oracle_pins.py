@@ -207,6 +207,44 @@ def test_bias_only_layer_places_biases_and_qkv_blocks():
     np.testing.assert_array_equal(r["q"][0, 0], p["b_qkv"][:H].reshape(nh, d))
 
 
+def test_stack_chains_layers_and_routes_caches():
+    """Stack of bias-only layers (all matrices zero): layer l adds exactly
+    b_o + b_fc2 of its own to the residual stream, so the stack output is x
+    plus the sum over layers (dyadic biases: exact in float64), every
+    intermediate output is the partial sum, and layer l's new key / value are
+    its own bias blocks, written into its own cache only."""
+    rng = np.random.default_rng(18)
+    H, F, nh, n_layers = 16, 32, 4, 3
+    d = H // nh
+    layers = []
+    for l in range(n_layers):
+        p = {k: np.zeros_like(v) for k, v in _layer(rng, H, F).items()}
+        p["ln1_g"][:] = 1.0
+        p["ln2_g"][:] = 1.0
+        p["b_o"] = rng.integers(-64, 65, H) / 64.0
+        p["b_fc2"] = rng.integers(-64, 65, H) / 128.0
+        p["b_qkv"][H:2 * H] = l + 1.0
+        p["b_qkv"][2 * H:] = -(l + 1.0)
+        layers.append(p)
+    x = rng.standard_normal((2, 1, H))
+    caches = [_rand_cache(rng, 2, nh, 6, d) for _ in range(n_layers)]
+    Ks, Vs = [c[0] for c in caches], [c[1] for c in caches]
+    before = [(k.copy(), v.copy()) for k, v in caches]
+    past = [1, 4]
+    outs = oracle.stack_forward(x, layers, Ks, Vs, past, nh)
+    assert len(outs) == n_layers
+    acc = x.copy()
+    for l, p in enumerate(layers):
+        acc = acc + p["b_o"] + p["b_fc2"]
+        np.testing.assert_array_equal(outs[l]["y"], acc)
+        for b, pos in enumerate(past):
+            assert np.all(Ks[l][b, :, pos, :] == l + 1.0) and np.all(Vs[l][b, :, pos, :] == -(l + 1.0))
+            keep = np.ones(6, bool)
+            keep[pos] = False
+            np.testing.assert_array_equal(Ks[l][b][:, keep], before[l][0][b][:, keep])
+            np.testing.assert_array_equal(Vs[l][b][:, keep], before[l][1][b][:, keep])
+
+
 def test_zero_query_attention_averages_values_including_new_token():
     rng = np.random.default_rng(11)
     H, F, nh = 16, 32, 2
