@@ -294,6 +294,58 @@ def test_ffn_identity_weights_reduce_to_zscore_and_gelu():
     np.testing.assert_allclose(r["y"][0, 0], x[0, 0] + gelu_erf, atol=5e-4)
 
 
+def test_qkv_projects_the_normalised_input():
+    """Region 1 projects LN1(x), not x: with identity weights in the q block, no
+    bias, gamma = 1, beta = 0 and eps = 0, the query of each head is its slice
+    of the z-score of x."""
+    rng = np.random.default_rng(20)
+    H, nh = 16, 4
+    p = _layer(rng, H, 32)
+    p["w_qkv"] = np.zeros((3 * H, H)); p["w_qkv"][:H] = np.eye(H); p["b_qkv"] = np.zeros(3 * H)
+    p["ln1_g"] = np.ones(H); p["ln1_b"] = np.zeros(H)
+    x = 5.0 + 2.0 * rng.standard_normal((1, 1, H))
+    K, V = _rand_cache(rng, 1, nh, 4, H // nh)
+    r = oracle.layer_forward(x, p, K, V, [1], nh, eps=0.0)
+    np.testing.assert_allclose(r["q"][0, 0].reshape(H), zscore(x[0, 0], ddof=0), atol=1e-12)
+
+
+def test_ffn_bias_enters_before_the_gelu():
+    """g = GeLU(h2 W1^T + b1): with W1 = 0 the FFN activations are GeLU(b1),
+    compared with the exact (erf) GeLU b1 * Phi(b1) within the tanh form's
+    distance from it; W_o = 0 and identity W2 then give y = x + GeLU(b1)."""
+    rng = np.random.default_rng(21)
+    H, nh = 16, 4
+    p = _layer(rng, H, H)
+    p["w_o"] = np.zeros((H, H)); p["b_o"] = np.zeros(H)
+    p["w_fc1"] = np.zeros((H, H)); p["b_fc1"] = np.linspace(-3.0, 3.0, H)
+    p["w_fc2"] = np.eye(H); p["b_fc2"] = np.zeros(H)
+    x = rng.standard_normal((1, 1, H))
+    K, V = _rand_cache(rng, 1, nh, 4, H // nh)
+    r = oracle.layer_forward(x, p, K, V, [1], nh)
+    c = p["b_fc1"]
+    np.testing.assert_allclose(r["g"][0, 0], c * ndtr(c), atol=5e-4)
+    np.testing.assert_allclose(r["y"][0, 0], x[0, 0] + c * ndtr(c), atol=5e-4)
+
+
+def test_ffn_normalises_the_post_attention_residual():
+    """The second LayerNorm sees x1 = x + o W_o^T + b_o, not the layer input:
+    with W_o = 0 and a large b_o, identity FFN weights and eps = 0, h2 is the
+    z-score of x + b_o, and y = x + b_o + GeLU(h2)."""
+    rng = np.random.default_rng(19)
+    H, nh = 32, 4
+    p = _layer(rng, H, H)
+    p["w_o"] = np.zeros((H, H)); p["b_o"] = 3.0 * rng.standard_normal(H)
+    p["w_fc1"] = np.eye(H); p["b_fc1"] = np.zeros(H)
+    p["w_fc2"] = np.eye(H); p["b_fc2"] = np.zeros(H)
+    p["ln2_g"] = np.ones(H); p["ln2_b"] = np.zeros(H)
+    x = rng.standard_normal((1, 1, H))
+    K, V = _rand_cache(rng, 1, nh, 4, H // nh)
+    r = oracle.layer_forward(x, p, K, V, [2], nh, eps=0.0)
+    z = zscore(x[0, 0] + p["b_o"], ddof=0)
+    np.testing.assert_allclose(r["h2"][0, 0], z, atol=1e-12)
+    np.testing.assert_allclose(r["y"][0, 0], x[0, 0] + p["b_o"] + z * ndtr(z), atol=5e-4)
+
+
 # ---------------------------------------------------------------- int8 (MoQ)
 def _fp16_rne_of_fraction(fr):
     """Round a positive Fraction to the nearest float16, ties to even, exactly."""
