@@ -37,6 +37,12 @@
  *     weights and of 512 for int8 weights, and of 1024 where a matrix with
  *     that input width uses groups of 128 (H with quant_group 128; F with
  *     quant_group 128 and no extra MLP grouping); B*T must be 1..64.
+ *     With int8 weights the activations staged per GEMV slice (80 KB of
+ *     shared memory) bound B*T further: up to 64 rows with fp16 activations
+ *     and 39 with bf16 for groups of 64; 39 (fp16) and 19 (bf16) once a
+ *     matrix uses groups of 128.  Beyond that ds_layer_workspace_bytes and
+ *     ds_stack_workspace_bytes return 0 and the forward calls return
+ *     DS_ERR_UNSUPPORTED before any launch.
  *   - Calls are asynchronous on the given stream (never synchronising, except
  *     ds_stack_region_times, ds_workspace_status and ds_stack_decode_host,
  *     which say so).  A stream of 0 means the legacy default stream.
