@@ -36,13 +36,21 @@
  *     d must be 64 or 128; H and F must be multiples of 256 for fp16/bf16
  *     weights and of 512 for int8 weights, and of 1024 where a matrix with
  *     that input width uses groups of 128 (H with quant_group 128; F with
- *     quant_group 128 and no extra MLP grouping); B*T must be 1..64.
- *     With int8 weights the activations staged per GEMV slice (80 KB of
- *     shared memory) bound B*T further: up to 64 rows with fp16 activations
- *     and 39 with bf16 for groups of 64; 39 (fp16) and 19 (bf16) once a
- *     matrix uses groups of 128.  Beyond that ds_layer_workspace_bytes and
- *     ds_stack_workspace_bytes return 0 and the forward calls return
- *     DS_ERR_UNSUPPORTED before any launch.
+ *     quant_group 128 and no extra MLP grouping).
+ *   - Rows R = B*T (batch rows x new tokens) per call: 1..4096 with fp16 /
+ *     bf16 weights, 1..64 with int8 weights.  Up to 8 rows (and always for
+ *     int8) the GEMMs run as streaming skinny-GEMM kernels with the
+ *     LayerNorm fused into their prologue; above 8 rows as tensor-core tile
+ *     kernels (tcgen05, accumulators in tensor memory), each LayerNorm then
+ *     running as a small row kernel ahead of its GEMM (seven kernels per
+ *     layer instead of five).  With int8 weights the activations staged per
+ *     GEMV slice (80 KB of shared memory) bound R further: up to 64 rows with
+ *     fp16 activations and 39 with bf16 for groups of 64; 39 (fp16) and 19
+ *     (bf16) once a matrix uses groups of 128.  Beyond the limits
+ *     ds_layer_workspace_bytes and ds_stack_workspace_bytes return 0 and the
+ *     forward calls return DS_ERR_UNSUPPORTED before any launch.
+ *   - The forward calls run on the device the layer was created on, which
+ *     must be the current device (else DS_ERR_INVALID_ARG, nothing launched).
  *   - Calls are asynchronous on the given stream (never synchronising, except
  *     ds_stack_region_times, ds_workspace_status and ds_stack_decode_host,
  *     which say so).  A stream of 0 means the legacy default stream.
@@ -127,7 +135,8 @@ DS_API size_t ds_layer_workspace_bytes(const ds_layer* layer, int batch, int new
 DS_API ds_status ds_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 
 /* One layer forward over T = new_tokens new tokens per sequence (regions
- * R1..R4 of [P1] §3.2).
+ * R1..R4 of [P1] §3.2); T > 1 is a prompt chunk (query t of sequence b sees
+ * keys 0 .. past_len[b] + t, [P3] triangular_masking).
  *   x_in     [B][T][H] act_dtype, read only
  *   x_out    [B][T][H] act_dtype, written (must not alias x_in)
  *   k_cache, v_cache  [B][nh][max_len][d]; positions past_len[b]+t are written
@@ -137,7 +146,8 @@ DS_API ds_status ds_workspace_init(void* workspace, size_t ws_bytes, void* strea
  *            DS_DEVFLAG_CACHE_OVERFLOW (read it with ds_workspace_status).
  *   workspace  device scratch of at least ds_layer_workspace_bytes() bytes,
  *            zero-filled once (ds_workspace_init) before first use.
- * Five kernels are enqueued on `stream` (a cudaStream_t). */
+ * Five kernels (seven on the tile path) are enqueued on `stream` (a
+ * cudaStream_t). */
 DS_API ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out, int batch,
                            int new_tokens, void* k_cache, void* v_cache, int max_len,
                            const int32_t* past_len, void* workspace, size_t ws_bytes,
@@ -148,20 +158,28 @@ DS_API ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out
  * that must not risk the device-wide synchronisation of an allocation,
  * real-time hosts that forbid allocation after start-up).  The pages have no
  * counterpart: this is a property of the library, not of the method.
- * Runs the same five kernels, with the workspace taken from a 16 MiB static
+ * Runs the same kernels, with the workspace taken from a 16 MiB static
  * device array inside the library (every GPU that loads the library holds
  * it until the process exits); nothing is allocated or freed.
  *   - Returns DS_ERR_UNSUPPORTED when ds_layer_workspace_bytes(layer, batch,
- *     new_tokens) exceeds 16 MiB, and the argument errors of ds_layer_forward.
+ *     new_tokens) exceeds 16 MiB, and the argument errors of ds_layer_forward
+ *     (a rejected call enqueues nothing and leaves the array untouched).
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make it before any
- *     stream capture.
+ *     stream capture.  The cached address is not valid across
+ *     cudaDeviceReset: do not use this entry point after a device reset.
  *   - All calls share the array: calls that overlap on the GPU race.  Each
- *     call clears the array's status word and counters first, so device
- *     status flags of this entry point are not reported. */
+ *     accepted call clears the array's status word and counters first;
+ *     ds_noalloc_status reads the flags the last call left. */
 DS_API ds_status ds_layer_forward_noalloc(ds_layer* layer, const void* x_in, void* x_out, int batch,
                                           int new_tokens, void* k_cache, void* v_cache, int max_len,
                                           const int32_t* past_len, void* stream);
+
+/* Device status flags (DS_DEVFLAG_*) of the last ds_layer_forward_noalloc
+ * call on the current device: copies the static array's status word to
+ * *flags_out, clears it and synchronises `stream` (order it after that call).
+ * Returns DS_ERR_DEVICE when a flag was set, DS_OK otherwise. */
+DS_API ds_status ds_noalloc_status(uint32_t* flags_out, void* stream);
 
 /* A stack of layers that share one config.  The layer handles stay owned by
  * the caller and must outlive the stack. */
@@ -176,13 +194,15 @@ DS_API size_t ds_stack_workspace_bytes(const ds_stack* stack, int batch);
  *   seq_len  [B] int32 DEVICE array: positions already cached; the new token
  *            is written at seq_len[b], and the step adds 1 to every entry on
  *            the device after the last layer has read it.
- * The launch sequence (5 kernels per layer, chained with programmatic
- * dependent launch; the first kernel waits for all earlier work on `stream`)
- * is captured into a CUDA graph on the first call with a given argument set
- * and replayed afterwards; when `stream` is the legacy default stream or is
- * already capturing, the kernels are launched directly.  With the environment
- * variable DS_STEP_KERNEL=1 the step runs instead as one persistent,
- * cooperative kernel where it can (same results within tolerance; slower). */
+ * The launch sequence (5 kernels per layer, 7 on the tile path, chained with
+ * programmatic dependent launch; the first kernel waits for all earlier work
+ * on `stream`) is captured into a CUDA graph on the first call with a given
+ * (batch, caches, max_len, seq_len, workspace) and replayed afterwards.  A
+ * call with other x_in / x_out buffers updates the captured graph in place
+ * (the kernel nodes that hold them) instead of capturing again, so a decode
+ * loop may alternate or rotate its hidden-state buffers freely.  When
+ * `stream` is the legacy default stream or is already capturing, the kernels
+ * are launched directly. */
 DS_API ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, int batch,
                                void* const* k_caches, void* const* v_caches, int max_len,
                                int32_t* seq_len, void* workspace, size_t ws_bytes,
@@ -208,6 +228,11 @@ DS_API ds_status ds_stack_set_profiling(ds_stack* stack, int enabled);
  * [3] R4a FFN-up+GeLU, [4] R4b FFN-down+residual; launches_out[i] = launches
  * averaged.  Resets the accumulators. */
 DS_API ds_status ds_stack_region_times(ds_stack* stack, float us_out[5], int launches_out[5]);
+
+/* Number of CUDA-graph captures ds_stack_decode_step has made for this
+ * stack since it was created (a new argument set captures again; new x_in /
+ * x_out buffers do not). */
+DS_API uint64_t ds_stack_graph_captures(const ds_stack* stack);
 
 /* MoQ-style quantisation of a float16 weight matrix w_f16 [n][k] ([P1] §5.2):
  * per group of `group` (32, 64 or 128) consecutive weights along k, scale

@@ -127,6 +127,20 @@ def test_skinny_gemm_sweep_layer(act, B):
         L.close()
 
 
+@pytest.mark.parametrize("act,B", [(torch.float16, 32), (torch.float16, 64), (torch.bfloat16, 32)])
+def test_int8_layer_many_rows(act, B):
+    """MoQ int8 weights at 32 and 64 batch rows (the streaming GEMV kernels
+    with four and eight MMA column tiles; bf16 activations up to 39 rows)."""
+    H, nh, F = 1024, 8, 4096
+    L = DeviceLayer(H, nh, F, seed=1011, act_dtype=act, weight_dtype=torch.int8)
+    try:
+        past = [(17 * b) % 90 for b in range(B)]
+        res = run_layer(L, B, 1, past, max_len=100, seed=15)
+        check_layer(L, res, B, 1, past, f"int8 {act} B={B}")
+    finally:
+        L.close()
+
+
 @pytest.mark.parametrize("B", [1, 16])
 def test_int8_13b_shaped_layer(B):
     """A 13B-shaped layer (hidden 5120, 40 heads, FFN 20480) with MoQ int8
@@ -166,6 +180,24 @@ def test_int8_group_lengths(group, act, B, extra):
         past = [40 + 11 * b for b in range(B)]
         res = run_layer(L, B, 1, past, max_len=256, seed=13)
         check_layer(L, res, B, 1, past, f"int8 g{group} extra {extra} {act} B={B}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("act", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("B,T", [(9, 1), (16, 1), (40, 1), (64, 1), (10, 10), (2, 128), (3, 100)])
+def test_tile_path_layer(act, B, T):
+    """Above 8 rows (B * T) fp16 / bf16 layers run the tensor-core tile
+    kernels: decode batches that are not a multiple of 16, prompt chunks of up
+    to 128 new tokens per sequence (causal mask among them), ragged cache
+    lengths, several token tiles for 300 rows.  Every element against the
+    oracle."""
+    H, nh, F = 1024, 8, 4096
+    L = DeviceLayer(H, nh, F, seed=1010, act_dtype=act, weight_dtype=act)
+    try:
+        past = [(29 * b) % 60 for b in range(B)]
+        res = run_layer(L, B, T, past, max_len=200, seed=14)
+        check_layer(L, res, B, T, past, f"tile {act} B={B} T={T}")
     finally:
         L.close()
 
@@ -234,8 +266,31 @@ def test_bad_arguments_rejected_before_launch():
             ds.ds_layer_forward(L.handle, x, x, 1, 1, kc, kc, 8, past, ws, nbytes)
         assert e.value.code == ds.DS_ERR_INVALID_ARG
         with pytest.raises(ds.DSError) as e:
-            ds.ds_layer_forward(L.handle, x, out, 65, 1, kc, kc, 8, past, ws, nbytes)
+            ds.ds_layer_forward(L.handle, x, out, 4097, 1, kc, kc, 8, past, ws, nbytes)
         assert e.value.code == ds.DS_ERR_UNSUPPORTED
+        assert ds.ds_launch_count() == n0
+    finally:
+        L.close()
+
+
+@pytest.mark.skipif(torch.cuda.device_count() < 2, reason="needs a second GPU to make current")
+def test_forward_on_another_current_device_is_rejected():
+    """A layer's kernels run on the device it was created on; a call made with
+    another device current is refused before any launch."""
+    L = DeviceLayer(256, 4, 1024, seed=8)
+    try:
+        x = torch.zeros(1, 1, 256, dtype=torch.float16, device="cuda:0")
+        out = torch.empty_like(x)
+        kc = torch.zeros(1, 4, 8, 64, dtype=torch.float16, device="cuda:0")
+        past = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+        nbytes = ds.ds_layer_workspace_bytes(L.handle, 1, 1)
+        ws = new_workspace(nbytes, device="cuda:0")
+        n0 = ds.ds_launch_count()
+        with torch.cuda.device(1):
+            with pytest.raises(ds.DSError) as e:
+                ds.ds_layer_forward(L.handle, x, out, 1, 1, kc, kc.clone(), 8, past, ws, nbytes,
+                                    stream=torch.cuda.current_stream(0))
+            assert e.value.code == ds.DS_ERR_INVALID_ARG
         assert ds.ds_launch_count() == n0
     finally:
         L.close()

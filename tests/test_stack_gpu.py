@@ -71,24 +71,23 @@ def prefix_outputs(S, x, stream):
     return outs
 
 
-@pytest.mark.parametrize("act,step_kernel,int8", [(torch.float16, False, False), (torch.bfloat16, False, False),
-                                                   (torch.float16, True, False), (torch.float16, False, True),
-                                                   (torch.bfloat16, True, True)])
-def test_stack_steps_graph_vs_oracle(act, step_kernel, int8, monkeypatch):
-    """Four graph-replayed decode steps of a 3-layer stack, run as the chain of
-    region kernels or (DS_STEP_KERNEL=1) by the persistent step kernel.  Each layer is checked
-    against the oracle fed that layer's device input and the device cache
-    contents before the step (teacher-forced, layer by layer); the step output
-    must equal the last prefix's output bit for bit; the free-running drift of
-    the whole stack against the oracle is checked only loosely.  The int8 cases
-    take MoQ groups of 128 for w_qkv / w_o and, with the extra MLP grouping,
-    64 for the FFN matrices, so consecutive GEMVs differ in group length."""
-    n_layers, H, nh, F, B, max_len = 3, 512, 8, 2048, 2, 40
+@pytest.mark.parametrize("act,int8,B", [(torch.float16, False, 2), (torch.bfloat16, False, 2),
+                                        (torch.float16, True, 2), (torch.bfloat16, True, 3),
+                                        (torch.float16, False, 12), (torch.bfloat16, False, 16)])
+def test_stack_steps_graph_vs_oracle(act, int8, B):
+    """Four graph-replayed decode steps of a 3-layer stack.  Each layer is
+    checked against the oracle fed that layer's device input and the device
+    cache contents before the step (teacher-forced, layer by layer); the step
+    output must equal the last prefix's output bit for bit; the free-running
+    drift of the whole stack against the oracle is checked only loosely.  The
+    int8 cases take MoQ groups of 128 for w_qkv / w_o and, with the extra MLP
+    grouping, 64 for the FFN matrices, so consecutive GEMVs differ in group
+    length.  Batch 12 and 16 run the tensor-core tile kernels."""
+    n_layers, H, nh, F, max_len = 3, 512, 8, 2048, 40
     quant = {}
     if int8:
         H, nh, quant = 1024, 8, dict(wdt=torch.int8, quant_group=128, mlp_extra_grouping=1)
-    past = [7, 20]
-    monkeypatch.setenv("DS_STEP_KERNEL", "1" if step_kernel else "0")
+    past = [(7 + 13 * b) % 30 for b in range(B)]
     S = DeviceStack(n_layers, H, nh, F, B, max_len, past, seed=1100, act=act, **({"wdt": act} | quant))
     stream = torch.cuda.Stream()
     try:
@@ -176,7 +175,7 @@ def test_decode_host_entry_point():
         n0 = ds.ds_launch_count()
         ds.ds_stack_decode_host(S.handle, xh, yh, xd, yd, B, S.kc, S.vc, max_len, S.seq, S.ws, S.nbytes,
                                 stream)
-        assert ds.ds_launch_count() - n0 in (1, 5 * n_layers)   # one step kernel, or the region chain
+        assert ds.ds_launch_count() - n0 == 5 * n_layers   # the region chain, replayed as one graph
         out = torch.empty_like(x)
         S2.step(x, out, stream)
         stream.synchronize()
@@ -184,3 +183,38 @@ def test_decode_host_entry_point():
     finally:
         S.close()
         S2.close()
+
+
+@pytest.mark.parametrize("B", [2, 16])
+def test_rotating_hidden_buffers_reuse_the_graph(B):
+    """A decode loop that rotates its input buffers (three) and output buffers
+    (two) keeps one captured graph: the kernel nodes holding x_in / x_out are
+    updated in place.  Results are bit-identical to direct launches on the
+    legacy stream with the same buffers."""
+    n_layers, H, nh, F, max_len = 2, 256, 4, 1024, 24
+    past = [(3 + 5 * b) % 17 for b in range(B)]
+    ys = {}
+    for mode in ("graph", "legacy"):
+        S = DeviceStack(n_layers, H, nh, F, B, max_len, past, seed=1400)
+        try:
+            xs = [inputs.hidden(B, 1, H, 1400, step=i, device="cuda").reshape(B, H) for i in range(3)]
+            outs = [torch.empty_like(xs[0]) for _ in range(2)]
+            stream = torch.cuda.Stream() if mode == "graph" else None
+            got = []
+            for step in range(6):
+                torch.cuda.synchronize()
+                x, out = xs[step % 3], outs[step % 2]
+                if mode == "graph":
+                    S.step(x, out, stream)
+                else:
+                    ds.ds_stack_decode_step(S.handle, x, out, B, S.kc, S.vc, max_len, S.seq, S.ws, S.nbytes, 0)
+                torch.cuda.synchronize()
+                got.append(out.clone())
+            if mode == "graph":
+                assert ds.ds_stack_graph_captures(S.handle) == 1
+            ys[mode] = (torch.stack(got), torch.stack([k.clone() for k in S.kc]))
+            assert S.seq.cpu().tolist() == [p + 6 for p in past]
+        finally:
+            S.close()
+    assert torch.equal(ys["graph"][0], ys["legacy"][0])
+    assert torch.equal(ys["graph"][1], ys["legacy"][1])

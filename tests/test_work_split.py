@@ -20,7 +20,7 @@ def test_work_split_replay(tmp_path):
         pytest.skip("no host C++ compiler")
     cuda_inc = "/usr/local/cuda/include"
     exe = str(tmp_path / "work_split_check")
-    subprocess.run([cxx, "-std=c++17", "-O2", "-I", cuda_inc, "-I",
+    subprocess.run([cxx, "-std=c++17", "-O2", "-I", cuda_inc, "-I", os.path.join(ROOT, "include"), "-I",
                     os.path.join(ROOT, "transformer_layer_gb300", "csrc"),
                     os.path.join(ROOT, "tests", "work_split_check.cpp"), "-o", exe], check=True)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=300)

@@ -52,3 +52,24 @@ def test_noalloc_refuses_workspace_beyond_static_size():
         assert e.value.code == ds.DS_ERR_UNSUPPORTED
     finally:
         L.close()
+
+
+def test_noalloc_status_reports_a_cache_overflow():
+    """The device status flags of the no-allocation path are read back with
+    ds_noalloc_status: a row whose cache position is past max_len is not
+    written and raises the cache-overflow flag; the flag is cleared once read."""
+    L = DeviceLayer(256, 4, 1024, seed=1502)
+    try:
+        B, T, max_len = 2, 2, 16
+        kc, vc = inputs.kv_cache(B, 4, max_len, 64, 1502, device="cuda")
+        kc0 = kc.clone()
+        x = inputs.hidden(B, T, 256, 1502, device="cuda")
+        past = torch.tensor([3, 15], dtype=torch.int32, device="cuda")   # 15 + 2 > 16
+        ds.ds_layer_forward_noalloc(L.handle, x, torch.empty_like(x), B, T, kc, vc, max_len, past)
+        code, flags = ds.ds_noalloc_status()
+        assert code == ds.DS_ERR_DEVICE and flags & ds.DS_DEVFLAG_CACHE_OVERFLOW
+        assert torch.equal(kc[1, :, :15], kc0[1, :, :15])
+        code, flags = ds.ds_noalloc_status()
+        assert code == ds.DS_OK and flags == 0
+    finally:
+        L.close()

@@ -24,14 +24,9 @@ static int fail(const char* what, int N, int K, int M, int G, int a, int b) {
   return 1;
 }
 
-static int check(int N, int K, int M, int G0, bool i8, bool split, bool fixed = false) {
-  const int blk_k = i8 ? 64 : 32, pad = i8 ? 8 : 32;
-  auto xs = [&](int K_S) { return (size_t)(split ? 2 : 1) * M * (K_S + pad) * 2; };
-  GemvPlan P;
-  if (!ws_make_plan(N, K, M, G0, blk_k, 8, 80 * 1024, xs, &P, fixed)) return 0;  // shape not supported
+static int verify(const GemvPlan& P, int N, int K, int M) {
   const int G = P.grid, C = P.C, tiles = P.tiles;
-  if (fixed && G != G0) return fail("fixed grid not kept", N, K, M, G, G0, 0);
-  if (!fixed && !P.whole && P.R > 0 && P.R < G) return fail("fewer leftover chunks than CTAs", N, K, M, G, (int)P.R, G);
+  if (!P.whole && P.R > 0 && P.R < G) return fail("fewer leftover chunks than CTAs", N, K, M, G, (int)P.R, G);
   std::map<std::tuple<int, int, int>, int> cover;
   std::map<int, std::vector<std::pair<int, int>>> parts;  // tile -> (slice, slot)
   for (int cta = 0; cta < G; ++cta) {
@@ -93,6 +88,28 @@ static int check(int N, int K, int M, int G0, bool i8, bool split, bool fixed = 
   return 0;
 }
 
+static int check(int N, int K, int M, int G0, bool i8, bool split) {
+  const int blk_k = i8 ? 64 : 32, pad = i8 ? 8 : 32;
+  auto xs = [&](int K_S) { return (size_t)(split ? 2 : 1) * M * (K_S + pad) * 2; };
+  GemvPlan P;
+  if (!ws_make_plan(N, K, M, G0, blk_k, 8, 80 * 1024, xs, &P)) return 0;  // shape not supported
+  return verify(P, N, K, M);
+}
+
+// The tensor-core tile path: units are output tiles (128 weight rows x one
+// token tile), one K slice, chunks of 128 along K.
+static int check_tiles(int tiles, int K, int G0) {
+  GemvPlan P;
+  P.tiles = tiles;
+  P.KS = 1;
+  P.K_S = K;
+  P.chunk_k = 128;
+  P.C = K / 128;
+  P.units = tiles;
+  ws_distribute(P, G0);
+  return verify(P, 128 * tiles, K, 0);
+}
+
 int main() {
   int bad = 0;
   // Shapes of the shipped workloads (QKV, O-proj, FFN-up, FFN-down), batch rows 1..64.
@@ -108,8 +125,6 @@ int main() {
             bad |= check(H, H, M, G, i8, split);
             bad |= check(F, H, M, G, i8, split);
             bad |= check(H, F, M, G, i8, split);
-            bad |= check(3 * H, H, M, G, i8, split, true);   // persistent step kernel: grid fixed
-            bad |= check(H, F, M, G, i8, split, true);
           }
   // Pseudo-random shapes and grid sizes.
   unsigned x = 12345u;
@@ -121,8 +136,16 @@ int main() {
     const int M = 1 + rnd(64);
     const int G = 1 + rnd(400);
     bad |= check(N, K, M, G, i8, rnd(2));
-    bad |= check(N, K, M, G, i8, rnd(2), true);
+    if (it % 4 == 0) bad |= check_tiles(1 + rnd(400), 256 * (1 + rnd(40)), G);
   }
+  for (auto& hf : HF)
+    for (int tt = 1; tt <= 8; tt *= 2) {      // token tiles of a long prompt
+      const int H = hf[0], F = hf[1];
+      bad |= check_tiles(tt * 3 * H / 128, H, 152);
+      bad |= check_tiles(tt * H / 128, H, 152);
+      bad |= check_tiles(tt * F / 128, H, 152);
+      bad |= check_tiles(tt * H / 128, F, 152);
+    }
   if (!bad) std::printf("ok\n");
   return bad;
 }

@@ -116,7 +116,11 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   }
   pdl_wait();
   pdl_launch_dependents();
-  if (n_st > 0) mbar_wait(smem_u32(bar), 0, a.status);
+  // If the staging copy does not complete within the wait budget (the flag is
+  // then set), this thread reads those rows from global memory instead of
+  // shared memory, and the CTA waits again for the copy before it exits.
+  const bool staged = (n_st == 0) || mbar_wait(smem_u32(bar), 0, a.status);
+  const int n_sm = staged ? n_st : 0;  // rows read from shared memory
 
   for (int t = 0; t < a.T; ++t) {
     const int St = min(past + t + 1, S_all);
@@ -140,8 +144,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
         const int j = base + i * KPI + kr;
         if (j < n_keys) {
           // staged rows from shared memory, the rest (new rows) from global
-          const ACT* kp = (j < n_st) ? Ks + (size_t)j * D : Kc + (size_t)(lo + j) * D;
-          const ACT* vp = (j < n_st) ? Vs + (size_t)j * D : Vc + (size_t)(lo + j) * D;
+          const ACT* kp = (j < n_sm) ? Ks + (size_t)j * D : Kc + (size_t)(lo + j) * D;
+          const ACT* vp = (j < n_sm) ? Vs + (size_t)j * D : Vc + (size_t)(lo + j) * D;
           kk[i] = *reinterpret_cast<const uint4*>(kp + kq * 8);
           vv[i] = *reinterpret_cast<const uint4*>(vp + kq * 8);
         } else {
@@ -223,10 +227,19 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
         L += w * mrg[r * (D + 2) + D + 1];
         O += w * mrg[r * (D + 2) + tid];
       }
-      a.out[(size_t)(b * a.T + t) * a.H + h * D + tid] = O / L;
+      const float o = O / L;
+      const size_t oi = (size_t)(b * a.T + t) * a.H + h * D + tid;
+      if (a.out_hi != nullptr) {  // tensor-core operand: hi (and lo for bf16)
+        const ACT hv = Act<ACT>::from_f(o);
+        static_cast<ACT*>(a.out_hi)[oi] = hv;
+        if (a.out_lo != nullptr) static_cast<ACT*>(a.out_lo)[oi] = Act<ACT>::from_f(o - Act<ACT>::to_f(hv));
+      } else {
+        a.out[oi] = o;
+      }
     }
     if (t + 1 < a.T) cluster_sync_all();  // rank 0 has read the partials before they are overwritten
   }
+  if (!staged) mbar_wait(smem_u32(bar), 0, a.status);  // no copy may land after the CTA exits
 }
 
 int attn_nsplit(int B, int heads, int max_len, int num_sms) {

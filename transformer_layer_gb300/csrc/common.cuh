@@ -248,6 +248,11 @@ __device__ __forceinline__ void i8x4_to_bf162x2(uint32_t w, uint32_t& lo, uint32
   hi = Act<__nv_bfloat16>::pack2(f2, f3);
 }
 
+// Named barrier over n threads (a multiple of 32); id 0 is __syncthreads.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
+
 // ---------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

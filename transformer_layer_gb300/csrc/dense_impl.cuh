@@ -1,0 +1,467 @@
+// Tensor-core tile path of the region GEMMs (tcgen05 + TMEM), for the batch
+// rows at which the skinny GEMM becomes a real dense contraction: decode at
+// B*T = 9..64 rows and multi-token (prompt) steps of up to a few thousand rows.
+//
+// Page cited as [P1]: "DeepSpeed Inference 内核优化深度解析：多 GPU 自适应并行、
+// 算子融合推理内核与 MoQ 量化支持".
+//   §3 intro: the GEMM is built so that more operations fuse at its reduction
+//     boundary -- here the region epilogues run straight out of the tensor
+//     memory accumulator.
+//   §3.2: regions 1 (LayerNorm + QKV + bias), 3 (FF + LayerNorm + bias +
+//     residual + GeLU) and 4 (bias + residual).
+//   §3.3: shared memory stages the operands between the reductions.
+//
+// What one launch computes: y[m][n] = sum_k X[m][k] W[n][k] for m < M (batch
+// rows or tokens), n < N, followed by the region epilogue.  The region
+// prologue (the LayerNorm) has already been applied to X by the row
+// normalisation kernel (or X is the attention / GeLU output), and X is stored
+// in the MMA operand format: the activation dtype, plus for bf16 the residual
+// lo = bf16(x - bf16(x)) so that hi + lo carries ~16 significant bits.
+//
+// GB300 design:
+//  * One output tile is 128 weight rows x NTOK (16..256) rows of X, held as an
+//    fp32 accumulator in tensor memory (two buffers of NTOK columns, so the
+//    MMAs of the next tile overlap the epilogue of the previous one).
+//  * Warp 0 streams W (128 rows x KC) and X (NTOK rows x KC) chunks with TMA
+//    tensor copies (128-byte swizzle, K-major) into a ring of up to 8 stages.
+//    The weights of the first stages are requested before griddepcontrol.wait
+//    (they do not depend on the previous kernel); X after it.
+//  * Warp 1 allocates the tensor memory and one lane issues tcgen05.mma
+//    (kind::f16, M = 128, N = NTOK, K = 16 per instruction; bf16 issues the lo
+//    operand as a second MMA into the same accumulator) and tcgen05.commit to
+//    release ring stages and to publish finished tiles.
+//  * Warps 2..5 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
+//    32 (w % 4) ..: one weight row per thread, 16 token columns per load) and
+//    run the region epilogue, or publish a split-K partial; the last CTA to
+//    contribute to a tile (acquire-release counter, nothing waits) sums the
+//    partials in fixed order and runs the epilogue, so results are
+//    deterministic.
+//  * Work split (work_split.h): units are output tiles, chunks are KC-wide K
+//    ranges; every CTA owns whole tiles and/or an even share of the leftover
+//    tiles' chunks.
+#pragma once
+
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+#include "work_split.h"
+
+namespace ds {
+
+constexpr int kDenseThreads = 192;   // 6 warps
+constexpr int kDenseTmaWarp = 0;
+constexpr int kDenseMmaWarp = 1;
+constexpr int kDenseEpiWarp0 = 2;    // warps 2..5
+constexpr int kDenseEpiThreads = 128;
+constexpr int kDenseBarEpi = 1;      // named barrier of the four epilogue warps
+constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
+
+// ---------------------------------------------------------------- tcgen05
+// Shared-memory matrix descriptor of a K-major operand tile in the canonical
+// 128-byte-swizzle layout: rows of 128 bytes (64 16-bit elements), groups of
+// 8 rows 1024 bytes apart (stride byte offset), descriptor version 1,
+// swizzle mode 2 (128 B).  Advancing K by 16 elements inside the 128-byte row
+// adds 32 bytes to the start address.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B fp16 (0) or
+// bf16 (1), both K-major, N >> 3 at bit 17, M >> 4 (M = 128) at bit 24.
+__device__ __forceinline__ uint32_t umma_idesc(bool bf16, int n) {
+  return (1u << 4) | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10) | ((uint32_t)(n >> 3) << 17) | (8u << 24);
+}
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(idesc), "r"(acc));
+}
+// Arrives on `bar` once every tcgen05.mma issued so far by this thread is complete.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- geometry
+// One ring stage: W [KC/64 atoms][128 rows][128 B], then X [KC/64][NTOK][128 B]
+// (and, for bf16, X lo the same), each part on a 1024-byte boundary.
+__host__ __device__ inline size_t dense_w_bytes(int kc) { return (size_t)128 * kc * 2; }
+__host__ __device__ inline size_t dense_x_bytes(int ntok, int kc) { return (size_t)ntok * kc * 2; }
+__host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split) {
+  return dense_w_bytes(kc) + (split ? 2 : 1) * dense_x_bytes(ntok, kc);
+}
+__host__ __device__ inline uint32_t dense_tmem_cols(int ntok) {
+  uint32_t c = 32;
+  while (c < (uint32_t)(2 * ntok)) c <<= 1;
+  return c;
+}
+
+// A role's position in the ring (same convention as the GEMV ring).
+struct DRing {
+  int st = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void advance(int S) {
+    if (++st == S) {
+      st = 0;
+      ph ^= 1;
+    }
+  }
+};
+
+// Segment enumeration shared by the three roles: leftover segments of this
+// CTA, then its whole units.  f(u, kc0, kc1, j_slot) per segment.
+template <typename F>
+__device__ __forceinline__ void dense_for_segments(const GemvPlan& P, F&& f) {
+  const int cta = blockIdx.x, G = gridDim.x;
+  long long ra, rb;
+  ws_left_range(P, cta, G, &ra, &rb);
+  for (long long i = ra; i < rb;) {
+    int u, j_slot;
+    long long end;
+    ws_leftover_segment(P, i, rb, cta, G, &u, &end, &j_slot);
+    const int kc0 = (int)(i - (long long)(u - P.U_dp) * P.C);
+    f(u, kc0, kc0 + (int)(end - i), j_slot);
+    i = end;
+  }
+  for (int u = cta * P.q; u < cta * P.q + P.q; ++u) f(u, 0, P.C, 0);
+}
+
+template <Region R, typename ACT>
+__global__ void __launch_bounds__(kDenseThreads, 1)
+    dense_region_kernel(const __grid_constant__ CUtensorMap xmap_hi, const __grid_constant__ CUtensorMap xmap_lo,
+                        const DenseArgs a) {
+  constexpr bool kSplit = std::is_same<ACT, __nv_bfloat16>::value;
+  constexpr bool kStats = (R == Region::OprojRes || R == Region::FfnDown);
+  extern __shared__ __align__(1024) unsigned char dsm_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+  const DensePlan& DP = a.plan;
+  const GemvPlan& P = DP.ws;
+  const int S = DP.stages, KC = DP.kc, NTOK = DP.ntok;
+  const size_t WB = dense_w_bytes(KC), XB = dense_x_bytes(NTOK, KC);
+  const size_t SB = (dense_stage_bytes(NTOK, KC, kSplit) + 1023) & ~(size_t)1023;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)S * SB);
+  // full[S], empty[S], acc_full[2], acc_empty[2]
+  auto full_bar = [&](int i) { return smem_u32(bars + i); };
+  auto empty_bar = [&](int i) { return smem_u32(bars + S + i); };
+  auto accf_bar = [&](int i) { return smem_u32(bars + 2 * S + i); };
+  auto acce_bar = [&](int i) { return smem_u32(bars + 2 * S + 2 + i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  const uint32_t tcols = dense_tmem_cols(NTOK);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(accf_bar(i), 1);
+      mbar_init(acce_bar(i), 4);  // one arrival per epilogue warp
+    }
+    mbar_init_fence();
+  }
+  if (warp == kDenseMmaWarp) tmem_alloc(smem_u32(tmem_slot), tcols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int row_tiles = DP.row_tiles;
+
+  if (warp == kDenseTmaWarp) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_evict_first_policy();
+      const uint64_t pol_x = l2_evict_normal_policy();
+      const uint32_t tx = (uint32_t)(WB + (kSplit ? 2 : 1) * XB);
+      long long ra, rb;
+      ws_left_range(P, blockIdx.x, gridDim.x, &ra, &rb);
+      const int dp_b = blockIdx.x * P.q;
+      const int nchunks = (int)(rb - ra) + P.q * P.C;
+      bool dead = false;
+      uint32_t last_ph[kDenseMaxStagesDev];  // parity of the last copy issued into each stage
+      uint32_t issued = 0;                   // stages that received a copy (bit mask)
+      // The first stages' weights before the dependency wait, their X after it.
+      const int pre = nchunks < S ? nchunks : S;
+      Cursor q;
+      ws_cursor_init(q, P, ra, rb, dp_b);
+      Cursor q0 = q;
+      DRing rp;
+      for (int j = 0; j < pre; ++j) {
+        const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
+        const int trow = q.t % row_tiles;
+        mbar_arrive_expect_tx(full_bar(rp.st), tx);
+        tma_load_3d(stage, a.tmap_w, 0, trow * 128, q.kc * KC / 64, full_bar(rp.st), pol_w);
+        last_ph[rp.st] = rp.ph;
+        issued |= 1u << rp.st;
+        ws_cursor_next(q, P, dp_b);
+        rp.advance(S);
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      {
+        DRing r2;
+        Cursor c = q0;
+        for (int j = 0; j < pre; ++j) {
+          const uint32_t stage = smem_u32(sm + (size_t)r2.st * SB);
+          const int jt = c.t / row_tiles;
+          tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, c.kc * KC / 64, full_bar(r2.st), pol_x);
+          if constexpr (kSplit)
+            tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, c.kc * KC / 64, full_bar(r2.st), pol_x);
+          ws_cursor_next(c, P, dp_b);
+          r2.advance(S);
+        }
+      }
+      for (int j = pre; j < nchunks; ++j) {
+        if (!dead) dead = !mbar_wait(empty_bar(rp.st), rp.ph ^ 1, a.status);
+        if (dead) break;
+        const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
+        const int trow = q.t % row_tiles, jt = q.t / row_tiles;
+        mbar_arrive_expect_tx(full_bar(rp.st), tx);
+        tma_load_3d(stage, a.tmap_w, 0, trow * 128, q.kc * KC / 64, full_bar(rp.st), pol_w);
+        tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, q.kc * KC / 64, full_bar(rp.st), pol_x);
+        if constexpr (kSplit)
+          tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, q.kc * KC / 64, full_bar(rp.st), pol_x);
+        last_ph[rp.st] = rp.ph;
+        issued |= 1u << rp.st;
+        ws_cursor_next(q, P, dp_b);
+        rp.advance(S);
+      }
+      // No copy may still be landing in this CTA's shared memory when it
+      // exits: wait (bounded) for the last copy of every stage.  Immediate in
+      // normal operation, where the MMA thread has consumed them all.
+      for (int st = 0; st < S; ++st)
+        if ((issued >> st) & 1u) mbar_wait(full_bar(st), last_ph[st], a.status);
+      // L2 prefetch of the next GEMM's first weight chunks for this CTA index.
+      if (a.next_tmap_w != nullptr && blockIdx.x < a.next_plan.ws.grid) {
+        const GemvPlan& Pn = a.next_plan.ws;
+        long long na, nb;
+        ws_left_range(Pn, blockIdx.x, Pn.grid, &na, &nb);
+        const int ndp = blockIdx.x * Pn.q;
+        int nn = (int)(nb - na) + Pn.q * Pn.C;
+        if (nn > 16) nn = 16;
+        Cursor c;
+        ws_cursor_init(c, Pn, na, nb, ndp);
+        for (int j = 0; j < nn; ++j) {
+          tma_prefetch_3d(a.next_tmap_w, 0, (c.t % a.next_plan.row_tiles) * 128, c.kc * a.next_plan.kc / 64);
+          ws_cursor_next(c, Pn, ndp);
+        }
+      }
+    }
+  } else if (warp == kDenseMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    pdl_launch_dependents();
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc(kSplit, NTOK);
+      DRing rp;
+      int seg = 0;
+      bool dead = false;
+      dense_for_segments(P, [&](int u, int kc0, int kc1, int) {
+        (void)u;
+        const int buf = seg & 1;
+        if (seg >= 2 && !dead) dead = !mbar_wait(acce_bar(buf), ((seg >> 1) - 1) & 1, a.status);
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * NTOK);
+        for (int kc = kc0; kc < kc1; ++kc) {
+          if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);
+          if (!dead) {
+            tc_fence_after();
+            const uint32_t wbase = smem_u32(sm + (size_t)rp.st * SB);
+            const uint32_t xbase = wbase + (uint32_t)WB;
+#pragma unroll 1
+            for (int kb = 0; kb < KC / 64; ++kb) {
+#pragma unroll
+              for (int k16 = 0; k16 < 4; ++k16) {
+                const uint64_t dw = umma_desc_sw128(wbase + kb * (128 * 128) + k16 * 32);
+                const uint32_t xo = (uint32_t)(kb * NTOK * 128 + k16 * 32);
+                const uint32_t acc = (kc > kc0 || kb > 0 || k16 > 0) ? 1u : 0u;
+                umma_f16(d, dw, umma_desc_sw128(xbase + xo), idesc, acc);
+                if constexpr (kSplit) umma_f16(d, dw, umma_desc_sw128(xbase + (uint32_t)XB + xo), idesc, 1u);
+              }
+            }
+            umma_commit(empty_bar(rp.st));
+          }
+          rp.advance(S);
+        }
+        if (!dead) umma_commit(accf_bar(buf));
+        ++seg;
+      });
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    pdl_wait();
+    pdl_launch_dependents();
+    const int et = threadIdx.x - kDenseEpiWarp0 * 32;  // 0..127
+    const int qd = warp & 3;                            // TMEM lane quarter
+    const int r = 32 * qd + lane;                       // weight row within the tile
+    const int M = a.M, N = a.N;
+    int seg = 0;
+    bool dead = false;
+    dense_for_segments(P, [&](int u, int kc0, int kc1, int j_slot) {
+      (void)kc0; (void)kc1;
+      const int buf = seg & 1;
+      const int t = u;
+      const int trow = t % row_tiles, jt = t / row_tiles;
+      const int n = trow * 128 + r;
+      const int m0 = jt * NTOK;
+      const int mrows = min(NTOK, M - m0);
+      const int contrib = ws_unit_contrib(u, P, gridDim.x);
+      const float bias = Act<ACT>::to_f(static_cast<const ACT*>(a.bias)[n]);
+      if (!dead) dead = !mbar_wait(accf_bar(buf), (seg >> 1) & 1, a.status);
+      dead = __any_sync(0xffffffffu, dead);  // tcgen05.ld below is warp-collective
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * NTOK);
+      // Region epilogue of 16 token columns [m0 + c16, m0 + c16 + 16) of row n.
+      auto epi16 = [&](int c16, const float (&v)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int mi = c16 + i;  // column within the tile
+          const bool ok = mi < mrows;
+          const int m = m0 + mi;
+          float y = v[i] + bias;
+          if constexpr (R == Region::LnQkv) {
+            if (ok) {
+              const int H = a.H;
+              const int part = n / H, within = n - part * H;
+              if (part == 0) {
+                a.out_f32[(size_t)m * H + within] = y;
+              } else {
+                const int b = m / a.T;
+                const int pos = a.past_len[b] + (m - b * a.T);
+                if (pos >= 0 && pos < a.max_len) {
+                  const int head = within / a.head_dim, dim = within - head * a.head_dim;
+                  ACT* cache = static_cast<ACT*>(part == 1 ? a.k_cache : a.v_cache);
+                  cache[(((size_t)b * a.heads + head) * a.max_len + pos) * a.head_dim + dim] = Act<ACT>::from_f(y);
+                } else {
+                  atomicOr(a.status, kFlagCacheOverflow);
+                }
+              }
+            }
+          } else if constexpr (R == Region::FfnUp) {
+            if (ok) {
+              y = gelu_tanh(y);
+              const ACT h = Act<ACT>::from_f(y);
+              static_cast<ACT*>(a.out_act)[(size_t)m * N + n] = h;
+              if constexpr (kSplit) static_cast<ACT*>(a.out_lo)[(size_t)m * N + n] = Act<ACT>::from_f(y - Act<ACT>::to_f(h));
+            }
+          } else {
+            if constexpr (R == Region::OprojRes) {
+              if (ok) {
+                y += Act<ACT>::to_f(static_cast<const ACT*>(a.resid_act)[(size_t)m * N + n]);
+                a.out_f32[(size_t)m * N + n] = y;
+              }
+            } else {
+              if (ok) {
+                y += a.resid_f32[(size_t)m * N + n];
+                const ACT h = Act<ACT>::from_f(y);
+                static_cast<ACT*>(a.out_act)[(size_t)m * N + n] = h;
+                y = Act<ACT>::to_f(h);
+              }
+            }
+            if constexpr (kStats) {
+              // (sum, M2) over each 16-row group of the tile (lanes 0..15, 16..31)
+              if (a.stats_out != nullptr && mi < mrows) {
+                float s = y;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                const float mean = s * (1.0f / 16.0f);
+                float dd = (y - mean) * (y - mean);
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+                if ((lane & 15) == 0) {
+                  a.stats_out[((size_t)(n >> 4) * M + m) * 2] = s;
+                  a.stats_out[((size_t)(n >> 4) * M + m) * 2 + 1] = dd;
+                }
+              }
+            }
+          }
+        }
+      };
+      if (contrib == 1) {
+        for (int c16 = 0; c16 < mrows; c16 += 16) {
+          float v[16];
+          if (!dead) tmem_ld16(tbase + (uint32_t)c16, v);
+          epi16(c16, v);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(buf));
+      } else {
+        // publish this CTA's partial tile, count, the last contributor finishes
+        // (only leftover tiles, u >= U_dp, have several contributors)
+        float* pbase = a.partials + (size_t)(t - P.U_dp) * P.maxc * NTOK * 128;
+        for (int c16 = 0; c16 < mrows; c16 += 16) {
+          float v[16];
+          if (!dead) tmem_ld16(tbase + (uint32_t)c16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c16 + i < mrows) pbase[((size_t)j_slot * NTOK + c16 + i) * 128 + r] = v[i];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(buf));
+        // every epilogue thread's partial stores, then one release-acquire arrival
+        __threadfence();
+        named_bar_sync(kDenseBarEpi, kDenseEpiThreads);
+        if (et == 0) *last_flag = (atomic_add_acq_rel_gpu(&a.counters[t], 1) == contrib - 1);
+        named_bar_sync(kDenseBarEpi, kDenseEpiThreads);
+        const bool last = *last_flag != 0;
+        if (last) {
+          __threadfence();
+          for (int c16 = 0; c16 < mrows; c16 += 16) {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            for (int js = 0; js < contrib; ++js) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (c16 + i < mrows) v[i] += ld_cg(pbase + ((size_t)js * NTOK + c16 + i) * 128 + r);
+            }
+            epi16(c16, v);
+          }
+          if (et == 0) a.counters[t] = 0;
+        }
+        named_bar_sync(kDenseBarEpi, kDenseEpiThreads);  // last_flag is read before the next segment writes it
+      }
+      ++seg;
+    });
+    if constexpr (R == Region::FfnDown) {
+      if (a.seq_len_inc != nullptr && blockIdx.x == 0 && warp == kDenseEpiWarp0)
+        for (int b = lane; b < a.B; b += 32) a.seq_len_inc[b] += 1;
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kDenseMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tcols);
+  }
+}
+
+}  // namespace ds

@@ -8,13 +8,23 @@
 // the FFN-down kernel's epilogue.  The all-reduce boundaries of §3.1 collapse on
 // one GPU; they remain as the kernel boundaries.
 //
+// Two GEMM paths serve the regions (§3 intro: the skinny GEMM at small batch):
+//  * up to 8 rows (B * T), and for int8 weights up to 64, the streaming GEMV
+//    kernels (gemv_impl.cuh) with the LayerNorm fused into their prologue;
+//  * above 8 rows with fp16 / bf16 weights, the tensor-core tile kernels
+//    (dense_impl.cuh, tcgen05 + TMEM), each LayerNorm run by a small row
+//    normalisation kernel that writes the tensor-core operand.
+//
 // Host-side responsibilities here: argument validation before any launch,
-// workspace layout, the per-GEMV work split, the launch chain with
-// programmatic dependent launch, CUDA-graph capture/replay of a stack step,
-// and per-region event timing in profile mode.
+// workspace layout, the work splits, the launch chain with programmatic
+// dependent launch, CUDA-graph capture/replay of a stack step, and per-region
+// event timing in profile mode.
+#include <cuda.h>
+
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstddef>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -41,11 +51,14 @@ ds_status cuda_fail(cudaError_t e, const char* what) {
 }
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kGemvMaxRows = 64;   // streaming GEMV kernels: up to 8 MMA column tiles
+constexpr int kTileMinRows = 9;    // fp16 / bf16 weights: tensor-core tiles from 9 rows
+constexpr int kTileMaxRows = 4096; // rows (B * T) of one tile-path call
+
 struct DevInfo {
   bool ready = false;
   int sms = 0;
-  int max_smem = 0;     // opt-in shared memory of one block
-  int smem_per_sm = 0;  // shared memory of one SM (shared by its resident blocks)
+  int max_smem = 0;  // opt-in shared memory of one block
 };
 std::mutex g_dev_mu;
 DevInfo g_dev[64];
@@ -63,35 +76,17 @@ ds_status device_info(int* dev_out, DevInfo* out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
     e = cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(max smem)");
-    e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem per SM)");
     e = prepare_region_kernels(d.max_smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(region kernels)");
+    e = prepare_dense_kernels(d.max_smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tile kernels)");
     e = prepare_attention_kernels(d.max_smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention kernel)");
-    e = prepare_step_kernels(d.max_smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(step kernel)");
     d.ready = true;
   }
   *dev_out = dev;
   *out = d;
   return DS_OK;
-}
-
-int ctas_per_sm_knob() {
-  const char* s = std::getenv("DS_GEMV_CTAS_PER_SM");
-  if (s == nullptr) return 1;
-  const int v = std::atoi(s);
-  return (v >= 1 && v <= 4) ? v : 1;
-}
-
-// A stack step runs as the chain of region kernels (graph-captured, PDL
-// overlapped); DS_STEP_KERNEL=1 selects the persistent step kernel instead
-// where it can run (one cooperative launch per step; measured slower on
-// GB300, kept for comparison).
-bool step_kernel_knob() {
-  const char* s = std::getenv("DS_STEP_KERNEL");
-  return s != nullptr && std::atoi(s) != 0;
 }
 
 WKind wkind(ds_dtype d) { return d == DS_I8 ? WKind::I8 : (d == DS_BF16 ? WKind::BF16 : WKind::F16); }
@@ -105,68 +100,73 @@ struct ds_layer {
   int device = 0;
   int sms = 0;
   int max_smem = 0;
-  int smem_per_sm = 0;
-  int ctas_per_sm = 1;
   // TMA tensor maps in device memory, kTensorMapBytes each: weights of QKV,
-  // O-proj, FFN-up, FFN-down, then (int8) their scales in the same order, one
-  // map per k-blocks-per-step choice (1, 2, 4): a map's box is one chunk.
+  // O-proj, FFN-up, FFN-down for the GEMV path, one map per k-blocks-per-step
+  // choice (1, 2, 4: a map's box is one chunk); then (int8) their scales in
+  // the same order; then (fp16 / bf16) the tile maps of the four matrices for
+  // ring stages of 64 and of 128 along K.
   unsigned char* tmaps = nullptr;
   static int nblk_index(int nblk) { return nblk == 4 ? 2 : (nblk == 2 ? 1 : 0); }
   const void* tmap_w(int r, int nblk) const { return tmaps + (size_t)(3 * r + nblk_index(nblk)) * kTensorMapBytes; }
   const void* tmap_s(int r, int nblk) const {
     return cfg.weight_dtype == DS_I8 ? tmaps + (size_t)(12 + 3 * r + nblk_index(nblk)) * kTensorMapBytes : nullptr;
   }
+  const void* tmap_tile(int r, int kc) const {
+    return tmaps + (size_t)(24 + 2 * r + (kc == 128 ? 1 : 0)) * kTensorMapBytes;
+  }
   // int8 scale group length of matrix r (0 QKV, 1 O-proj, 2 FFN-up, 3 FFN-down):
   // the FFN matrices take half the length under mlp_extra_grouping.
   int qgroup(int r) const { return (r >= 2 && cfg.mlp_extra_grouping == 1) ? cfg.quant_group / 2 : cfg.quant_group; }
+  bool tile_capable() const { return cfg.weight_dtype != DS_I8; }
+  int max_rows() const { return tile_capable() ? kTileMaxRows : kGemvMaxRows; }
 };
 
 namespace {
 
 struct Plans {
-  GemvPlan qkv, o, up, down;  // region kernels (ds_layer_forward, profile mode)
-  GemvPlan step[4];           // persistent step kernel: one CTA per SM for every phase
-  bool step_ok = false;
+  bool tile = false;          // tensor-core tile path
+  GemvPlan qkv, o, up, down;  // streaming GEMV path
+  DensePlan tq, to, tu, td;   // tile path
 };
 
-bool make_plans(const ds_layer& L, int M, int B, Plans* p) {
-  (void)B;
+bool use_tile_path(const ds_layer& L, int M) { return L.tile_capable() && M >= kTileMinRows; }
+
+bool make_plans(const ds_layer& L, int M, Plans* p) {
   const int H = L.cfg.hidden, F = L.cfg.ffn;
   const WKind wk = wkind(L.cfg.weight_dtype);
   const ActKind ak = akind(L.cfg.act_dtype);
-  // Several CTAs per SM share its shared memory (1 KB of it reserved per CTA).
-  const int cps = L.ctas_per_sm;
-  const int smem = cps == 1 ? L.max_smem : std::min(L.max_smem, L.smem_per_sm / cps - 1024);
-  if (!gemv_make_plan(wk, ak, 3 * H, H, M, L.sms, cps, smem, &p->qkv)) return false;
-  if (!gemv_make_plan(wk, ak, H, H, M, L.sms, cps, smem, &p->o)) return false;
-  if (!gemv_make_plan(wk, ak, F, H, M, L.sms, cps, smem, &p->up)) return false;
-  if (!gemv_make_plan(wk, ak, H, F, M, L.sms, cps, smem, &p->down)) return false;
+  if (M < 1 || M > L.max_rows()) return false;
+  p->tile = use_tile_path(L, M);
+  if (p->tile) {
+    return dense_make_plan(ak, 3 * H, H, M, L.sms, L.max_smem, &p->tq) &&
+           dense_make_plan(ak, H, H, M, L.sms, L.max_smem, &p->to) &&
+           dense_make_plan(ak, F, H, M, L.sms, L.max_smem, &p->tu) &&
+           dense_make_plan(ak, H, F, M, L.sms, L.max_smem, &p->td);
+  }
+  if (!gemv_make_plan(wk, ak, 3 * H, H, M, L.sms, L.max_smem, &p->qkv)) return false;
+  if (!gemv_make_plan(wk, ak, H, H, M, L.sms, L.max_smem, &p->o)) return false;
+  if (!gemv_make_plan(wk, ak, F, H, M, L.sms, L.max_smem, &p->up)) return false;
+  if (!gemv_make_plan(wk, ak, H, F, M, L.sms, L.max_smem, &p->down)) return false;
   if (wk == WKind::I8) {  // the scale box of a chunk must hold at least 8 groups
     const GemvPlan* pl[4] = {&p->qkv, &p->o, &p->up, &p->down};
     for (int i = 0; i < 4; ++i)
       if (pl[i]->chunk_k / L.qgroup(i) < 8) return false;
   }
-  const int NK[4][2] = {{3 * H, H}, {H, H}, {F, H}, {H, F}};
-  p->step_ok = true;
-  for (int i = 0; i < 4; ++i)
-    if (!gemv_make_plan(wk, ak, NK[i][0], NK[i][1], M, L.sms, 1, L.max_smem, &p->step[i], true) ||
-        (wk == WKind::I8 && p->step[i].chunk_k / L.qgroup(i) < 8))
-      p->step_ok = false;
   return true;
 }
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t status, cnt_gemv, grid_bar, attn_cnt, q, o, x1, g, stats_a, stats_b, partials, attn_part, act,
-      total;
+  size_t status, cnt, q, o, x1, g, stats_a, stats_b, partials, op_a_hi, op_a_lo, op_b_hi, op_b_lo, act, total;
 };
 
-// Workspace regions, each 256-byte aligned.  Counters first so that a
-// zero-fill of the first bytes is enough to reset them.
+// Workspace regions, each 256-byte aligned.  The status word and the arrival
+// counters come first so that a zero-fill of the first bytes resets them.
 WsLayout ws_layout(const ds_layer& L, int B, int T, const Plans& p) {
-  const int H = L.cfg.hidden, F = L.cfg.ffn, nh = L.cfg.heads, d = H / nh;
+  const int H = L.cfg.hidden, F = L.cfg.ffn;
   const size_t M = (size_t)B * T;
+  const bool split = L.cfg.act_dtype == DS_BF16;
   WsLayout w{};
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -175,25 +175,36 @@ WsLayout ws_layout(const ds_layer& L, int B, int T, const Plans& p) {
     return o;
   };
   w.status = take(256);
-  const size_t tiles_max = (size_t)std::max(3 * H, F) / 16;
-  w.cnt_gemv = take(tiles_max * sizeof(int));
-  w.grid_bar = take(sizeof(unsigned));
-  w.attn_cnt = take((size_t)B * nh * sizeof(int));
+  size_t tiles = (size_t)std::max(3 * H, F) / 16;
+  if (p.tile) {
+    const DensePlan* d[4] = {&p.tq, &p.to, &p.tu, &p.td};
+    tiles = 0;
+    for (const DensePlan* x : d) tiles = std::max(tiles, (size_t)x->ws.tiles);
+  }
+  w.cnt = take(tiles * sizeof(int));
   w.q = take(M * H * 4);
-  w.o = take(M * H * 4);
   w.x1 = take(M * H * 4);
-  w.g = take(M * F * 4);
   w.stats_a = take((size_t)(H / 16) * M * 2 * 4);
   w.stats_b = take((size_t)(H / 16) * M * 2 * 4);
   size_t part = 0;
-  const GemvPlan* ps[4] = {&p.qkv, &p.o, &p.up, &p.down};
-  for (int i = 0; i < 4; ++i) {
-    part = std::max(part, (size_t)ps[i]->tiles * ps[i]->KS * ps[i]->maxc * 16 * M * 4);
-    const GemvPlan& q = p.step[i];
-    if (p.step_ok) part = std::max(part, (size_t)q.tiles * q.KS * q.maxc * 16 * M * 4);
+  if (p.tile) {
+    w.o = w.g = 0;
+    const DensePlan* d[4] = {&p.tq, &p.to, &p.tu, &p.td};
+    for (const DensePlan* x : d)  // only leftover tiles (u >= U_dp) publish partials
+      part = std::max(part, (size_t)(x->ws.units - x->ws.U_dp) * x->ws.maxc * x->ntok * 128 * 4);
+    w.partials = take(part);
+    w.op_a_hi = take(M * H * 2);
+    w.op_a_lo = split ? take(M * H * 2) : 0;
+    w.op_b_hi = take(M * std::max(H, F) * 2);
+    w.op_b_lo = split ? take(M * std::max(H, F) * 2) : 0;
+  } else {
+    w.o = take(M * H * 4);
+    w.g = take(M * F * 4);
+    const GemvPlan* ps[4] = {&p.qkv, &p.o, &p.up, &p.down};
+    for (const GemvPlan* g : ps) part = std::max(part, (size_t)g->tiles * g->KS * g->maxc * 16 * M * 4);
+    w.partials = take(part);
+    w.op_a_hi = w.op_a_lo = w.op_b_hi = w.op_b_lo = 0;
   }
-  w.partials = take(part);
-  w.attn_part = take((size_t)B * nh * step_attn_nsplit(B, nh, 1 << 30, L.sms) * (d + 2) * 4);
   w.act = take(2 * M * H * 2);
   w.total = off;
   return w;
@@ -236,35 +247,57 @@ ds_status validate_config(const ds_layer_config* c) {
 
 struct Bufs {
   unsigned* status;
-  int* cnt_gemv;
-  unsigned* grid_bar;
-  int* attn_cnt;
-  float *q, *o, *x1, *g, *stats_a, *stats_b, *partials, *attn_part;
+  int* cnt;
+  float *q, *o, *x1, *g, *stats_a, *stats_b, *partials;
+  void *op_a_hi, *op_a_lo, *op_b_hi, *op_b_lo;
   char* act;
 };
 
 Bufs bufs_of(void* ws, const WsLayout& w) {
   char* b = static_cast<char*>(ws);
+  auto at = [&](size_t off) -> void* { return off ? static_cast<void*>(b + off) : nullptr; };
   Bufs r;
   r.status = reinterpret_cast<unsigned*>(b + w.status);
-  r.cnt_gemv = reinterpret_cast<int*>(b + w.cnt_gemv);
-  r.grid_bar = reinterpret_cast<unsigned*>(b + w.grid_bar);
-  r.attn_cnt = reinterpret_cast<int*>(b + w.attn_cnt);
-  r.attn_part = reinterpret_cast<float*>(b + w.attn_part);
-  r.q = reinterpret_cast<float*>(b + w.q);
-  r.o = reinterpret_cast<float*>(b + w.o);
-  r.x1 = reinterpret_cast<float*>(b + w.x1);
-  r.g = reinterpret_cast<float*>(b + w.g);
-  r.stats_a = reinterpret_cast<float*>(b + w.stats_a);
-  r.stats_b = reinterpret_cast<float*>(b + w.stats_b);
-  r.partials = reinterpret_cast<float*>(b + w.partials);
+  r.cnt = reinterpret_cast<int*>(b + w.cnt);
+  r.q = static_cast<float*>(at(w.q));
+  r.o = static_cast<float*>(at(w.o));
+  r.x1 = static_cast<float*>(at(w.x1));
+  r.g = static_cast<float*>(at(w.g));
+  r.stats_a = static_cast<float*>(at(w.stats_a));
+  r.stats_b = static_cast<float*>(at(w.stats_b));
+  r.partials = static_cast<float*>(at(w.partials));
+  r.op_a_hi = at(w.op_a_hi);
+  r.op_a_lo = at(w.op_a_lo);
+  r.op_b_hi = at(w.op_b_hi);
+  r.op_b_lo = at(w.op_b_lo);
   r.act = b + w.act;
   return r;
 }
 
+// Tensor maps of the tile path's activation operands for one workspace and
+// row count: op_a with K = H, op_b with K = H (attention output) and K = F
+// (GeLU output); hi and (bf16) lo parts.
+struct alignas(64) XMaps {
+  unsigned char a_hi[kTensorMapBytes], a_lo[kTensorMapBytes];
+  unsigned char bh_hi[kTensorMapBytes], bh_lo[kTensorMapBytes];
+  unsigned char bf_hi[kTensorMapBytes], bf_lo[kTensorMapBytes];
+};
+
+bool make_xmaps(const ds_layer& L, const Plans& p, const Bufs& bf, int M, XMaps* x) {
+  const int H = L.cfg.hidden, F = L.cfg.ffn, nt = p.tq.ntok, kc = p.tq.kc;
+  const bool split = L.cfg.act_dtype == DS_BF16;
+  std::memset(x, 0, sizeof(*x));
+  bool ok = encode_tile_map(x->a_hi, bf.op_a_hi, M, H, nt, kc) && encode_tile_map(x->bh_hi, bf.op_b_hi, M, H, nt, kc) &&
+            encode_tile_map(x->bf_hi, bf.op_b_hi, M, F, nt, kc);
+  if (ok && split)
+    ok = encode_tile_map(x->a_lo, bf.op_a_lo, M, H, nt, kc) && encode_tile_map(x->bh_lo, bf.op_b_lo, M, H, nt, kc) &&
+         encode_tile_map(x->bf_lo, bf.op_b_lo, M, F, nt, kc);
+  return ok;
+}
+
 // Optional per-kernel event pairs (profile mode).
 struct EventSink {
-  std::vector<cudaEvent_t>* ev = nullptr;  // 2 per launch
+  std::vector<cudaEvent_t>* ev = nullptr;  // 2 per region
   size_t next = 0;
 };
 
@@ -274,24 +307,196 @@ cudaError_t record(EventSink* es, cudaStream_t st) {
   return cudaEventRecord((*es->ev)[es->next++], st);
 }
 
-// Enqueues the five region kernels of one layer.
-cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, const void* x_in,
-                          void* x_out, int B, int T, void* kc, void* vc, int max_len,
-                          const int32_t* past_len, const float* stats_in, float* stats_out,
-                          int32_t* seq_inc, const ds_layer* next, bool first, cudaStream_t st,
-                          bool pdl, EventSink* es) {
+// A captured kernel node whose arguments hold the caller's x_in or x_out: the
+// graph is kept for these pointers being replaced in place (no re-capture).
+struct PatchNode {
+  cudaGraphNode_t node = nullptr;
+  int arg_index = 0;                 // which kernel parameter is the argument struct
+  std::vector<unsigned char> args;   // its bytes as captured
+  std::vector<size_t> in_offsets;    // offsets of x_in pointers inside it
+  std::vector<size_t> out_offsets;   // offsets of x_out pointers
+};
+
+// During stream capture: records the node just added to the capture.
+template <typename A>
+cudaError_t record_patch(std::vector<PatchNode>* rec, cudaStream_t st, int arg_index, const A& args,
+                         std::vector<size_t> in_off, std::vector<size_t> out_off) {
+  if (rec == nullptr || (in_off.empty() && out_off.empty())) return cudaSuccess;
+  cudaStreamCaptureStatus cs;
+  const cudaGraphNode_t* deps = nullptr;
+  size_t nd = 0;
+  cudaError_t e = cudaStreamGetCaptureInfo(st, &cs, nullptr, nullptr, &deps, nullptr, &nd);
+  if (e != cudaSuccess) return e;
+  if (cs != cudaStreamCaptureStatusActive || nd != 1) return cudaErrorStreamCaptureUnsupported;
+  PatchNode p;
+  p.node = deps[0];
+  p.arg_index = arg_index;
+  p.args.resize(sizeof(A));
+  std::memcpy(p.args.data(), &args, sizeof(A));
+  p.in_offsets = std::move(in_off);
+  p.out_offsets = std::move(out_off);
+  rec->push_back(std::move(p));
+  return cudaSuccess;
+}
+
+struct LayerIO {
+  const void* x_in;
+  void* x_out;
+  bool in_is_caller;   // x_in is the caller's buffer (record for patching)
+  bool out_is_caller;  // x_out is the caller's buffer
+};
+
+// Enqueues the region kernels of one layer.
+cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, const XMaps* xm, const LayerIO& io,
+                          int B, int T, void* kc, void* vc, int max_len, const int32_t* past_len,
+                          const float* stats_in, float* stats_out, int32_t* seq_inc, const ds_layer* next,
+                          bool first, cudaStream_t st, bool pdl, EventSink* es, std::vector<PatchNode>* rec) {
   const ds_layer_config& c = L.cfg;
   const int H = c.hidden, F = c.ffn, nh = c.heads, d = H / nh, M = B * T;
   const WKind wk = wkind(c.weight_dtype);
   const ActKind ak = akind(c.act_dtype);
+  const bool split = ak == ActKind::BF16;
   cudaError_t e;
+  auto in_if = [&](size_t off) { return io.in_is_caller ? std::vector<size_t>{off} : std::vector<size_t>{}; };
+  auto out_if = [&](size_t off) { return io.out_is_caller ? std::vector<size_t>{off} : std::vector<size_t>{}; };
+
+  AttnArgs ra;
+  ra.q = bf.q;
+  ra.k_cache = kc;
+  ra.v_cache = vc;
+  ra.past_len = past_len;
+  ra.B = B;
+  ra.T = T;
+  ra.heads = nh;
+  ra.head_dim = d;
+  ra.max_len = max_len;
+  ra.H = H;
+  ra.nsplit = attn_nsplit(B, nh, max_len, L.sms);
+  ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  ra.stage_keys = attn_stage_keys(d, max_len, ra.nsplit);
+  ra.smem = attn_smem_bytes(d, ra.stage_keys);
+  ra.status = bf.status;
+
+  if (P.tile) {
+    DenseArgs base;
+    base.M = M;
+    base.B = B;
+    base.T = T;
+    base.partials = bf.partials;
+    base.counters = bf.cnt;
+    base.status = bf.status;
+    base.H = H;
+    // R1: LayerNorm1 (row kernel) + QKV + bias + KV append
+    LnPrepArgs p1;
+    p1.M = M;
+    p1.K = H;
+    p1.eps = c.ln_eps;
+    p1.x_act = io.x_in;
+    p1.stats_in = stats_in;
+    p1.ln_g = L.w.ln1_g;
+    p1.ln_b = L.w.ln1_b;
+    p1.out_hi = bf.op_a_hi;
+    p1.out_lo = bf.op_a_lo;
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    // The first kernel of an enqueue waits for everything before it (no
+    // programmatic overlap): later kernels may then read past_len early.
+    if ((e = launch_ln_prep(ak, p1, st, pdl && !first)) != cudaSuccess) return e;
+    if ((e = record_patch(rec, st, 0, p1, in_if(offsetof(LnPrepArgs, x_act)), {})) != cudaSuccess) return e;
+    DenseArgs r1 = base;
+    r1.tmap_w = L.tmap_tile(0, P.tq.kc);
+    r1.N = 3 * H;
+    r1.K = H;
+    r1.plan = P.tq;
+    r1.bias = L.w.b_qkv;
+    r1.out_f32 = bf.q;
+    r1.k_cache = kc;
+    r1.v_cache = vc;
+    r1.heads = nh;
+    r1.head_dim = d;
+    r1.max_len = max_len;
+    r1.past_len = past_len;
+    r1.next_tmap_w = L.tmap_tile(1, P.to.kc);
+    r1.next_plan = P.to;
+    if ((e = launch_dense(Region::LnQkv, ak, r1, xm->a_hi, split ? xm->a_lo : nullptr, st, pdl)) != cudaSuccess)
+      return e;
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    // R2: attention, output in the operand format
+    ra.out_hi = bf.op_b_hi;
+    ra.out_lo = bf.op_b_lo;
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    if ((e = launch_attention(ak, ra, st, pdl)) != cudaSuccess) return e;
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    // R3: O-proj + bias + residual + LayerNorm2 statistics
+    DenseArgs r3 = base;
+    r3.tmap_w = L.tmap_tile(1, P.to.kc);
+    r3.N = H;
+    r3.K = H;
+    r3.plan = P.to;
+    r3.bias = L.w.b_o;
+    r3.resid_act = io.x_in;
+    r3.out_f32 = bf.x1;
+    r3.stats_out = bf.stats_a;
+    r3.next_tmap_w = L.tmap_tile(2, P.tu.kc);
+    r3.next_plan = P.tu;
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    if ((e = launch_dense(Region::OprojRes, ak, r3, xm->bh_hi, split ? xm->bh_lo : nullptr, st, pdl)) != cudaSuccess)
+      return e;
+    if ((e = record_patch(rec, st, 2, r3, in_if(offsetof(DenseArgs, resid_act)), {})) != cudaSuccess) return e;
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    // R4a: LayerNorm2 (row kernel) + FFN-up + bias + GeLU
+    LnPrepArgs p2;
+    p2.M = M;
+    p2.K = H;
+    p2.eps = c.ln_eps;
+    p2.x_f32 = bf.x1;
+    p2.stats_in = bf.stats_a;
+    p2.ln_g = L.w.ln2_g;
+    p2.ln_b = L.w.ln2_b;
+    p2.out_hi = bf.op_a_hi;
+    p2.out_lo = bf.op_a_lo;
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    if ((e = launch_ln_prep(ak, p2, st, pdl)) != cudaSuccess) return e;
+    DenseArgs r4 = base;
+    r4.tmap_w = L.tmap_tile(2, P.tu.kc);
+    r4.N = F;
+    r4.K = H;
+    r4.plan = P.tu;
+    r4.bias = L.w.b_fc1;
+    r4.out_act = bf.op_b_hi;
+    r4.out_lo = bf.op_b_lo;
+    r4.next_tmap_w = L.tmap_tile(3, P.td.kc);
+    r4.next_plan = P.td;
+    if ((e = launch_dense(Region::FfnUp, ak, r4, xm->a_hi, split ? xm->a_lo : nullptr, st, pdl)) != cudaSuccess)
+      return e;
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    // R4b: FFN-down + bias + residual (+ next LayerNorm statistics)
+    DenseArgs r5 = base;
+    r5.tmap_w = L.tmap_tile(3, P.td.kc);
+    r5.N = H;
+    r5.K = F;
+    r5.plan = P.td;
+    r5.bias = L.w.b_fc2;
+    r5.resid_f32 = bf.x1;
+    r5.out_act = io.x_out;
+    r5.stats_out = stats_out;
+    r5.seq_len_inc = seq_inc;
+    if (next != nullptr) {
+      r5.next_tmap_w = next->tmap_tile(0, P.tq.kc);
+      r5.next_plan = P.tq;
+    }
+    if ((e = record(es, st)) != cudaSuccess) return e;
+    if ((e = launch_dense(Region::FfnDown, ak, r5, xm->bf_hi, split ? xm->bf_lo : nullptr, st, pdl)) != cudaSuccess)
+      return e;
+    if ((e = record_patch(rec, st, 2, r5, {}, out_if(offsetof(DenseArgs, out_act)))) != cudaSuccess) return e;
+    return record(es, st);
+  }
 
   RegionArgs base;
   base.M = M;
   base.B = B;
   base.T = T;
   base.partials = bf.partials;
-  base.counters = bf.cnt_gemv;
+  base.counters = bf.cnt;
   base.eps = c.ln_eps;
   base.status = bf.status;
   base.H = H;
@@ -311,7 +516,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   r1.K = H;
   r1.plan = P.qkv;
   r1.bias = L.w.b_qkv;
-  r1.x_act = x_in;
+  r1.x_act = io.x_in;
   r1.ln_g = L.w.ln1_g;
   r1.ln_b = L.w.ln1_b;
   r1.stats_in = stats_in;
@@ -326,26 +531,11 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   // The first kernel of an enqueue waits for everything before it (no
   // programmatic overlap): later kernels may then read past_len early.
   if ((e = launch_region(Region::LnQkv, wk, ak, r1, st, pdl && !first)) != cudaSuccess) return e;
+  if ((e = record_patch(rec, st, 0, r1, in_if(offsetof(RegionArgs, x_act)), {})) != cudaSuccess) return e;
   if ((e = record(es, st)) != cudaSuccess) return e;
 
   // R2: attention
-  AttnArgs ra;
-  ra.q = bf.q;
-  ra.k_cache = kc;
-  ra.v_cache = vc;
-  ra.past_len = past_len;
-  ra.B = B;
-  ra.T = T;
-  ra.heads = nh;
-  ra.head_dim = d;
-  ra.max_len = max_len;
-  ra.H = H;
-  ra.nsplit = attn_nsplit(B, nh, max_len, L.sms);
-  ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  ra.stage_keys = attn_stage_keys(d, max_len, ra.nsplit);
-  ra.smem = attn_smem_bytes(d, ra.stage_keys);
   ra.out = bf.o;
-  ra.status = bf.status;
   if ((e = record(es, st)) != cudaSuccess) return e;
   if ((e = launch_attention(ak, ra, st, pdl)) != cudaSuccess) return e;
   if ((e = record(es, st)) != cudaSuccess) return e;
@@ -367,10 +557,11 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   r3.bias = L.w.b_o;
   r3.x_f32 = bf.o;
   r3.out_f32 = bf.x1;
-  r3.resid_act = x_in;
+  r3.resid_act = io.x_in;
   r3.stats_out = bf.stats_a;
   if ((e = record(es, st)) != cudaSuccess) return e;
   if ((e = launch_region(Region::OprojRes, wk, ak, r3, st, pdl)) != cudaSuccess) return e;
+  if ((e = record_patch(rec, st, 0, r3, in_if(offsetof(RegionArgs, resid_act)), {})) != cudaSuccess) return e;
   if ((e = record(es, st)) != cudaSuccess) return e;
 
   // R4a: LayerNorm2 + FFN-up + bias + GeLU
@@ -416,22 +607,25 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   r5.bias = L.w.b_fc2;
   r5.x_f32 = bf.g;
   r5.resid_f32 = bf.x1;
-  r5.out_act = x_out;
+  r5.out_act = io.x_out;
   r5.stats_out = stats_out;
   r5.seq_len_inc = seq_inc;
   if ((e = record(es, st)) != cudaSuccess) return e;
   if ((e = launch_region(Region::FfnDown, wk, ak, r5, st, pdl)) != cudaSuccess) return e;
-  if ((e = record(es, st)) != cudaSuccess) return e;
-  return cudaSuccess;
+  if ((e = record_patch(rec, st, 0, r5, {}, out_if(offsetof(RegionArgs, out_act)))) != cudaSuccess) return e;
+  return record(es, st);
 }
 
-ds_status check_forward_args(const void* x_in, const void* x_out, int batch, int T, const void* kc,
+int kernels_per_layer(const Plans& p) { return p.tile ? 7 : 5; }
+
+ds_status check_forward_args(const ds_layer& L, const void* x_in, const void* x_out, int batch, int T, const void* kc,
                              const void* vc, int max_len, const void* len, const void* ws) {
   if (!aligned16(x_in) || !aligned16(x_out))
     return fail(DS_ERR_INVALID_ARG, "x_in / x_out must be non-null and 16-byte aligned");
   if (x_in == x_out) return fail(DS_ERR_INVALID_ARG, "x_out must not alias x_in");
-  if (batch < 1 || T < 1 || (long long)batch * T > 64)
-    return fail(DS_ERR_UNSUPPORTED, "batch * new_tokens must be in 1..64");
+  if (batch < 1 || T < 1 || (long long)batch * T > L.max_rows())
+    return fail(DS_ERR_UNSUPPORTED, L.tile_capable() ? "batch * new_tokens must be in 1..4096"
+                                                     : "batch * new_tokens must be in 1..64 for int8 weights");
   if (!aligned16(kc) || !aligned16(vc))
     return fail(DS_ERR_INVALID_ARG, "KV caches must be non-null and 16-byte aligned");
   if (max_len < 1 || max_len < T) return fail(DS_ERR_INVALID_ARG, "max_len must be >= new_tokens");
@@ -442,8 +636,17 @@ ds_status check_forward_args(const void* x_in, const void* x_out, int batch, int
   return DS_OK;
 }
 
-ds_status check_attn_smem(const ds_layer& L, int T) {
-  (void)T;  // tokens are processed one after another: shared memory does not grow with T
+// The library's kernels run on the device a layer was created on, with that
+// device current: its weights and tensor maps live there.
+ds_status check_device(const ds_layer& L) {
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != L.device) return fail(DS_ERR_INVALID_ARG, "the current device is not the device the layer was created on");
+  return DS_OK;
+}
+
+ds_status check_attn_smem(const ds_layer& L) {
   const int d = L.cfg.hidden / L.cfg.heads;
   if (attn_smem_bytes(d, attn_stage_keys(d, 1 << 30, 1)) > (size_t)L.max_smem)
     return fail(DS_ERR_UNSUPPORTED, "attention kernel's shared memory exceeds the device limit");
@@ -461,7 +664,7 @@ ds_status make_tensor_maps(ds_layer* L) {
   const int rows[4] = {3 * H, H, F, H};
   const int cols[4] = {H, H, H, F};
   const bool i8 = (c.weight_dtype == DS_I8);
-  const int nmaps = i8 ? 24 : 12;
+  const int nmaps = 32;
   std::vector<unsigned char> host((size_t)nmaps * kTensorMapBytes, 0);
   const int blk_k = i8 ? 64 : 32;  // k per 16-byte lane load
   for (int r = 0; r < 4; ++r) {
@@ -478,6 +681,12 @@ ds_status make_tensor_maps(ds_layer* L) {
                             cols[r] / grp, 8 * nb * 64 / grp))
         return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a scale matrix");
     }
+    if (!i8) {
+      for (int j = 0; j < 2; ++j)
+        if (!encode_tile_map(host.data() + (size_t)(24 + 2 * r + j) * kTensorMapBytes, W[r], rows[r], cols[r], 128,
+                             j ? 128 : 64))
+          return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight tile map");
+    }
   }
   int cur = 0;
   cudaGetDevice(&cur);
@@ -492,16 +701,13 @@ ds_status make_tensor_maps(ds_layer* L) {
 }  // namespace
 
 struct GraphKey {
-  const void* x_in = nullptr;
-  void* x_out = nullptr;
   int batch = 0;
   std::vector<void*> kc, vc;
   int max_len = 0;
   int32_t* seq = nullptr;
   void* ws = nullptr;
   bool operator==(const GraphKey& o) const {
-    return x_in == o.x_in && x_out == o.x_out && batch == o.batch && kc == o.kc && vc == o.vc &&
-           max_len == o.max_len && seq == o.seq && ws == o.ws;
+    return batch == o.batch && kc == o.kc && vc == o.vc && max_len == o.max_len && seq == o.seq && ws == o.ws;
   }
 };
 
@@ -509,13 +715,63 @@ struct ds_stack {
   std::vector<ds_layer*> layers;
   bool have_graph = false;
   GraphKey key;
+  cudaGraph_t graph = nullptr;   // kept alive for in-place updates of its kernel nodes
   cudaGraphExec_t exec = nullptr;
+  std::vector<PatchNode> patch;  // nodes holding x_in / x_out
+  const void* x_in = nullptr;    // the pointers the executable graph currently uses
+  void* x_out = nullptr;
   int graph_kernels = 0;
+  unsigned long long captures = 0;  // graph captures since creation
   bool profiling = false;
   std::vector<cudaEvent_t> events;
   double acc_ms[5] = {0, 0, 0, 0, 0};
   int acc_n[5] = {0, 0, 0, 0, 0};
 };
+
+namespace ds {
+void set_last_error(const char* msg) { g_err = msg; }
+int layer_device(const ds_layer* layer) { return layer->device; }
+
+// Validates a ds_layer_forward call (nothing is enqueued).  On success
+// *zero_prefix is the number of leading workspace bytes (status word and
+// counters) that must be zero before the call.
+ds_status layer_forward_check(const ds_layer* layer, const void* x_in, const void* x_out, int batch, int new_tokens,
+                              const void* k_cache, const void* v_cache, int max_len, const int32_t* past_len,
+                              const void* workspace, size_t ws_bytes, size_t* zero_prefix) {
+  if (layer == nullptr) return fail(DS_ERR_INVALID_ARG, "layer is null");
+  ds_status s = check_forward_args(*layer, x_in, x_out, batch, new_tokens, k_cache, v_cache, max_len, past_len,
+                                   workspace);
+  if (s != DS_OK) return s;
+  if ((s = check_device(*layer)) != DS_OK) return s;
+  if ((s = check_attn_smem(*layer)) != DS_OK) return s;
+  Plans p;
+  if (!make_plans(*layer, batch * new_tokens, &p)) return fail(DS_ERR_UNSUPPORTED, "no GEMM work split for this shape");
+  const WsLayout wl = ws_layout(*layer, batch, new_tokens, p);
+  if (ws_bytes < wl.total) return fail(DS_ERR_WORKSPACE, "workspace smaller than ds_layer_workspace_bytes()");
+  if (zero_prefix != nullptr) *zero_prefix = wl.q;
+  return DS_OK;
+}
+
+// Enqueues a ds_layer_forward call that layer_forward_check accepted.
+ds_status layer_forward_enqueue(ds_layer* layer, const void* x_in, void* x_out, int batch, int new_tokens,
+                                void* k_cache, void* v_cache, int max_len, const int32_t* past_len, void* workspace,
+                                void* stream) {
+  Plans p;
+  make_plans(*layer, batch * new_tokens, &p);
+  const WsLayout wl = ws_layout(*layer, batch, new_tokens, p);
+  const Bufs bf = bufs_of(workspace, wl);
+  XMaps xm;
+  if (p.tile && !make_xmaps(*layer, p, bf, batch * new_tokens, &xm))
+    return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation operand");
+  const LayerIO io{x_in, x_out, false, false};
+  cudaError_t e = enqueue_layer(*layer, p, bf, &xm, io, batch, new_tokens, k_cache, v_cache, max_len, past_len,
+                                nullptr, nullptr, nullptr, nullptr, true, static_cast<cudaStream_t>(stream), true,
+                                nullptr, nullptr);
+  if (e != cudaSuccess) return cuda_fail(e, "region kernel launch");
+  g_launches += kernels_per_layer(p);
+  return DS_OK;
+}
+}  // namespace ds
 
 extern "C" {
 
@@ -564,10 +820,8 @@ ds_status ds_layer_create(const ds_layer_config* cfg, const ds_layer_weights* w,
   L->device = dev;
   L->sms = di.sms;
   L->max_smem = di.max_smem;
-  L->smem_per_sm = di.smem_per_sm;
-  L->ctas_per_sm = ctas_per_sm_knob();
   Plans p;
-  if (!make_plans(*L, 1, 1, &p)) {
+  if (!make_plans(*L, 1, &p)) {
     delete L;
     return fail(DS_ERR_UNSUPPORTED, "no GEMV work split for this shape");
   }
@@ -593,9 +847,9 @@ ds_status ds_layer_destroy(ds_layer* layer) {
 }
 
 size_t ds_layer_workspace_bytes(const ds_layer* layer, int batch, int new_tokens) {
-  if (layer == nullptr || batch < 1 || new_tokens < 1 || (long long)batch * new_tokens > 64) return 0;
+  if (layer == nullptr || batch < 1 || new_tokens < 1 || (long long)batch * new_tokens > layer->max_rows()) return 0;
   Plans p;
-  if (!make_plans(*layer, batch * new_tokens, batch, &p)) return 0;
+  if (!make_plans(*layer, batch * new_tokens, &p)) return 0;
   return ws_layout(*layer, batch, new_tokens, p).total;
 }
 
@@ -609,41 +863,12 @@ ds_status ds_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
 ds_status ds_layer_forward(ds_layer* layer, const void* x_in, void* x_out, int batch, int new_tokens,
                            void* k_cache, void* v_cache, int max_len, const int32_t* past_len,
                            void* workspace, size_t ws_bytes, void* stream) {
-  if (layer == nullptr) return fail(DS_ERR_INVALID_ARG, "layer is null");
-  ds_status s = check_forward_args(x_in, x_out, batch, new_tokens, k_cache, v_cache, max_len,
-                                   past_len, workspace);
+  ds_status s = layer_forward_check(layer, x_in, x_out, batch, new_tokens, k_cache, v_cache, max_len, past_len,
+                                    workspace, ws_bytes, nullptr);
   if (s != DS_OK) return s;
-  if ((s = check_attn_smem(*layer, new_tokens)) != DS_OK) return s;
-  Plans p;
-  if (!make_plans(*layer, batch * new_tokens, batch, &p))
-    return fail(DS_ERR_UNSUPPORTED, "no GEMV work split for this shape");
-  const WsLayout wl = ws_layout(*layer, batch, new_tokens, p);
-  if (ws_bytes < wl.total) return fail(DS_ERR_WORKSPACE, "workspace smaller than ds_layer_workspace_bytes()");
-  const Bufs bf = bufs_of(workspace, wl);
-  cudaError_t e = enqueue_layer(*layer, p, bf, x_in, x_out, batch, new_tokens, k_cache, v_cache,
-                                max_len, past_len, nullptr, nullptr, nullptr, nullptr, true,
-                                static_cast<cudaStream_t>(stream), true, nullptr);
-  if (e != cudaSuccess) return cuda_fail(e, "region kernel launch");
-  g_launches += 5;
-  return DS_OK;
+  return layer_forward_enqueue(layer, x_in, x_out, batch, new_tokens, k_cache, v_cache, max_len, past_len, workspace,
+                               stream);
 }
-
-}  // extern "C"
-
-namespace ds {
-void set_last_error(const char* msg) { g_err = msg; }
-
-// Bytes at the start of a workspace that must be zero before a call (status
-// word and arrival counters); 0 for invalid arguments.
-size_t layer_workspace_zero_prefix(const ds_layer* layer, int batch, int new_tokens) {
-  if (layer == nullptr || batch < 1 || new_tokens < 1 || (long long)batch * new_tokens > 64) return 0;
-  Plans p;
-  if (!make_plans(*layer, batch * new_tokens, batch, &p)) return 0;
-  return ws_layout(*layer, batch, new_tokens, p).q;
-}
-}  // namespace ds
-
-extern "C" {
 
 ds_status ds_stack_create(ds_layer* const* layers, int n_layers, ds_stack** out) {
   if (out == nullptr) return fail(DS_ERR_INVALID_ARG, "out is null");
@@ -665,9 +890,69 @@ ds_status ds_stack_create(ds_layer* const* layers, int n_layers, ds_stack** out)
   return DS_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+void drop_graph(ds_stack* S) {
+  if (S->exec != nullptr) cudaGraphExecDestroy(S->exec);
+  if (S->graph != nullptr) cudaGraphDestroy(S->graph);
+  S->exec = nullptr;
+  S->graph = nullptr;
+  S->patch.clear();
+  S->have_graph = false;
+}
+
+cudaError_t enqueue_stack(ds_stack* S, const Plans& p, const Bufs& bf, const XMaps* xm, const void* x_in, void* x_out,
+                          int B, void* const* kc, void* const* vc, int max_len, int32_t* seq, cudaStream_t st,
+                          bool pdl, EventSink* es, std::vector<PatchNode>* rec) {
+  const int L = (int)S->layers.size();
+  const size_t act_bytes = (size_t)B * S->layers[0]->cfg.hidden * 2;
+  for (int l = 0; l < L; ++l) {
+    LayerIO io;
+    io.x_in = (l == 0) ? x_in : static_cast<const void*>(bf.act + ((l - 1) & 1) * act_bytes);
+    io.x_out = (l == L - 1) ? x_out : static_cast<void*>(bf.act + (l & 1) * act_bytes);
+    io.in_is_caller = (l == 0);
+    io.out_is_caller = (l == L - 1);
+    const float* sin = (l == 0) ? nullptr : bf.stats_b;
+    float* sout = (l == L - 1) ? nullptr : bf.stats_b;
+    cudaError_t e = enqueue_layer(*S->layers[l], p, bf, xm, io, B, 1, kc[l], vc[l], max_len, seq, sin, sout,
+                                  (l == L - 1) ? seq : nullptr, (l + 1 < L) ? S->layers[l + 1] : nullptr, l == 0, st,
+                                  pdl, es, rec);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Replaces the captured x_in / x_out pointers in the executable graph.
+cudaError_t patch_graph(ds_stack* S, const void* x_in, void* x_out) {
+  for (PatchNode& pn : S->patch) {
+    cudaKernelNodeParams kp{};
+    cudaError_t e = cudaGraphKernelNodeGetParams(pn.node, &kp);
+    if (e != cudaSuccess) return e;
+    std::vector<unsigned char> args = pn.args;
+    for (size_t off : pn.in_offsets) std::memcpy(args.data() + off, &x_in, sizeof(void*));
+    for (size_t off : pn.out_offsets) std::memcpy(args.data() + off, &x_out, sizeof(void*));
+    void* params[3] = {nullptr, nullptr, nullptr};
+    for (int i = 0; i <= pn.arg_index; ++i) params[i] = kp.kernelParams[i];
+    params[pn.arg_index] = args.data();
+    kp.kernelParams = params;
+    kp.extra = nullptr;
+    e = cudaGraphExecKernelNodeSetParams(S->exec, pn.node, &kp);
+    if (e != cudaSuccess) return e;
+  }
+  S->x_in = x_in;
+  S->x_out = x_out;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
 ds_status ds_stack_destroy(ds_stack* stack) {
   if (stack == nullptr) return DS_OK;
-  if (stack->exec != nullptr) cudaGraphExecDestroy(stack->exec);
+  drop_graph(stack);
   for (cudaEvent_t ev : stack->events) cudaEventDestroy(ev);
   delete stack;
   return DS_OK;
@@ -678,122 +963,33 @@ size_t ds_stack_workspace_bytes(const ds_stack* stack, int batch) {
   return ds_layer_workspace_bytes(stack->layers[0], batch, 1);
 }
 
-namespace {
-
-// Arguments of the persistent step kernel; false when it cannot run this
-// configuration (too many layers, no ring geometry, or not co-resident).
-bool build_step_args(const ds_stack* S, const Plans& p, const Bufs& bf, const void* x_in, void* x_out, int B,
-                     void* const* kc, void* const* vc, int max_len, int32_t* seq, StepArgs* a) {
-  const int L = (int)S->layers.size();
-  if (!p.step_ok || L > kStepMaxLayers || !step_kernel_knob()) return false;
-  const ds_layer& L0 = *S->layers[0];
-  const ds_layer_config& c = L0.cfg;
-  const WKind wk = wkind(c.weight_dtype);
-  const ActKind ak = akind(c.act_dtype);
-  a->L = L;
-  a->B = B;
-  a->H = c.hidden;
-  a->F = c.ffn;
-  a->heads = c.heads;
-  a->head_dim = c.hidden / c.heads;
-  a->max_len = max_len;
-  a->eps = c.ln_eps;
-  for (int i = 0; i < 4; ++i) a->qgroup[i] = L0.qgroup(i);
-  a->scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)a->head_dim));
-  a->nsplit = step_attn_nsplit(B, c.heads, max_len, L0.sms);
-  for (int i = 0; i < 4; ++i) a->plan[i] = p.step[i];
-  if (!step_geometry(wk, ak, B, L0.max_smem, a)) return false;
-  if (step_blocks_per_sm(wk, ak, a->plan[0].nt, step_smem_bytes(a->plan[0].nt, a->stages, a->SB, a->xs_cap)) < 1)
-    return false;
-  a->x_in = x_in;
-  a->x_out = x_out;
-  a->seq = seq;
-  a->status = bf.status;
-  a->counters = bf.cnt_gemv;
-  a->grid_bar = bf.grid_bar;
-  a->attn_cnt = bf.attn_cnt;
-  a->q = bf.q;
-  a->o = bf.o;
-  a->x1 = bf.x1;
-  a->g = bf.g;
-  a->stats_a = bf.stats_a;
-  a->stats_b = bf.stats_b;
-  a->partials = bf.partials;
-  a->attn_part = bf.attn_part;
-  a->act = bf.act;
-  for (int l = 0; l < L; ++l) {
-    const ds_layer_weights& w = S->layers[l]->w;
-    StepLayer& y = a->layer[l];
-    y.w[0] = w.w_qkv;
-    y.w[1] = w.w_o;
-    y.w[2] = w.w_fc1;
-    y.w[3] = w.w_fc2;
-    y.sc[0] = static_cast<const __half*>(w.s_qkv);
-    y.sc[1] = static_cast<const __half*>(w.s_o);
-    y.sc[2] = static_cast<const __half*>(w.s_fc1);
-    y.sc[3] = static_cast<const __half*>(w.s_fc2);
-    y.bias[0] = w.b_qkv;
-    y.bias[1] = w.b_o;
-    y.bias[2] = w.b_fc1;
-    y.bias[3] = w.b_fc2;
-    y.ln1_g = w.ln1_g;
-    y.ln1_b = w.ln1_b;
-    y.ln2_g = w.ln2_g;
-    y.ln2_b = w.ln2_b;
-    y.kc = kc[l];
-    y.vc = vc[l];
-    for (int r = 0; r < 4; ++r) {
-      y.tmap_w[r] = S->layers[l]->tmap_w(r, p.step[r].nblk);
-      y.tmap_s[r] = S->layers[l]->tmap_s(r, p.step[r].nblk);
-    }
-  }
-  return true;
-}
-
-cudaError_t enqueue_stack(ds_stack* S, const Plans& p, const Bufs& bf, const void* x_in, void* x_out,
-                          int B, void* const* kc, void* const* vc, int max_len, int32_t* seq,
-                          cudaStream_t st, bool pdl, EventSink* es) {
-  const int L = (int)S->layers.size();
-  const size_t act_bytes = (size_t)B * S->layers[0]->cfg.hidden * 2;
-  for (int l = 0; l < L; ++l) {
-    const void* xi = (l == 0) ? x_in : static_cast<const void*>(bf.act + ((l - 1) & 1) * act_bytes);
-    void* xo = (l == L - 1) ? x_out : static_cast<void*>(bf.act + (l & 1) * act_bytes);
-    const float* sin = (l == 0) ? nullptr : bf.stats_b;
-    float* sout = (l == L - 1) ? nullptr : bf.stats_b;
-    cudaError_t e = enqueue_layer(*S->layers[l], p, bf, xi, xo, B, 1, kc[l], vc[l], max_len, seq, sin,
-                                  sout, (l == L - 1) ? seq : nullptr, (l + 1 < L) ? S->layers[l + 1] : nullptr,
-                                  l == 0, st, pdl, es);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
-}  // namespace
-
 ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, int batch,
                                void* const* k_caches, void* const* v_caches, int max_len,
                                int32_t* seq_len, void* workspace, size_t ws_bytes, void* stream) {
   if (stack == nullptr) return fail(DS_ERR_INVALID_ARG, "stack is null");
   if (k_caches == nullptr || v_caches == nullptr) return fail(DS_ERR_INVALID_ARG, "cache arrays are null");
   const int L = (int)stack->layers.size();
+  const ds_layer& L0 = *stack->layers[0];
   for (int l = 0; l < L; ++l) {
-    ds_status s = check_forward_args(x_in, x_out, batch, 1, k_caches[l], v_caches[l], max_len,
-                                     seq_len, workspace);
+    ds_status s = check_forward_args(L0, x_in, x_out, batch, 1, k_caches[l], v_caches[l], max_len, seq_len, workspace);
     if (s != DS_OK) return s;
   }
-  const ds_layer& L0 = *stack->layers[0];
-  ds_status s = check_attn_smem(L0, 1);
+  ds_status s = check_device(L0);
   if (s != DS_OK) return s;
+  if ((s = check_attn_smem(L0)) != DS_OK) return s;
   Plans p;
-  if (!make_plans(L0, batch, batch, &p)) return fail(DS_ERR_UNSUPPORTED, "no GEMV work split for this shape");
+  if (!make_plans(L0, batch, &p)) return fail(DS_ERR_UNSUPPORTED, "no GEMM work split for this shape");
   const WsLayout wl = ws_layout(L0, batch, 1, p);
   if (ws_bytes < wl.total) return fail(DS_ERR_WORKSPACE, "workspace smaller than ds_stack_workspace_bytes()");
   const Bufs bf = bufs_of(workspace, wl);
+  XMaps xm;
+  if (p.tile && !make_xmaps(L0, p, bf, batch, &xm))
+    return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation operand");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int kernels = 5 * L;
+  const int kernels = kernels_per_layer(p) * L;
 
   if (stack->profiling) {
-    const size_t need = (size_t)2 * kernels;
+    const size_t need = (size_t)2 * 5 * L;
     while (stack->events.size() < need) {
       cudaEvent_t ev;
       cudaError_t e = cudaEventCreate(&ev);
@@ -802,13 +998,13 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
     }
     EventSink es;
     es.ev = &stack->events;
-    cudaError_t e = enqueue_stack(stack, p, bf, x_in, x_out, batch, k_caches, v_caches, max_len,
-                                  seq_len, st, false, &es);
+    cudaError_t e = enqueue_stack(stack, p, bf, &xm, x_in, x_out, batch, k_caches, v_caches, max_len, seq_len, st,
+                                  false, &es, nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "region kernel launch (profile)");
     g_launches += kernels;
     e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize (profile)");
-    for (int k = 0; k < kernels; ++k) {
+    for (int k = 0; k < 5 * L; ++k) {
       float ms = 0.f;
       e = cudaEventElapsedTime(&ms, stack->events[2 * k], stack->events[2 * k + 1]);
       if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
@@ -818,35 +1014,20 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
     return DS_OK;
   }
 
-  // Default path: one persistent, cooperative launch for the whole step;
-  // otherwise the chain of region kernels.
-  static thread_local StepArgs step_args;  // ~10 KB: kept off the call stack
-  const bool use_step = build_step_args(stack, p, bf, x_in, x_out, batch, k_caches, v_caches, max_len,
-                                        seq_len, &step_args);
-  const WKind swk = wkind(L0.cfg.weight_dtype);
-  const ActKind sak = akind(L0.cfg.act_dtype);
-  auto enqueue = [&]() -> cudaError_t {
-    if (use_step) return launch_step(swk, sak, step_args, L0.sms, st);
-    return enqueue_stack(stack, p, bf, x_in, x_out, batch, k_caches, v_caches, max_len, seq_len, st, true,
-                         nullptr);
-  };
-  const int launched = use_step ? 1 : kernels;
-
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (st != nullptr) {
     cudaError_t e = cudaStreamIsCapturing(st, &cs);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
   }
   if (st == nullptr || cs != cudaStreamCaptureStatusNone) {
-    cudaError_t e = enqueue();
-    if (e != cudaSuccess) return cuda_fail(e, use_step ? "step kernel launch" : "region kernel launch");
-    g_launches += launched;
+    cudaError_t e = enqueue_stack(stack, p, bf, &xm, x_in, x_out, batch, k_caches, v_caches, max_len, seq_len, st,
+                                  true, nullptr, nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "region kernel launch");
+    g_launches += kernels;
     return DS_OK;
   }
 
   GraphKey key;
-  key.x_in = x_in;
-  key.x_out = x_out;
   key.batch = batch;
   key.kc.assign(k_caches, k_caches + L);
   key.vc.assign(v_caches, v_caches + L);
@@ -854,14 +1035,12 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
   key.seq = seq_len;
   key.ws = workspace;
   if (!stack->have_graph || !(stack->key == key)) {
-    if (stack->exec != nullptr) {
-      cudaGraphExecDestroy(stack->exec);
-      stack->exec = nullptr;
-    }
-    stack->have_graph = false;
+    drop_graph(stack);
     cudaError_t e = cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamBeginCapture");
-    cudaError_t el = enqueue();
+    std::vector<PatchNode> rec;
+    cudaError_t el = enqueue_stack(stack, p, bf, &xm, x_in, x_out, batch, k_caches, v_caches, max_len, seq_len, st,
+                                   true, nullptr, &rec);
     cudaGraph_t graph = nullptr;
     e = cudaStreamEndCapture(st, &graph);
     if (el != cudaSuccess) {
@@ -870,14 +1049,25 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
     }
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
     e = cudaGraphInstantiate(&stack->exec, graph, 0);
-    cudaGraphDestroy(graph);
     if (e != cudaSuccess) {
+      cudaGraphDestroy(graph);
       stack->exec = nullptr;
       return cuda_fail(e, "cudaGraphInstantiate");
     }
+    stack->graph = graph;
+    stack->patch = std::move(rec);
     stack->key = key;
+    stack->x_in = x_in;
+    stack->x_out = x_out;
     stack->have_graph = true;
-    stack->graph_kernels = launched;
+    stack->graph_kernels = kernels;
+    stack->captures += 1;
+  } else if (x_in != stack->x_in || x_out != stack->x_out) {
+    cudaError_t e = patch_graph(stack, x_in, x_out);
+    if (e != cudaSuccess) {
+      drop_graph(stack);
+      return cuda_fail(e, "cudaGraphExecKernelNodeSetParams");
+    }
   }
   cudaError_t e = cudaGraphLaunch(stack->exec, st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
@@ -891,7 +1081,7 @@ ds_status ds_stack_decode_host(ds_stack* stack, const void* x_host, void* y_host
                                void* workspace, size_t ws_bytes, void* stream) {
   if (stack == nullptr) return fail(DS_ERR_INVALID_ARG, "stack is null");
   if (x_host == nullptr || y_host == nullptr) return fail(DS_ERR_INVALID_ARG, "host buffers are null");
-  if (batch < 1 || batch > 64) return fail(DS_ERR_UNSUPPORTED, "batch must be in 1..64");
+  if (batch < 1 || batch > stack->layers[0]->max_rows()) return fail(DS_ERR_UNSUPPORTED, "batch out of range");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t bytes = (size_t)batch * stack->layers[0]->cfg.hidden * 2;
   cudaError_t e = cudaMemcpyAsync(x_dev_in, x_host, bytes, cudaMemcpyHostToDevice, st);
@@ -922,6 +1112,8 @@ ds_status ds_stack_region_times(ds_stack* stack, float us_out[5], int launches_o
   }
   return DS_OK;
 }
+
+uint64_t ds_stack_graph_captures(const ds_stack* stack) { return stack == nullptr ? 0 : stack->captures; }
 
 ds_status ds_quantize_int8(const void* w_f16, int n, int k, int group, int8_t* codes, void* scales_f16,
                            void* stream) {

@@ -33,8 +33,7 @@ static size_t fixed_nt(int nt, int M, int K_S, int pad, bool split) {
   }
 }
 
-bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int ctas_per_sm,
-                    int max_smem, GemvPlan* plan, bool fixed_grid) {
+bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int max_smem, GemvPlan* plan) {
   const bool i8 = (wk == WKind::I8);
   const int blk_k = i8 ? 64 : 32;
   const int pad = i8 ? 8 : 32;
@@ -42,7 +41,7 @@ bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int 
   const bool split = (ak == ActKind::BF16);
   const int nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
   auto xs = [&](int K_S) { return xs_bytes_nt(nt, M, K_S, pad, split); };
-  if (!ws_make_plan(N, K, M, num_sms * ctas_per_sm, blk_k, kProducers, kXBudget, xs, plan, fixed_grid))
+  if (!ws_make_plan(N, K, M, num_sms, blk_k, kProducers, kXBudget, xs, plan))
     return false;
   // As deep a weight ring as the rest of shared memory allows (up to kMaxStages).
   const size_t fixed = fixed_nt(plan->nt, M, plan->K_S, pad, split);

@@ -141,8 +141,7 @@ struct Slot {
 
 // Shared-memory carve-up of a GEMV CTA: the weight ring (S stages of SB
 // bytes), the staged x slice (xs_cap bytes), the segment buffers, tile
-// values, LayerNorm mean / rstd, optional attention scratch (the step
-// kernel) and the ring's full / empty mbarriers.
+// values, LayerNorm mean / rstd and the ring's full / empty mbarriers.
 struct GemvSmem {
   unsigned char* ring;
   size_t SB;
@@ -152,21 +151,13 @@ struct GemvSmem {
   float* tileval;
   float* s_mean;
   float* s_rstd;
-  float* attn;
   uint64_t* mbar;
   __device__ __forceinline__ uint32_t full_bar(int i) const { return smem_u32(mbar + i); }
   __device__ __forceinline__ uint32_t empty_bar(int i) const { return smem_u32(mbar + S + i); }
 };
 
 template <int NT>
-__host__ __device__ inline size_t gemv_smem_bytes(int S, size_t SB, size_t xs_cap, size_t attn_floats) {
-  return 1024 + (size_t)S * SB + xs_cap +
-         4 * (SmemLayout<NT>::red_floats() + kEpiWarps * 16 * 8 * NT + 128 + attn_floats) + (size_t)16 * S;
-}
-
-template <int NT>
-__device__ __forceinline__ GemvSmem gemv_carve(unsigned char* base, int S, size_t SB, size_t xs_cap,
-                                               size_t attn_floats) {
+__device__ __forceinline__ GemvSmem gemv_carve(unsigned char* base, int S, size_t SB, size_t xs_cap) {
   GemvSmem m;
   base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(base) + 1023) & ~(uintptr_t)1023);
   m.ring = base;
@@ -177,8 +168,7 @@ __device__ __forceinline__ GemvSmem gemv_carve(unsigned char* base, int S, size_
   m.tileval = m.red + SmemLayout<NT>::red_floats();
   m.s_mean = m.tileval + kEpiWarps * 16 * 8 * NT;
   m.s_rstd = m.s_mean + 64;
-  m.attn = m.s_rstd + 64;
-  m.mbar = reinterpret_cast<uint64_t*>(m.attn + attn_floats);
+  m.mbar = reinterpret_cast<uint64_t*>(m.s_rstd + 64);
   return m;
 }
 
@@ -244,6 +234,7 @@ __device__ void gemv_tma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
   const int nchunks = (int)(rb - ra) + P.q * C;
   (void)nchunks; (void)K; (void)S; (void)SB; (void)ring; (void)M; (void)K_S;
   const uint32_t tx = (uint32_t)(RB + (kI8 ? 16 * (P.chunk_k / a.qgroup) * 2 : 0));
+  const int qshift = 31 - __clz(a.qgroup);  // group lengths are powers of two (64, 128)
   (void)tw;
   // Lanes 0 .. kIssueLanes-1 each issue every kIssueLanes-th chunk: one
   // issuing thread cannot keep a CTA's copies in flight at HBM rate (it spends
@@ -267,7 +258,7 @@ __device__ void gemv_tma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
       const uint32_t stage = smem_u32(ring + (size_t)st * SB);
       mbar_arrive_expect_tx(sm.full_bar(st), tx);
       tma_load_3d(stage, a.tmap_w, 0, row0, kg * ESZ / kSwizzleBytes, sm.full_bar(st), pol);
-      if constexpr (kI8) tma_load_2d(stage + (uint32_t)RB, a.tmap_s, kg / a.qgroup, row0, sm.full_bar(st), pol);
+      if constexpr (kI8) tma_load_2d(stage + (uint32_t)RB, a.tmap_s, kg >> qshift, row0, sm.full_bar(st), pol);
       for (int i = 0; i < kIssueLanes; ++i) ws_cursor_next(q, P, dp_b);
     }
     __syncwarp();
@@ -290,12 +281,13 @@ __device__ void gemv_l2_prefetch_phase(const void* tmap_w, const void* tmap_s, c
   const int dp_b = cta * P.q;
   int nchunks = (int)(rb - ra) + P.q * P.C;
   if (nchunks > max_chunks) nchunks = max_chunks;
+  const int qshift = 31 - __clz(qgroup);  // group lengths are powers of two
   Cursor q;
   ws_cursor_init(q, P, ra, rb, dp_b);
   for (int j = 0; j < nchunks; ++j) {
     const int kg = q.s * P.K_S + q.kc * P.chunk_k;
     tma_prefetch_3d(tmap_w, 0, q.t * 16, kg * ESZ / kSwizzleBytes);
-    if (WK == WKind::I8) tma_prefetch_2d(tmap_s, kg / qgroup, q.t * 16);
+    if (WK == WKind::I8) tma_prefetch_2d(tmap_s, kg >> qshift, q.t * 16);
     ws_cursor_next(q, P, dp_b);
   }
 }
@@ -303,8 +295,7 @@ __device__ void gemv_l2_prefetch_phase(const void* tmap_w, const void* tmap_s, c
 // MMA warps: LayerNorm prologue, x staging and the chunk loop of one GEMV
 // phase; each finished segment's per-warp tiles go to the epilogue warp.
 // `seg` counts segments across phases (it picks the segment buffer).
-// XB: input groups a thread loads together while staging x (1 inside the
-// persistent step kernel, whose register budget is shared by all regions).
+// XB: input groups a thread loads together while staging x.
 template <Region R, WKind WK, typename ACT, int NT, int XB = 2>
 __device__ void gemv_mma_phase(const RegionArgs& a, const GemvPlan& P, const GemvSmem& sm, RingPos& rp,
                                int& seg) {
@@ -353,6 +344,7 @@ __device__ void gemv_mma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
   // int8: scale groups per chunk row, and the group of block blk (groups of
   // 64 or 128 codes: uniform over the block, whose codes one MMA sums)
   const int gpc = P.chunk_k / a.qgroup;
+  const int qshift = 31 - __clz(a.qgroup);  // group lengths are powers of two (64, 128)
   const int sofs = wr * gpc;
   const int sg0 = warp * step_k + 16 * c;
   auto load = [&](int st, Slot& sl) {
@@ -370,7 +362,7 @@ __device__ void gemv_mma_phase(const RegionArgs& a, const GemvPlan& P, const Gem
 #pragma unroll
       for (int blk = 0; blk < kMaxBlk; ++blk) {
         if (blk < P.nblk) {
-          const int gi = (sg0 + 64 * blk) / a.qgroup;
+          const int gi = (sg0 + 64 * blk) >> qshift;
           sl.sc[blk] = sc[gi];
           sl.sc[kMaxBlk + blk] = sc[8 * gpc + gi];
         }
@@ -896,7 +888,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) region_gemv_kernel(const Regi
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const GemvPlan& P = a.plan;
   const GemvSmem sm = gemv_carve<NT>(smem_raw, P.stages, SmemLayout<NT>::stage_bytes(P.chunk_k, ESZ, WK == WKind::I8),
-                                     SmemLayout<NT>::xs_bytes(a.M, P.K_S, PAD, kSplit), 0);
+                                     SmemLayout<NT>::xs_bytes(a.M, P.K_S, PAD, kSplit));
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) gemv_init_ring(sm);
   __syncthreads();

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "ds_layer.h"
+
 namespace ds {
 
 enum class WKind : int { F16 = 0, BF16 = 1, I8 = 2 };
@@ -98,6 +100,57 @@ struct RegionArgs {
   int next_qgroup = 64;  // int8: that matrix's scale group length
 };
 
+// Tensor-core tile path (dense_impl.cuh): one output tile is 128 weight rows x
+// ntok rows of X; units of the work split are output tiles (u = token tile *
+// row_tiles + row tile), chunks are kc-wide K ranges, one K slice.
+struct DensePlan {
+  GemvPlan ws;         // tiles = units = row_tiles * tok_tiles, KS = 1, chunk_k = kc
+  int row_tiles = 0;   // N / 128
+  int tok_tiles = 0;   // ceil(M / ntok)
+  int ntok = 0;        // X rows per tile = MMA N (multiple of 16, <= 256)
+  int kc = 128;        // K per ring stage (64 or 128)
+  int stages = 0;
+  size_t smem = 0;
+};
+
+struct DenseArgs {
+  const void* tmap_w = nullptr;    // device address of W's tile tensor map (box 128 rows x kc)
+  int N = 0, K = 0, M = 0, B = 1, T = 1;
+  DensePlan plan;
+  float* partials = nullptr;       // [tiles - U_dp][maxc][ntok][128] partial sums of the leftover tiles
+  int* counters = nullptr;         // [tiles] arrival counters (self-resetting)
+  const void* bias = nullptr;      // [N] act dtype
+  // epilogue
+  float* out_f32 = nullptr;        // R1: q [M][H]; R3: x1
+  void* out_act = nullptr;         // R4a: GeLU output (operand hi); R4b: layer output
+  void* out_lo = nullptr;          // R4a, bf16: operand lo
+  const void* resid_act = nullptr; // R3: layer input
+  const float* resid_f32 = nullptr;// R4b: x1
+  float* stats_out = nullptr;      // R3 / R4b: [N/16][M][2] (sum, M2) partials, or null
+  void* k_cache = nullptr;         // R1 cache append
+  void* v_cache = nullptr;
+  int heads = 0, head_dim = 0, max_len = 0, H = 0;
+  const int32_t* past_len = nullptr;
+  unsigned* status = nullptr;
+  int32_t* seq_len_inc = nullptr;  // R4b of a stack step's last layer
+  const void* next_tmap_w = nullptr;  // the next tile GEMM (L2 prefetch), or null
+  DensePlan next_plan;
+};
+
+// Row normalisation ahead of a tile GEMM (regions 1 and 4a): out = LN(x) in
+// the MMA operand format (activation dtype; bf16 also writes the lo part).
+struct LnPrepArgs {
+  int M = 0, K = 0;
+  float eps = 1e-5f;
+  const void* x_act = nullptr;     // [M][K] act dtype (region 1), or
+  const float* x_f32 = nullptr;    // [M][K] fp32 (region 4a)
+  const float* stats_in = nullptr; // [K/16][M][2] (sum, M2) partials, or null (two passes over the row)
+  const void* ln_g = nullptr;
+  const void* ln_b = nullptr;
+  void* out_hi = nullptr;          // [M][K]
+  void* out_lo = nullptr;          // [M][K], bf16 only
+};
+
 struct AttnArgs {
   const float* q = nullptr;         // [B*T][H] fp32
   const void* k_cache = nullptr;    // [B][nh][max_len][d]
@@ -108,71 +161,31 @@ struct AttnArgs {
   float scale_log2 = 0.f;           // log2(e) / sqrt(head_dim)
   int stage_keys = 0;               // cached keys per split copied to shared memory up front
   size_t smem = 0;
-  float* out = nullptr;             // [B*T][H] fp32
+  float* out = nullptr;             // [B*T][H] fp32, or
+  void* out_hi = nullptr;           // [B*T][H] in the MMA operand format (tile path)
+  void* out_lo = nullptr;           // (bf16 only)
   unsigned* status = nullptr;       // workspace status word (wait-timeout flag)
 };
 
-// ---------------------------------------------------------------- step kernel
-// One persistent, cooperative launch runs a whole decode step (T = 1) of a
-// stack: per layer the phases LN1+QKV, attention, O-proj, LN2+FFN-up and
-// FFN-down, separated by grid-wide barriers, while the copy warps stream the
-// weights of the following phases without stopping.
-constexpr int kStepMaxLayers = 64;
-
-struct StepLayer {
-  const void* w[4];     // w_qkv, w_o, w_fc1, w_fc2
-  const __half* sc[4];  // their int8 group scales (int8 weights only)
-  const void* bias[4];  // b_qkv, b_o, b_fc1, b_fc2
-  const void* tmap_w[4];  // device addresses of the weights' tensor maps
-  const void* tmap_s[4];  // and of the int8 scales' tensor maps
-  const void* ln1_g;
-  const void* ln1_b;
-  const void* ln2_g;
-  const void* ln2_b;
-  void* kc;
-  void* vc;
-};
-
-struct StepArgs {
-  int L = 0, B = 1, H = 0, F = 0, heads = 0, head_dim = 0, max_len = 0;
-  int qgroup[4] = {64, 64, 64, 64};  // int8 scale group length of each phase's matrix
-  float eps = 1e-5f, scale_log2 = 0.f;
-  int nsplit = 1;           // attention key splits per (b, h)
-  GemvPlan plan[4];         // QKV, O-proj, FFN-up, FFN-down
-  int stages = 0;           // common weight-ring geometry
-  size_t SB = 0;            // ring stage stride, bytes
-  size_t xs_cap = 0;        // staged-x bytes (largest phase)
-  const void* x_in = nullptr;
-  void* x_out = nullptr;
-  int32_t* seq = nullptr;   // [B] cached positions; +1 at the end of the step
-  unsigned* status = nullptr;
-  int* counters = nullptr;  // GEMV row-tile arrival counters
-  unsigned* grid_bar = nullptr;  // grid barrier counter (returns to 0 at the end)
-  int* attn_cnt = nullptr;  // [B][nh] attention split counters
-  float *q = nullptr, *o = nullptr, *x1 = nullptr, *g = nullptr;
-  float *stats_a = nullptr, *stats_b = nullptr, *partials = nullptr, *attn_part = nullptr;
-  char* act = nullptr;      // [2][B][H] ping-pong layer outputs
-  StepLayer layer[kStepMaxLayers];
-};
-
-int step_attn_nsplit(int B, int heads, int max_len, int grid);
-size_t step_smem_bytes(int nt, int stages, size_t SB, size_t xs_cap);
-// Fills stages / SB / xs_cap of `s` from its four plans; false if no ring fits.
-bool step_geometry(WKind wk, ActKind ak, int M, int max_smem, StepArgs* s);
-cudaError_t launch_step(WKind wk, ActKind ak, const StepArgs& s, int grid, cudaStream_t st);
-// CTAs of the step kernel that fit on one SM (0 if the launch cannot work).
-int step_blocks_per_sm(WKind wk, ActKind ak, int nt, size_t smem);
-cudaError_t prepare_step_kernels(int max_smem);
-
-// Chooses the work split for one GEMV; returns false if no valid split exists.
-// fixed_grid: exactly num_sms * ctas_per_sm CTAs even for less work (step kernel).
-bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int ctas_per_sm,
-                    int max_smem, GemvPlan* plan, bool fixed_grid = false);
+// Chooses the work split for one GEMV over num_sms CTAs; returns false if no
+// valid split exists.
+bool gemv_make_plan(WKind wk, ActKind ak, int N, int K, int M, int num_sms, int max_smem, GemvPlan* plan);
 cudaError_t launch_region(Region r, WKind wk, ActKind ak, const RegionArgs& a,
                           cudaStream_t st, bool pdl);
 // Sets the dynamic shared-memory limit of every region kernel (call once per
 // device before the first launch).
 cudaError_t prepare_region_kernels(int max_smem);
+
+// Tile path: plan (false if the shape has no tile split), launch, and the
+// row normalisation kernel.
+bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem, DensePlan* plan);
+// Encodes the tile tensor map of a row-major [rows][cols] 16-bit matrix
+// (box 128 rows x kc, or ntok rows x kc for activation operands).
+bool encode_tile_map(void* map128, const void* base, int rows, int cols, int box_rows, int kc);
+cudaError_t launch_dense(Region r, ActKind ak, const DenseArgs& a, const void* xmap_hi, const void* xmap_lo,
+                         cudaStream_t st, bool pdl);
+cudaError_t launch_ln_prep(ActKind ak, const LnPrepArgs& a, cudaStream_t st, bool pdl);
+cudaError_t prepare_dense_kernels(int max_smem);
 
 int attn_nsplit(int B, int heads, int max_len, int num_sms);
 // Shared memory of the attention kernel, and the cached keys per split it
@@ -186,11 +199,20 @@ cudaError_t prepare_attention_kernels(int max_smem);
 
 struct ds_layer;
 namespace ds {
-// Leading workspace bytes (status word + arrival counters) that must be zero
-// before a ds_layer_forward call with this batch shape; 0 if invalid.
-size_t layer_workspace_zero_prefix(const ds_layer* layer, int batch, int new_tokens);
+// ds_layer_forward in two steps: validation (nothing enqueued; on success
+// *zero_prefix = leading workspace bytes -- status word and arrival counters --
+// that must be zero before the call), then the launches.
+ds_status layer_forward_check(const ds_layer* layer, const void* x_in, const void* x_out, int batch,
+                                int new_tokens, const void* k_cache, const void* v_cache, int max_len,
+                                const int32_t* past_len, const void* workspace, size_t ws_bytes,
+                                size_t* zero_prefix);
+ds_status layer_forward_enqueue(ds_layer* layer, const void* x_in, void* x_out, int batch, int new_tokens,
+                                  void* k_cache, void* v_cache, int max_len, const int32_t* past_len,
+                                  void* workspace, void* stream);
 // Sets the detail string returned by ds_last_error() on this thread.
 void set_last_error(const char* msg);
+// The device a layer was created on.
+int layer_device(const ds_layer* layer);
 
 cudaError_t launch_quantize_int8(const void* w, int n, int k, int group, int8_t* codes, void* scales,
                                  cudaStream_t st);

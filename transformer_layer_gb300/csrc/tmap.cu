@@ -65,4 +65,24 @@ bool encode_scale_map(void* map128, const void* base, int rows, int groups, int 
   return r == CUDA_SUCCESS;
 }
 
+bool encode_tile_map(void* map128, const void* base, int rows, int cols, int box_rows, int kc) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr || rows < 1 || cols % 64 != 0 || kc % 64 != 0 || box_rows < 8 || box_rows > 256 ||
+      (reinterpret_cast<uintptr_t>(base) & 15u) != 0)
+    return false;
+  // [rows][cols] 16-bit elements as (element within a 128-byte atom, row,
+  // atom): a box of (64, box_rows, kc / 64) lands as [atom][row][128 bytes],
+  // 128-byte swizzled -- the K-major operand layout of tcgen05.mma.  Rows past
+  // the end read as zero.
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)(kc / 64)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(static_cast<CUtensorMap*>(map128), CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace ds

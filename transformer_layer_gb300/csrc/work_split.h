@@ -126,15 +126,50 @@ DS_HD void ws_leftover_segment(const GemvPlan& P, long long i, long long rb, int
   *j_slot = P.whole ? 0 : (P.R < G) ? (int)(i - uo * P.C) : cta - ws_cta_of(uo * P.C, P.R, G);
 }
 
+// Distributes p.units units of p.C chunks each over at most num_ctas CTAs:
+// p.grid, q whole units per CTA, and either whole leftover units or their
+// chunks spread evenly (p.whole, p.U_dp, p.R, p.maxc).  p.units and p.C must
+// be set.
+inline void ws_distribute(GemvPlan& p, int num_ctas) {
+  const long long total = (long long)p.units * p.C;
+  long long G = num_ctas;
+  if (G > total) G = total;
+  p.grid = (int)G;
+  p.q = p.units / p.grid;
+  p.whole = 0;
+  // Leftover units go whole to CTAs when that lengthens the busiest CTA by at
+  // most 3 chunks: a split-K fix-up costs global round trips (several us under
+  // the weight stream) that the short kernels cannot hide.
+  {
+    const long long lu = p.units - (long long)p.q * p.grid;
+    const long long whole_max = ((long long)p.q + (lu > 0 ? 1 : 0)) * p.C;
+    long long qs = p.q;
+    if (qs > 0 && lu * p.C > 0 && lu * p.C < p.grid) qs -= 1;
+    const long long rs = (p.units - qs * p.grid) * p.C;
+    const long long split_max = qs * p.C + (rs + p.grid - 1) / p.grid;
+    if (lu > 0 && whole_max - split_max <= 3) p.whole = 1;
+  }
+  // Every CTA must own at least one leftover chunk when there are any (so the
+  // CTAs sharing a leftover unit are consecutive, with no empty ranges in
+  // between): with fewer leftover chunks than CTAs, hand one whole unit per
+  // CTA back to the leftover pool.
+  const long long left = (long long)(p.units - p.q * p.grid) * p.C;
+  if (!p.whole && p.q > 0 && left > 0 && left < p.grid) p.q -= 1;
+  p.U_dp = p.q * p.grid;
+  p.R = (long long)(p.units - p.U_dp) * p.C;
+  p.maxc = 1;
+  for (int u = p.U_dp; u < p.units; ++u) {
+    const int n = ws_unit_contrib(u, p, p.grid);
+    if (n > p.maxc) p.maxc = n;
+  }
+}
+
 // Host planner: the longest K slice whose staged x fits `x_budget` bytes, then
 // q whole units per CTA and the leftover units' chunks spread evenly.
 // xs_bytes(K_S) gives the staged-x bytes for a slice length.
-// fixed_grid: use exactly num_ctas CTAs even when there is less work (the
-// persistent step kernel has one CTA per SM for every phase); CTAs may then
-// own no chunk of this GEMV.
 template <typename XsBytes>
 inline bool ws_make_plan(int N, int K, int M, int num_ctas, int blk_k, int warps, size_t x_budget,
-                         XsBytes xs_bytes, GemvPlan* plan, bool fixed_grid = false) {
+                         XsBytes xs_bytes, GemvPlan* plan) {
   if (N <= 0 || K <= 0 || M < 1 || M > 64 || (N % 16) != 0 || num_ctas < 1) return false;
   GemvPlan p;
   p.nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
@@ -159,37 +194,7 @@ inline bool ws_make_plan(int N, int K, int M, int num_ctas, int blk_k, int warps
   p.KS = K / p.K_S;
   p.C = p.K_S / p.chunk_k;
   p.units = p.KS * p.tiles;
-  const long long total = (long long)p.units * p.C;
-  long long G = num_ctas;
-  if (G > total && !fixed_grid) G = total;
-  p.grid = (int)G;
-  p.q = p.units / p.grid;
-  p.whole = 0;
-  // Leftover units go whole to CTAs when that lengthens the busiest CTA by at
-  // most 3 chunks: a split-K fix-up costs global round trips (several us under
-  // the weight stream) that the short kernels cannot hide.
-  if (!fixed_grid) {
-    const long long lu = p.units - (long long)p.q * p.grid;
-    const long long whole_max = ((long long)p.q + (lu > 0 ? 1 : 0)) * p.C;
-    long long qs = p.q;
-    if (qs > 0 && lu * p.C > 0 && lu * p.C < p.grid) qs -= 1;
-    const long long rs = (p.units - qs * p.grid) * p.C;
-    const long long split_max = qs * p.C + (rs + p.grid - 1) / p.grid;
-    if (lu > 0 && whole_max - split_max <= 3) p.whole = 1;
-  }
-  // Every CTA must own at least one leftover chunk when there are any (so the
-  // CTAs sharing a leftover unit are consecutive, with no empty ranges in
-  // between): with fewer leftover chunks than CTAs, hand one whole unit per
-  // CTA back to the leftover pool.
-  const long long left = (long long)(p.units - p.q * p.grid) * p.C;
-  if (!p.whole && p.q > 0 && left > 0 && left < p.grid) p.q -= 1;
-  p.U_dp = p.q * p.grid;
-  p.R = (long long)(p.units - p.U_dp) * p.C;
-  p.maxc = 1;
-  for (int u = p.U_dp; u < p.units; ++u) {
-    const int n = ws_unit_contrib(u, p, p.grid);
-    if (n > p.maxc) p.maxc = n;
-  }
+  ws_distribute(p, num_ctas);
   *plan = p;
   return true;
 }

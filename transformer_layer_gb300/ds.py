@@ -29,6 +29,7 @@ _SIGS = {
     "ds_layer_forward": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, _vp, C.c_int, _vp, _vp,
                                    C.c_size_t, _vp]),
     "ds_layer_forward_noalloc": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, _vp, C.c_int, _vp, _vp]),
+    "ds_noalloc_status": (C.c_int, [C.POINTER(C.c_uint32), _vp]),
     "ds_stack_create": (C.c_int, [C.POINTER(_vp), C.c_int, C.POINTER(_vp)]),
     "ds_stack_destroy": (C.c_int, [_vp]),
     "ds_stack_workspace_bytes": (C.c_size_t, [_vp, C.c_int]),
@@ -38,6 +39,7 @@ _SIGS = {
                                        C.POINTER(_vp), C.c_int, _vp, _vp, C.c_size_t, _vp]),
     "ds_stack_set_profiling": (C.c_int, [_vp, C.c_int]),
     "ds_stack_region_times": (C.c_int, [_vp, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
+    "ds_stack_graph_captures": (C.c_uint64, [_vp]),
     "ds_quantize_int8": (C.c_int, [_vp, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp]),
     "ds_workspace_status": (C.c_int, [_vp, C.POINTER(C.c_uint32), _vp]),
     "ds_launch_count": (C.c_uint64, []),
@@ -152,6 +154,16 @@ def ds_layer_forward_noalloc(layer, x_in, x_out, batch, new_tokens, k_cache, v_c
            "ds_layer_forward_noalloc")
 
 
+def ds_noalloc_status(stream=None):
+    """Returns (status_code, flags) of the last no-allocation forward on the
+    current device and clears its status word."""
+    flags = C.c_uint32(0)
+    code = load().ds_noalloc_status(C.byref(flags), _stream(stream))
+    if code not in (DS_OK, DS_ERR_DEVICE):
+        raise DSError(code, "ds_noalloc_status")
+    return code, int(flags.value)
+
+
 def ds_stack_create(layers):
     arr = (C.c_void_p * len(layers))(*[l.value if isinstance(l, C.c_void_p) else l for l in layers])
     out = C.c_void_p()
@@ -196,6 +208,10 @@ def ds_stack_region_times(stack):
     n = (C.c_int * 5)()
     _check(load().ds_stack_region_times(stack, us, n), "ds_stack_region_times")
     return list(us), list(n)
+
+
+def ds_stack_graph_captures(stack):
+    return int(load().ds_stack_graph_captures(stack))
 
 
 def ds_quantize_int8(w_f16, codes, scales, group=64, stream=None):
