@@ -110,6 +110,25 @@ static int check_tiles(int tiles, int K, int G0) {
   return verify(P, 128 * tiles, K, 0);
 }
 
+// The tile path's plan with one whole unit per CTA: each tile cut into KS
+// slices along K when there are few tiles.
+static int check_tiles_sliced(int tiles, int K, int G0) {
+  GemvPlan P;
+  P.tiles = tiles;
+  P.chunk_k = 128;
+  int KS = 1;
+  if (tiles * 5 < G0 * 3)
+    while (KS < 8 && tiles * KS * 2 <= G0 && (K / 128) % (KS * 2) == 0) KS *= 2;
+  P.KS = KS;
+  P.K_S = K / KS;
+  P.C = P.K_S / 128;
+  P.units = tiles * KS;
+  ws_distribute(P, G0, true);
+  if (P.units <= G0 && (P.grid != P.units || P.q != 1 || P.R != 0))
+    return fail("one unit per CTA not kept", 128 * tiles, K, 0, P.grid, P.units, P.q);
+  return verify(P, 128 * tiles, K, 0);
+}
+
 int main() {
   int bad = 0;
   // Shapes of the shipped workloads (QKV, O-proj, FFN-up, FFN-down), batch rows 1..64.
@@ -145,7 +164,13 @@ int main() {
       bad |= check_tiles(tt * H / 128, H, 152);
       bad |= check_tiles(tt * F / 128, H, 152);
       bad |= check_tiles(tt * H / 128, F, 152);
+      bad |= check_tiles_sliced(tt * 3 * H / 128, H, 152);
+      bad |= check_tiles_sliced(tt * H / 128, H, 152);
+      bad |= check_tiles_sliced(tt * F / 128, H, 152);
+      bad |= check_tiles_sliced(tt * H / 128, F, 152);
     }
+  for (int it = 0; it < 400 && !bad; ++it)
+    bad |= check_tiles_sliced(1 + rnd(300), 256 * (1 + rnd(64)), 1 + rnd(300));
   if (!bad) std::printf("ok\n");
   return bad;
 }

@@ -248,6 +248,16 @@ __device__ __forceinline__ void i8x4_to_bf162x2(uint32_t w, uint32_t& lo, uint32
   hi = Act<__nv_bfloat16>::pack2(f2, f3);
 }
 
+// Shared-memory load / store at a 32-bit shared-window address.
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Named barrier over n threads (a multiple of 32); id 0 is __syncthreads.
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");

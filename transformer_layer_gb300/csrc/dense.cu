@@ -41,16 +41,24 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   p.kc = (ntok > 64 || K % 128 != 0) ? 64 : 128;
   GemvPlan& w = p.ws;
   w.tiles = p.row_tiles * p.tok_tiles;
-  w.KS = 1;
-  w.K_S = K;
   w.chunk_k = p.kc;
-  w.C = K / p.kc;
-  w.units = w.tiles;
   w.nt = 1;
   w.nblk = 1;
-  ws_distribute(w, num_sms);
+  // With at least ~60 % as many tiles as SMs every CTA takes one whole tile
+  // (no split-K: a fix-up costs more than the idle SMs).  With fewer, each
+  // tile is cut into KS slices along K (a power of two, at most 8), one whole
+  // unit per CTA, as many as the SMs hold.  With more tiles than SMs, the
+  // even split over CTAs (whole units first, leftover chunks spread).
+  int KS = 1;
+  if (w.tiles * 5 < num_sms * 3)
+    while (KS < 8 && w.tiles * KS * 2 <= num_sms && (K / p.kc) % (KS * 2) == 0) KS *= 2;
+  w.KS = KS;
+  w.K_S = K / KS;
+  w.C = w.K_S / p.kc;
+  w.units = w.tiles * KS;
+  ws_distribute(w, num_sms, /*one_unit_each=*/true);
   const size_t SB = (dense_stage_bytes(ntok, p.kc, split) + 1023) & ~(size_t)1023;
-  const size_t fixed = 1024 + 8 * (2 * kDenseMaxStages + 4) + 16;
+  const size_t fixed = 1024 + 8 * (2 * kDenseMaxStages + 6) + 16;
   if ((size_t)max_smem < fixed + 2 * SB) return false;
   size_t s = ((size_t)max_smem - fixed) / SB;
   if (s > (size_t)kDenseMaxStages) s = kDenseMaxStages;

@@ -30,14 +30,18 @@
 //    (kind::f16, M = 128, N = NTOK, K = 16 per instruction; bf16 issues the lo
 //    operand as a second MMA into the same accumulator) and tcgen05.commit to
 //    release ring stages and to publish finished tiles.
-//  * Warps 2..5 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
-//    32 (w % 4) ..: one weight row per thread, 16 token columns per load) and
-//    run the region epilogue, or publish a split-K partial; the last CTA to
-//    contribute to a tile (acquire-release counter, nothing waits) sums the
-//    partials in fixed order and runs the epilogue, so results are
-//    deterministic.
-//  * Work split (work_split.h): units are output tiles, chunks are KC-wide K
-//    ranges; every CTA owns whole tiles and/or an even share of the leftover
+//  * Warps 2..9 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
+//    32 (w % 4) ..: one weight row per thread; the two warps of a lane
+//    quarter take alternate groups of 8 token columns) and run the region
+//    epilogue, or publish a split-K partial; the last CTA to contribute to a
+//    tile (acquire-release counter, nothing waits) stages the partials in its
+//    idle ring with bulk copies, sums them in fixed order and runs the
+//    epilogue, so results are deterministic.
+//  * Work split (work_split.h): a unit is one output tile x one K slice,
+//    chunks are KC-wide K ranges.  With at least ~60 % as many tiles as SMs
+//    each CTA takes one whole tile (no split-K); with fewer (N = 4096 at
+//    decode) each tile is cut into K slices, one per CTA; with more (long
+//    prompts) CTAs own whole tiles and/or an even share of the leftover
 //    tiles' chunks.
 #pragma once
 
@@ -51,13 +55,15 @@
 
 namespace ds {
 
-constexpr int kDenseThreads = 192;   // 6 warps
+constexpr int kDenseEpiWarps = 8;    // two per TMEM lane quarter, each taking half the columns
+constexpr int kDenseThreads = (2 + kDenseEpiWarps) * 32;
 constexpr int kDenseTmaWarp = 0;
 constexpr int kDenseMmaWarp = 1;
-constexpr int kDenseEpiWarp0 = 2;    // warps 2..5
-constexpr int kDenseEpiThreads = 128;
+constexpr int kDenseEpiWarp0 = 2;    // warps 2 .. 9
+constexpr int kDenseEpiThreads = kDenseEpiWarps * 32;
 constexpr int kDenseBarEpi = 1;      // named barrier of the four epilogue warps
 constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
+constexpr int kL2Ahead = 8;            // weight chunks requested into L2 ahead of the ring
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor of a K-major operand tile in the canonical
@@ -93,6 +99,16 @@ __device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr, uint32_t ncols) 
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// 8 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -170,11 +186,18 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   auto empty_bar = [&](int i) { return smem_u32(bars + S + i); };
   auto accf_bar = [&](int i) { return smem_u32(bars + 2 * S + i); };
   auto acce_bar = [&](int i) { return smem_u32(bars + 2 * S + 2 + i); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 4);
+  const uint32_t fix_bar = smem_u32(bars + 2 * S + 4);   // staged partials of a fix-up
+  const uint32_t done_bar = smem_u32(bars + 2 * S + 5);  // epilogue warps done with TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const uint32_t tcols = dense_tmem_cols(NTOK);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 32) {  // the descriptors' first use is the TMA warp's first copy
+    asm volatile("prefetch.tensormap [%0];" ::"l"(a.tmap_w) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap_hi) : "memory");
+    if (kSplit) asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap_lo) : "memory");
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full_bar(i), 1);
@@ -182,8 +205,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(accf_bar(i), 1);
-      mbar_init(acce_bar(i), 4);  // one arrival per epilogue warp
+      mbar_init(acce_bar(i), kDenseEpiWarps);  // one arrival per epilogue warp
     }
+    mbar_init(fix_bar, 1);
+    mbar_init(done_bar, kDenseEpiWarps);
     mbar_init_fence();
   }
   if (warp == kDenseMmaWarp) tmem_alloc(smem_u32(tmem_slot), tcols);
@@ -216,12 +241,25 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
         const int trow = q.t % row_tiles;
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
-        tma_load_3d(stage, a.tmap_w, 0, trow * 128, q.kc * KC / 64, full_bar(rp.st), pol_w);
+        tma_load_3d(stage, a.tmap_w, 0, trow * 128, (q.s * P.C + q.kc) * (KC / 64), full_bar(rp.st), pol_w);
         last_ph[rp.st] = rp.ph;
         issued |= 1u << rp.st;
         ws_cursor_next(q, P, dp_b);
         rp.advance(S);
       }
+      // In-kernel L2 lookahead: the weight chunks after the ring's are
+      // requested from HBM into L2 (no shared memory needed), kL2Ahead ahead
+      // of the copy into the ring, so that the stream's bytes in flight do not
+      // depend on the ring depth.
+      Cursor qp = q;
+      int fpre = pre;
+      auto l2_ahead = [&](int upto) {
+        for (; fpre < upto && fpre < nchunks; ++fpre) {
+          tma_prefetch_3d(a.tmap_w, 0, (qp.t % row_tiles) * 128, (qp.s * P.C + qp.kc) * (KC / 64));
+          ws_cursor_next(qp, P, dp_b);
+        }
+      };
+      l2_ahead(pre + kL2Ahead);
       pdl_wait();
       pdl_launch_dependents();
       {
@@ -230,9 +268,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         for (int j = 0; j < pre; ++j) {
           const uint32_t stage = smem_u32(sm + (size_t)r2.st * SB);
           const int jt = c.t / row_tiles;
-          tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, c.kc * KC / 64, full_bar(r2.st), pol_x);
+          const int kseg = (c.s * P.C + c.kc) * (KC / 64);
+          tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
           if constexpr (kSplit)
-            tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, c.kc * KC / 64, full_bar(r2.st), pol_x);
+            tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
           ws_cursor_next(c, P, dp_b);
           r2.advance(S);
         }
@@ -242,15 +281,17 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         if (dead) break;
         const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
         const int trow = q.t % row_tiles, jt = q.t / row_tiles;
+        const int kseg = (q.s * P.C + q.kc) * (KC / 64);
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
-        tma_load_3d(stage, a.tmap_w, 0, trow * 128, q.kc * KC / 64, full_bar(rp.st), pol_w);
-        tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, q.kc * KC / 64, full_bar(rp.st), pol_x);
+        tma_load_3d(stage, a.tmap_w, 0, trow * 128, kseg, full_bar(rp.st), pol_w);
+        tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
         if constexpr (kSplit)
-          tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, q.kc * KC / 64, full_bar(rp.st), pol_x);
+          tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
         last_ph[rp.st] = rp.ph;
         issued |= 1u << rp.st;
         ws_cursor_next(q, P, dp_b);
         rp.advance(S);
+        l2_ahead(j + 1 + kL2Ahead);
       }
       // No copy may still be landing in this CTA's shared memory when it
       // exits: wait (bounded) for the last copy of every stage.  Immediate in
@@ -316,111 +357,214 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     // ---------------------------------------------------------- epilogue
     pdl_wait();
     pdl_launch_dependents();
-    const int et = threadIdx.x - kDenseEpiWarp0 * 32;  // 0..127
+    const int et = threadIdx.x - kDenseEpiWarp0 * 32;  // 0 .. kDenseEpiThreads-1
     const int qd = warp & 3;                            // TMEM lane quarter
     const int r = 32 * qd + lane;                       // weight row within the tile
+    const int cbeg = 8 * ((warp - kDenseEpiWarp0) >> 2); // this warp's first 8-column group; stride 16
     const int M = a.M, N = a.N;
+    // One output tile as this thread sees it: weight row n, token columns
+    // [m0, m0 + mrows), and the row's epilogue invariants.
+    struct TileCtx {
+      int t, n, m0, mrows;
+      float bias;
+      ACT* dst;         // R1: the row's KV-cache element of (b, position) 0; R4a / R4b: output column n
+      ACT* dst_lo;      // R4a, bf16: operand lo column n
+      float* dst_f32;   // R1 (q rows): q column; R3: x1 column n
+      bool to_cache;    // R1: this row is a k or v row
+    };
+    auto tile_ctx = [&](int t) {
+      TileCtx c;
+      c.t = t;
+      c.n = (t % row_tiles) * 128 + r;
+      c.m0 = (t / row_tiles) * NTOK;
+      c.mrows = min(NTOK, M - c.m0);
+      c.bias = Act<ACT>::to_f(static_cast<const ACT*>(a.bias)[c.n]);
+      c.dst = nullptr;
+      c.dst_lo = nullptr;
+      c.dst_f32 = nullptr;
+      c.to_cache = false;
+      if constexpr (R == Region::LnQkv) {
+        const int part = c.n / a.H, within = c.n - part * a.H;
+        if (part == 0) {
+          c.dst_f32 = a.out_f32 + within;
+        } else {
+          const int head = within / a.head_dim, dim = within - head * a.head_dim;
+          c.dst = static_cast<ACT*>(part == 1 ? a.k_cache : a.v_cache) + (size_t)head * a.max_len * a.head_dim + dim;
+          c.to_cache = true;
+        }
+      } else if constexpr (R == Region::OprojRes) {
+        c.dst_f32 = a.out_f32 + c.n;
+      } else {
+        c.dst = static_cast<ACT*>(a.out_act) + c.n;
+        if constexpr (R == Region::FfnUp && kSplit) c.dst_lo = static_cast<ACT*>(a.out_lo) + c.n;
+      }
+      return c;
+    };
+    // Global operands of 8 token columns (residual, or the cache position),
+    // requested one group ahead of their use.
+    auto ops_load = [&](const TileCtx& c, int c8, float (&o)[8]) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int mi = c8 + i;
+        const int m = c.m0 + (mi < c.mrows ? mi : c.mrows - 1);
+        if constexpr (R == Region::LnQkv) {
+          const int b = a.T == 1 ? m : m / a.T;
+          o[i] = __int_as_float(a.past_len[b] + (m - b * a.T));
+        } else if constexpr (R == Region::OprojRes) {
+          o[i] = Act<ACT>::to_f(static_cast<const ACT*>(a.resid_act)[(size_t)m * N + c.n]);
+        } else if constexpr (R == Region::FfnDown) {
+          o[i] = a.resid_f32[(size_t)m * N + c.n];
+        } else {
+          o[i] = 0.f;
+        }
+      }
+    };
+    // Region epilogue of 8 token columns [m0 + c8, m0 + c8 + 8) of row n.
+    auto epi8 = [&](const TileCtx& c, int c8, const float (&v)[8], const float (&op)[8]) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int mi = c8 + i;  // column within the tile
+        const bool ok = mi < c.mrows;
+        const int m = c.m0 + mi;
+        float y = v[i] + c.bias;
+        if constexpr (R == Region::LnQkv) {
+          if (ok) {
+            if (!c.to_cache) {
+              c.dst_f32[(size_t)m * a.H] = y;
+            } else {
+              const int b = a.T == 1 ? m : m / a.T;
+              const int pos = __float_as_int(op[i]);
+              if (pos >= 0 && pos < a.max_len)
+                c.dst[((size_t)b * a.heads * a.max_len + pos) * a.head_dim] = Act<ACT>::from_f(y);
+              else
+                atomicOr(a.status, kFlagCacheOverflow);
+            }
+          }
+        } else if constexpr (R == Region::FfnUp) {
+          if (ok) {
+            y = gelu_tanh(y);
+            const ACT h = Act<ACT>::from_f(y);
+            c.dst[(size_t)m * N] = h;
+            if constexpr (kSplit) c.dst_lo[(size_t)m * N] = Act<ACT>::from_f(y - Act<ACT>::to_f(h));
+          }
+        } else {
+          y += op[i];
+          if constexpr (R == Region::OprojRes) {
+            if (ok) c.dst_f32[(size_t)m * N] = y;
+          } else {
+            const ACT h = Act<ACT>::from_f(y);
+            if (ok) c.dst[(size_t)m * N] = h;
+            y = Act<ACT>::to_f(h);
+          }
+          if constexpr (kStats) {
+            // (sum, M2) over each 16-row group of the tile (lanes 0..15, 16..31)
+            if (a.stats_out != nullptr && ok) {
+              float s = y;
+#pragma unroll
+              for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+              const float mean = s * (1.0f / 16.0f);
+              float dd = (y - mean) * (y - mean);
+#pragma unroll
+              for (int o = 8; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+              if ((lane & 15) == 0) {
+                float* so = a.stats_out + ((size_t)(c.n >> 4) * M + m) * 2;
+                so[0] = s;
+                so[1] = dd;
+              }
+            }
+          }
+        }
+      }
+    };
+    // Split-K partials: [partial tile][KS * maxc slots][ntok][128] fp32, one
+    // contiguous block per contributor; partial tiles are all tiles when K is
+    // sliced, else only the leftover tiles (u >= U_dp).
+    const size_t slot_floats = (size_t)NTOK * 128;
+    const int tiles = P.tiles;
+    auto partial_base = [&](int t) {
+      const int pt = P.KS > 1 ? t : t - P.U_dp;
+      return a.partials + (size_t)pt * P.KS * P.maxc * slot_floats;
+    };
+    // The idx-th contribution to tile t (slice order, then CTA order) -> its slot.
+    auto slot_of = [&](int t, int idx) {
+      int sl = 0;
+      for (;;) {
+        const int nj = ws_unit_contrib(sl * tiles + t, P, gridDim.x);
+        if (idx < nj) return sl * P.maxc + idx;
+        idx -= nj;
+        ++sl;
+      }
+    };
+    const uint32_t st = smem_u32(sm);  // fix-up staging slots: slot k at st + k * slot_stride
+    const uint32_t slot_stride = (uint32_t)(slot_floats * 4);
+    // Finishes one tile: 8 columns at a time, the accumulator taken from
+    // tensor memory (src 0), from nk staged partial slots in shared memory
+    // (src 1) or from nk partials in global memory (src 2).
+    auto finish_tile = [&](const TileCtx& c, int src, uint32_t tbase, int nk, const float* pg) {
+      float opn[8];
+      if (cbeg < c.mrows) ops_load(c, cbeg, opn);
+#pragma unroll 1
+      for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {
+        float v[8], op[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          op[i] = opn[i];
+          v[i] = 0.f;
+        }
+        if (c8 + 16 < c.mrows) ops_load(c, c8 + 16, opn);
+        if (src == 0) {
+          tmem_ld8(tbase + (uint32_t)c8, v);
+        } else if (src == 1) {
+          const uint32_t e0 = st + (uint32_t)(c8 * 128 + r) * 4u;
+#pragma unroll 1
+          for (int k = 0; k < nk; ++k) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] += lds_f32(e0 + (uint32_t)k * slot_stride + (uint32_t)i * 512u);
+          }
+        } else {
+#pragma unroll 1
+          for (int k = 0; k < nk; ++k) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (c8 + i < c.mrows) v[i] += ld_cg(pg + (size_t)k * slot_floats + (size_t)(c8 + i) * 128 + r);
+          }
+        }
+        epi8(c, c8, v, op);
+      }
+    };
+    // Tiles this CTA finishes as their last contributor; done after its last
+    // segment, when the ring is idle and can stage the partials (a CTA's
+    // range has at most two partial segments: its first and its last unit).
+    int pend_t0 = 0, pend_c0 = 0, pend_t1 = 0, pend_c1 = 0, npend = 0;
+    const int nstage_slots = (int)(((size_t)S * SB) / (slot_floats * 4));  // staging slots in the ring
     int seg = 0;
     bool dead = false;
     dense_for_segments(P, [&](int u, int kc0, int kc1, int j_slot) {
       (void)kc0; (void)kc1;
       const int buf = seg & 1;
-      const int t = u;
-      const int trow = t % row_tiles, jt = t / row_tiles;
-      const int n = trow * 128 + r;
-      const int m0 = jt * NTOK;
-      const int mrows = min(NTOK, M - m0);
-      const int contrib = ws_unit_contrib(u, P, gridDim.x);
-      const float bias = Act<ACT>::to_f(static_cast<const ACT*>(a.bias)[n]);
+      const int sl = u / tiles, t = u - sl * tiles;   // K slice, output tile
+      const int target = ws_tile_target(t, P, gridDim.x);  // contributions that complete the tile
+      const TileCtx c = tile_ctx(t);
       if (!dead) dead = !mbar_wait(accf_bar(buf), (seg >> 1) & 1, a.status);
       dead = __any_sync(0xffffffffu, dead);  // tcgen05.ld below is warp-collective
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * NTOK);
-      // Region epilogue of 16 token columns [m0 + c16, m0 + c16 + 16) of row n.
-      auto epi16 = [&](int c16, const float (&v)[16]) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int mi = c16 + i;  // column within the tile
-          const bool ok = mi < mrows;
-          const int m = m0 + mi;
-          float y = v[i] + bias;
-          if constexpr (R == Region::LnQkv) {
-            if (ok) {
-              const int H = a.H;
-              const int part = n / H, within = n - part * H;
-              if (part == 0) {
-                a.out_f32[(size_t)m * H + within] = y;
-              } else {
-                const int b = m / a.T;
-                const int pos = a.past_len[b] + (m - b * a.T);
-                if (pos >= 0 && pos < a.max_len) {
-                  const int head = within / a.head_dim, dim = within - head * a.head_dim;
-                  ACT* cache = static_cast<ACT*>(part == 1 ? a.k_cache : a.v_cache);
-                  cache[(((size_t)b * a.heads + head) * a.max_len + pos) * a.head_dim + dim] = Act<ACT>::from_f(y);
-                } else {
-                  atomicOr(a.status, kFlagCacheOverflow);
-                }
-              }
-            }
-          } else if constexpr (R == Region::FfnUp) {
-            if (ok) {
-              y = gelu_tanh(y);
-              const ACT h = Act<ACT>::from_f(y);
-              static_cast<ACT*>(a.out_act)[(size_t)m * N + n] = h;
-              if constexpr (kSplit) static_cast<ACT*>(a.out_lo)[(size_t)m * N + n] = Act<ACT>::from_f(y - Act<ACT>::to_f(h));
-            }
-          } else {
-            if constexpr (R == Region::OprojRes) {
-              if (ok) {
-                y += Act<ACT>::to_f(static_cast<const ACT*>(a.resid_act)[(size_t)m * N + n]);
-                a.out_f32[(size_t)m * N + n] = y;
-              }
-            } else {
-              if (ok) {
-                y += a.resid_f32[(size_t)m * N + n];
-                const ACT h = Act<ACT>::from_f(y);
-                static_cast<ACT*>(a.out_act)[(size_t)m * N + n] = h;
-                y = Act<ACT>::to_f(h);
-              }
-            }
-            if constexpr (kStats) {
-              // (sum, M2) over each 16-row group of the tile (lanes 0..15, 16..31)
-              if (a.stats_out != nullptr && mi < mrows) {
-                float s = y;
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                const float mean = s * (1.0f / 16.0f);
-                float dd = (y - mean) * (y - mean);
-#pragma unroll
-                for (int o = 8; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
-                if ((lane & 15) == 0) {
-                  a.stats_out[((size_t)(n >> 4) * M + m) * 2] = s;
-                  a.stats_out[((size_t)(n >> 4) * M + m) * 2 + 1] = dd;
-                }
-              }
-            }
-          }
-        }
-      };
-      if (contrib == 1) {
-        for (int c16 = 0; c16 < mrows; c16 += 16) {
-          float v[16];
-          if (!dead) tmem_ld16(tbase + (uint32_t)c16, v);
-          epi16(c16, v);
-        }
+      if (target == 1) {
+        finish_tile(c, 0, tbase, 0, nullptr);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar(buf));
       } else {
-        // publish this CTA's partial tile, count, the last contributor finishes
-        // (only leftover tiles, u >= U_dp, have several contributors)
-        float* pbase = a.partials + (size_t)(t - P.U_dp) * P.maxc * NTOK * 128;
-        for (int c16 = 0; c16 < mrows; c16 += 16) {
-          float v[16];
-          if (!dead) tmem_ld16(tbase + (uint32_t)c16, v);
+        // publish this CTA's partial tile and count; the last contributor
+        // finishes the tile (only leftover tiles, u >= U_dp, have several)
+        float* pb = partial_base(t) + (size_t)(sl * P.maxc + j_slot) * slot_floats + r;
+#pragma unroll 1
+        for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {
+          float v[8];
+          tmem_ld8(tbase + (uint32_t)c8, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c16 + i < mrows) pbase[((size_t)j_slot * NTOK + c16 + i) * 128 + r] = v[i];
+          for (int i = 0; i < 8; ++i)
+            if (c8 + i < c.mrows) pb[(size_t)(c8 + i) * 128] = v[i];
         }
         tc_fence_before();
         __syncwarp();
@@ -428,37 +572,95 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         // every epilogue thread's partial stores, then one release-acquire arrival
         __threadfence();
         named_bar_sync(kDenseBarEpi, kDenseEpiThreads);
-        if (et == 0) *last_flag = (atomic_add_acq_rel_gpu(&a.counters[t], 1) == contrib - 1);
+        if (et == 0) *last_flag = (atomic_add_acq_rel_gpu(&a.counters[t], 1) == target - 1);
         named_bar_sync(kDenseBarEpi, kDenseEpiThreads);
         const bool last = *last_flag != 0;
-        if (last) {
-          __threadfence();
-          for (int c16 = 0; c16 < mrows; c16 += 16) {
-            float v[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
-            for (int js = 0; js < contrib; ++js) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                if (c16 + i < mrows) v[i] += ld_cg(pbase + ((size_t)js * NTOK + c16 + i) * 128 + r);
-            }
-            epi16(c16, v);
-          }
-          if (et == 0) a.counters[t] = 0;
-        }
         named_bar_sync(kDenseBarEpi, kDenseEpiThreads);  // last_flag is read before the next segment writes it
+        if (last) {
+          if (npend == 0) {
+            pend_t0 = t;
+            pend_c0 = target;
+          } else {
+            pend_t1 = t;
+            pend_c1 = target;
+          }
+          ++npend;
+        }
       }
       ++seg;
     });
+    // Deferred fix-ups: the ring is idle now (every copy into it has been
+    // consumed by the MMAs).  The contributors' partials are bulk-copied into
+    // the ring (one round trip for up to nstage_slots of them) and summed in
+    // slot order (deterministic), then the epilogue runs.
+    uint32_t fph = 0;
+#pragma unroll 1
+    for (int pi = 0; pi < npend && pi < 2; ++pi) {
+      const int t = pi == 0 ? pend_t0 : pend_t1;
+      const int contrib = pi == 0 ? pend_c0 : pend_c1;
+      const TileCtx c = tile_ctx(t);
+      const float* pbase = partial_base(t);
+      const uint32_t slot_bytes = (uint32_t)(c.mrows * 128 * 4);
+      if (nstage_slots < 2) {
+        // a slot larger than half the ring: sum from global memory (the plans
+        // give contiguous slots: one K slice, or one CTA per slice)
+        finish_tile(c, 2, 0u, contrib, pbase);
+      } else {
+        // Rounds of up to nstage_slots partials (one round in the common
+        // case); with more, slot 0 carries the running sum between rounds.
+        for (int js = 0; js < contrib;) {
+          const int dst0 = js == 0 ? 0 : 1;
+          const int nr = min(contrib - js, nstage_slots - dst0);
+          if (et == 0) {
+            // this thread's acquire (the arrival counter) orders the other
+            // contributors' partial stores; the proxy fence orders them before
+            // the async-proxy (bulk copy) reads
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint64_t pol = l2_evict_first_policy();
+            mbar_arrive_expect_tx(fix_bar, (uint32_t)nr * slot_bytes);
+            for (int k = 0; k < nr; ++k)
+              bulk_g2s(st + (uint32_t)(dst0 + k) * slot_stride, pbase + (size_t)slot_of(t, js + k) * slot_floats,
+                       slot_bytes, fix_bar, pol);
+          }
+          if (!dead) dead = !mbar_wait(fix_bar, fph, a.status);
+          fph ^= 1;
+          js += nr;
+          const int nk = dst0 + nr;  // slots holding data: 0 .. nk-1
+          if (js < contrib) {
+            // more rounds follow: fold this round into slot 0 (this thread's row)
+#pragma unroll 1
+            for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {  // this warp's 8-column groups
+              for (int col = c8; col < c8 + 8 && col < c.mrows; ++col) {
+                const uint32_t e = st + (uint32_t)(col * 128 + r) * 4u;
+                float acc = lds_f32(e);
+                for (int k = 1; k < nk; ++k) acc += lds_f32(e + (uint32_t)k * slot_stride);
+                sts_f32(e, acc);
+              }
+            }
+            named_bar_sync(kDenseBarEpi, kDenseEpiThreads);  // staging slots free for the next round
+          } else {
+            finish_tile(c, 1, 0u, nk, nullptr);
+          }
+        }
+      }
+      if (et == 0) a.counters[t] = 0;
+      named_bar_sync(kDenseBarEpi, kDenseEpiThreads);  // the staging slots are read before the next fix-up
+    }
     if constexpr (R == Region::FfnDown) {
       if (a.seq_len_inc != nullptr && blockIdx.x == 0 && warp == kDenseEpiWarp0)
         for (int b = lane; b < a.B; b += 32) a.seq_len_inc[b] += 1;
     }
+    // every tensor-memory read of this warp is done: let the MMA warp free it
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(done_bar);
   }
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
+  // Warp 1 frees the tensor memory once the four epilogue warps are done with
+  // it (an mbarrier, not a CTA barrier: the roles reach the end on different
+  // paths).
   if (warp == kDenseMmaWarp) {
+    if (lane == 0) mbar_wait(done_bar, 0, a.status);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, tcols);
   }

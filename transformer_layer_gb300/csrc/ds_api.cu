@@ -190,8 +190,10 @@ WsLayout ws_layout(const ds_layer& L, int B, int T, const Plans& p) {
   if (p.tile) {
     w.o = w.g = 0;
     const DensePlan* d[4] = {&p.tq, &p.to, &p.tu, &p.td};
-    for (const DensePlan* x : d)  // only leftover tiles (u >= U_dp) publish partials
-      part = std::max(part, (size_t)(x->ws.units - x->ws.U_dp) * x->ws.maxc * x->ntok * 128 * 4);
+    for (const DensePlan* x : d) {  // all tiles when K is sliced, else only the leftover tiles (u >= U_dp)
+      const size_t ptiles = x->ws.KS > 1 ? (size_t)x->ws.tiles : (size_t)(x->ws.units - x->ws.U_dp);
+      part = std::max(part, ptiles * x->ws.KS * x->ws.maxc * x->ntok * 128 * 4);
+    }
     w.partials = take(part);
     w.op_a_hi = take(M * H * 2);
     w.op_a_lo = split ? take(M * H * 2) : 0;
@@ -378,6 +380,9 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   ra.status = bf.status;
 
   if (P.tile) {
+    // (no L2 prefetch of the next GEMM's weights on this path: the tile
+    // kernels end with split-K fix-ups whose L2 traffic it would delay; each
+    // tile CTA requests its own first weight chunks before its dependency wait)
     DenseArgs base;
     base.M = M;
     base.B = B;
@@ -415,8 +420,6 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     r1.head_dim = d;
     r1.max_len = max_len;
     r1.past_len = past_len;
-    r1.next_tmap_w = L.tmap_tile(1, P.to.kc);
-    r1.next_plan = P.to;
     if ((e = launch_dense(Region::LnQkv, ak, r1, xm->a_hi, split ? xm->a_lo : nullptr, st, pdl)) != cudaSuccess)
       return e;
     if ((e = record(es, st)) != cudaSuccess) return e;
@@ -436,8 +439,6 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     r3.resid_act = io.x_in;
     r3.out_f32 = bf.x1;
     r3.stats_out = bf.stats_a;
-    r3.next_tmap_w = L.tmap_tile(2, P.tu.kc);
-    r3.next_plan = P.tu;
     if ((e = record(es, st)) != cudaSuccess) return e;
     if ((e = launch_dense(Region::OprojRes, ak, r3, xm->bh_hi, split ? xm->bh_lo : nullptr, st, pdl)) != cudaSuccess)
       return e;
@@ -464,8 +465,6 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     r4.bias = L.w.b_fc1;
     r4.out_act = bf.op_b_hi;
     r4.out_lo = bf.op_b_lo;
-    r4.next_tmap_w = L.tmap_tile(3, P.td.kc);
-    r4.next_plan = P.td;
     if ((e = launch_dense(Region::FfnUp, ak, r4, xm->a_hi, split ? xm->a_lo : nullptr, st, pdl)) != cudaSuccess)
       return e;
     if ((e = record(es, st)) != cudaSuccess) return e;
@@ -480,10 +479,6 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     r5.out_act = io.x_out;
     r5.stats_out = stats_out;
     r5.seq_len_inc = seq_inc;
-    if (next != nullptr) {
-      r5.next_tmap_w = next->tmap_tile(0, P.tq.kc);
-      r5.next_plan = P.tq;
-    }
     if ((e = record(es, st)) != cudaSuccess) return e;
     if ((e = launch_dense(Region::FfnDown, ak, r5, xm->bf_hi, split ? xm->bf_lo : nullptr, st, pdl)) != cudaSuccess)
       return e;

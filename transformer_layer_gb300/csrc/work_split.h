@@ -129,8 +129,18 @@ DS_HD void ws_leftover_segment(const GemvPlan& P, long long i, long long rb, int
 // Distributes p.units units of p.C chunks each over at most num_ctas CTAs:
 // p.grid, q whole units per CTA, and either whole leftover units or their
 // chunks spread evenly (p.whole, p.U_dp, p.R, p.maxc).  p.units and p.C must
-// be set.
-inline void ws_distribute(GemvPlan& p, int num_ctas) {
+// be set.  one_unit_each: when there are no more units than CTAs, give each
+// CTA exactly one whole unit (grid = units, nothing split).
+inline void ws_distribute(GemvPlan& p, int num_ctas, bool one_unit_each = false) {
+  if (one_unit_each && p.units <= num_ctas) {
+    p.grid = p.units;
+    p.q = 1;
+    p.whole = 0;
+    p.U_dp = p.units;
+    p.R = 0;
+    p.maxc = 1;
+    return;
+  }
   const long long total = (long long)p.units * p.C;
   long long G = num_ctas;
   if (G > total) G = total;
