@@ -103,6 +103,22 @@ def test_gelu_close_to_exact_erf_gelu():
     assert err.max() < 5e-4
 
 
+def test_gelu_at_known_points():
+    """The tanh form of GeLU at x = 0.5, +-1, +-2, 3 against its values in
+    40-digit arithmetic (tests/golden/gelu_tanh_points.txt).  A cubic
+    coefficient off by 2e-4 (0.0445) or sqrt(2/pi) off by 5e-4 moves gelu(2)
+    by ~1e-5, far outside 1e-12."""
+    pts = []
+    for ln in open(os.path.join(GOLDEN, "gelu_tanh_points.txt"), encoding="utf-8"):
+        ln = ln.strip()
+        if ln and not ln.startswith("#"):
+            x, y = ln.split()
+            pts.append((float(x), float(y)))
+    assert len(pts) == 6
+    for x, y in pts:
+        assert abs(float(oracle.gelu_tanh(x)) - y) <= 1e-12 * max(1.0, abs(y)), (x, y)
+
+
 def test_gelu_slope_and_tails():
     h = 1e-6
     assert abs((oracle.gelu_tanh(h) - oracle.gelu_tanh(-h)) / (2 * h) - 0.5) < 1e-9

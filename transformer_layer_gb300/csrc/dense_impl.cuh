@@ -497,21 +497,41 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     };
     const uint32_t st = smem_u32(sm);  // fix-up staging slots: slot k at st + k * slot_stride
     const uint32_t slot_stride = (uint32_t)(slot_floats * 4);
+    // Residual rows staged in shared memory by a fix-up: row col of the tile
+    // (128 features) at ops_sm + col * kResidRowBytes.
+    constexpr uint32_t kResidRowBytes = R == Region::OprojRes ? 128 * sizeof(ACT) : 128 * 4;
+    auto ops_from_smem = [&](uint32_t ops_sm, int c8, float (&o)[8]) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t e = ops_sm + (uint32_t)(c8 + i) * kResidRowBytes;
+        if constexpr (R == Region::OprojRes) {
+          unsigned short u;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(u) : "r"(e + (uint32_t)r * 2u) : "memory");
+          o[i] = Act<ACT>::to_f(*reinterpret_cast<const ACT*>(&u));
+        } else {
+          o[i] = lds_f32(e + (uint32_t)r * 4u);
+        }
+      }
+    };
     // Finishes one tile: 8 columns at a time, the accumulator taken from
     // tensor memory (src 0), from nk staged partial slots in shared memory
-    // (src 1) or from nk partials in global memory (src 2).
-    auto finish_tile = [&](const TileCtx& c, int src, uint32_t tbase, int nk, const float* pg) {
+    // (src 1) or from nk partials in global memory (src 2); the residual from
+    // shared memory when ops_sm != 0, else from global memory.
+    auto finish_tile = [&](const TileCtx& c, int src, uint32_t tbase, int nk, const float* pg, uint32_t ops_sm) {
       float opn[8];
-      if (cbeg < c.mrows) ops_load(c, cbeg, opn);
+      if (ops_sm == 0 && cbeg < c.mrows) ops_load(c, cbeg, opn);
 #pragma unroll 1
       for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {
         float v[8], op[8];
+        if (ops_sm != 0) {
+          ops_from_smem(ops_sm, c8, op);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          op[i] = opn[i];
-          v[i] = 0.f;
+          for (int i = 0; i < 8; ++i) op[i] = opn[i];
+          if (c8 + 16 < c.mrows) ops_load(c, c8 + 16, opn);
         }
-        if (c8 + 16 < c.mrows) ops_load(c, c8 + 16, opn);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
         if (src == 0) {
           tmem_ld8(tbase + (uint32_t)c8, v);
         } else if (src == 1) {
@@ -550,7 +570,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * NTOK);
       if (target == 1) {
-        finish_tile(c, 0, tbase, 0, nullptr);
+        finish_tile(c, 0, tbase, 0, nullptr, 0u);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar(buf));
@@ -604,23 +624,44 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       if (nstage_slots < 2) {
         // a slot larger than half the ring: sum from global memory (the plans
         // give contiguous slots: one K slice, or one CTA per slice)
-        finish_tile(c, 2, 0u, contrib, pbase);
+        finish_tile(c, 2, 0u, contrib, pbase, 0u);
       } else {
         // Rounds of up to nstage_slots partials (one round in the common
         // case); with more, slot 0 carries the running sum between rounds.
         for (int js = 0; js < contrib;) {
           const int dst0 = js == 0 ? 0 : 1;
           const int nr = min(contrib - js, nstage_slots - dst0);
-          if (et == 0) {
+          // the last round also stages the tile's residual rows behind the
+          // partials when they fit (the epilogue then reads no global memory)
+          uint32_t ops_sm = 0;
+          if constexpr (R == Region::OprojRes || R == Region::FfnDown) {
+            const uint32_t off = (uint32_t)(dst0 + nr) * slot_stride;
+            if (js + nr == contrib && (size_t)off + (size_t)c.mrows * kResidRowBytes <= (size_t)S * SB) ops_sm = st + off;
+          }
+          if (et < 32) {  // the first epilogue warp issues the copies
             // this thread's acquire (the arrival counter) orders the other
             // contributors' partial stores; the proxy fence orders them before
             // the async-proxy (bulk copy) reads
             asm volatile("fence.proxy.async.global;" ::: "memory");
             const uint64_t pol = l2_evict_first_policy();
-            mbar_arrive_expect_tx(fix_bar, (uint32_t)nr * slot_bytes);
-            for (int k = 0; k < nr; ++k)
-              bulk_g2s(st + (uint32_t)(dst0 + k) * slot_stride, pbase + (size_t)slot_of(t, js + k) * slot_floats,
-                       slot_bytes, fix_bar, pol);
+            if (et == 0) {
+              mbar_arrive_expect_tx(fix_bar, (uint32_t)nr * slot_bytes + (ops_sm ? (uint32_t)c.mrows * kResidRowBytes : 0u));
+              for (int k = 0; k < nr; ++k)
+                bulk_g2s(st + (uint32_t)(dst0 + k) * slot_stride, pbase + (size_t)slot_of(t, js + k) * slot_floats,
+                         slot_bytes, fix_bar, pol);
+            }
+            __syncwarp();
+            if (ops_sm != 0) {
+              const int n0 = c.n - r;
+              for (int col = et; col < c.mrows; col += 32) {
+                const void* src_row;
+                if constexpr (R == Region::OprojRes)
+                  src_row = static_cast<const ACT*>(a.resid_act) + (size_t)(c.m0 + col) * N + n0;
+                else
+                  src_row = a.resid_f32 + (size_t)(c.m0 + col) * N + n0;
+                bulk_g2s(ops_sm + (uint32_t)col * kResidRowBytes, src_row, kResidRowBytes, fix_bar, pol);
+              }
+            }
           }
           if (!dead) dead = !mbar_wait(fix_bar, fph, a.status);
           fph ^= 1;
@@ -639,7 +680,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
             }
             named_bar_sync(kDenseBarEpi, kDenseEpiThreads);  // staging slots free for the next round
           } else {
-            finish_tile(c, 1, 0u, nk, nullptr);
+            finish_tile(c, 1, 0u, nk, nullptr, ops_sm);
           }
         }
       }
