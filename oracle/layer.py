@@ -106,7 +106,7 @@ def decode_attention(q, k_cache, v_cache, past_len):
     return out
 
 
-def layer_forward(x, p, k_cache, v_cache, past_len, heads, eps=1e-5):
+def layer_forward(x, p, k_cache, v_cache, past_len, heads, eps=1e-5, kv_store=None):
     """One pre-LN layer over T new tokens per sequence ([P1] §3.2, regions 1-4).
 
     x        [B, T, H] layer input (float64 copy of what the device receives)
@@ -115,6 +115,11 @@ def layer_forward(x, p, k_cache, v_cache, past_len, heads, eps=1e-5):
              written in place at positions past_len[b] + t
     past_len [B]
     heads    number of attention heads nh (d = H / nh)
+    kv_store optional function applied to the new keys and values as they are
+             written into the cache (the cache's storage format, e.g. rounding
+             to float16 / bfloat16); attention reads the cache, so with T > 1
+             the new tokens see each other's stored keys and values.  Default:
+             stored exactly.  The returned k_new / v_new are the exact values.
 
     Returns a dict: y (layer output), h1, q, k_new, v_new [B, T, nh, d],
     attn (o before the output projection, [B, T, H]), x1, h2, g.
@@ -128,11 +133,12 @@ def layer_forward(x, p, k_cache, v_cache, past_len, heads, eps=1e-5):
     q = qkv[..., 0:H].reshape(B, T, heads, d)
     k_new = qkv[..., H:2 * H].reshape(B, T, heads, d)
     v_new = qkv[..., 2 * H:3 * H].reshape(B, T, heads, d)
+    store = kv_store if kv_store is not None else (lambda a: a)
     for b in range(B):
         for t in range(T):
             pos = int(past_len[b]) + t
-            k_cache[b, :, pos, :] = k_new[b, t]
-            v_cache[b, :, pos, :] = v_new[b, t]
+            k_cache[b, :, pos, :] = store(k_new[b, t])
+            v_cache[b, :, pos, :] = store(v_new[b, t])
     # Region 2: attention over the cache (scale, causal mask, softmax, . V).
     attn = decode_attention(q, k_cache, v_cache, past_len).reshape(B, T, H)
     # Region 3 (first half): output projection, bias, residual, next LayerNorm.

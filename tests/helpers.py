@@ -42,6 +42,14 @@ def to64(t):
     return t.detach().double().cpu().numpy()
 
 
+def cache_store(dtype):
+    """The KV cache's storage rounding for the oracle (round to nearest even
+    into the cache dtype, float16 or bfloat16)."""
+    def store(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dtype).double().numpy()
+    return store
+
+
 class DeviceLayer:
     """One layer's device weights + library handle (int8 weights quantised on
     the device with ds_quantize_int8 when weight_dtype is torch.int8).

@@ -103,6 +103,29 @@ def test_gelu_close_to_exact_erf_gelu():
     assert err.max() < 5e-4
 
 
+def test_layer_attention_reads_the_stored_cache_rows():
+    """kv_store models the cache's storage format: the new keys / values are
+    written through it and attention reads the cache.  With a store that zeroes
+    values and an empty cache, the one key's value is 0, so the attention
+    output is 0 and x1 = x + b_o exactly; k_new / v_new stay the exact
+    projections, and the cache rows hold the stored values."""
+    rng = np.random.default_rng(31)
+    H, nh, F = 8, 2, 16
+    p = {k: rng.standard_normal(sh) for k, sh in (("ln1_g", (H,)), ("ln1_b", (H,)), ("w_qkv", (3 * H, H)),
+                                                   ("b_qkv", (3 * H,)), ("w_o", (H, H)), ("b_o", (H,)),
+                                                   ("ln2_g", (H,)), ("ln2_b", (H,)), ("w_fc1", (F, H)),
+                                                   ("b_fc1", (F,)), ("w_fc2", (H, F)), ("b_fc2", (H,)))}
+    x = rng.standard_normal((1, 1, H))
+    K = rng.standard_normal((1, nh, 4, H // nh))
+    V = rng.standard_normal((1, nh, 4, H // nh))
+    r = oracle.layer_forward(x, p, K, V, [0], nh, kv_store=lambda a: 0.0 * a)
+    assert np.array_equal(r["attn"], np.zeros((1, 1, H)))
+    np.testing.assert_allclose(r["x1"], x + p["b_o"], rtol=0, atol=1e-15)
+    qkv = oracle.linear(oracle.layer_norm(x, p["ln1_g"], p["ln1_b"]), p["w_qkv"], p["b_qkv"])
+    np.testing.assert_allclose(r["k_new"].reshape(-1), qkv[0, 0, H:2 * H], rtol=0, atol=1e-13)
+    assert np.array_equal(K[0, :, 0, :], np.zeros((nh, H // nh)))
+
+
 def test_gelu_at_known_points():
     """The tanh form of GeLU at x = 0.5, +-1, +-2, 3 against its values in
     40-digit arithmetic (tests/golden/gelu_tanh_points.txt).  A cubic
