@@ -208,6 +208,18 @@ DS_API ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x
                                int32_t* seq_len, void* workspace, size_t ws_bytes,
                                void* stream);
 
+/* A prompt chunk through every layer of the stack: T = new_tokens new tokens
+ * per sequence, query t of sequence b attending keys 0 .. past_len[b] + t
+ * ([P3] triangular_masking); each layer appends its keys and values at
+ * positions past_len[b] .. past_len[b] + T - 1 of its own caches.
+ *   x_in, x_out  [B][T][H] act_dtype (must not alias)
+ *   past_len [B] int32 DEVICE array, read only (not advanced)
+ *   workspace    at least ds_layer_workspace_bytes(layer 0, batch, new_tokens)
+ * Launched directly (no graph capture), 5 or 7 kernels per layer. */
+DS_API ds_status ds_stack_forward(ds_stack* stack, const void* x_in, void* x_out, int batch, int new_tokens,
+                                  void* const* k_caches, void* const* v_caches, int max_len,
+                                  const int32_t* past_len, void* workspace, size_t ws_bytes, void* stream);
+
 /* The same decode step with the step's input and output in HOST memory:
  * copies x_host -> x_dev_in, runs ds_stack_decode_step, copies x_dev_out ->
  * y_host and synchronises `stream` before returning (end-to-end timing).
@@ -249,6 +261,17 @@ DS_API ds_status ds_quantize_int8(const void* w_f16, int n, int k, int group, in
 /* Copies the workspace status word to *flags_out, clears it, and synchronises
  * `stream`.  Returns DS_ERR_DEVICE when a flag was set, DS_OK otherwise. */
 DS_API ds_status ds_workspace_status(void* workspace, uint32_t* flags_out, void* stream);
+
+/* Self-test of the device-side failure detection (the pages describe no such
+ * mechanism; it is a property of this library).  Every wait inside the
+ * kernels is bounded: when it runs out, the kernel records
+ * DS_DEVFLAG_WAIT_TIMEOUT in the workspace status word and returns instead of
+ * hanging.  This call launches one thread that waits, with the same routine,
+ * on a barrier nothing arrives on, for budget_us microseconds (1 .. 10^6);
+ * the wait runs out and sets the flag in `workspace` (any workspace, 256-byte
+ * aligned), which ds_workspace_status then reports.  Asynchronous on
+ * `stream`; the context stays usable. */
+DS_API ds_status ds_selftest_wait_timeout(void* workspace, uint32_t budget_us, void* stream);
 
 /* Number of kernels this library has launched (a graph replay counts every
  * kernel node in the graph) since the process started. */

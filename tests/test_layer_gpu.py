@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import DeviceLayer, check_close, new_workspace, to64
+from helpers import DeviceLayer, cache_store, check_close, new_workspace, to64
 from transformer_layer_gb300 import ds, inputs
 
 pytestmark = pytest.mark.gpu
@@ -32,7 +32,9 @@ def run_layer(L, B, T, past, max_len, seed=7):
     torch.cuda.synchronize()
     code, flags = ds.ds_workspace_status(ws)
     assert code == ds.DS_OK and flags == 0
-    r = oracle.layer_forward(to64(x), L.oracle_params(), K0, V0, past, nh)
+    # the device cache stores the new keys / values in the activation dtype
+    # before attention reads them: the oracle stores them the same way
+    r = oracle.layer_forward(to64(x), L.oracle_params(), K0, V0, past, nh, kv_store=cache_store(L.act_dtype))
     return dict(out=out, kc=kc, vc=vc, kc0=kc0, vc0=vc0, ref=r, ws=ws, nbytes=nbytes, x=x,
                 past_t=past_t)
 
@@ -202,6 +204,34 @@ def test_tile_path_layer(act, B, T):
         L.close()
 
 
+@pytest.mark.parametrize("act,B,T,past", [(torch.float16, 2, 128, [0, 333]), (torch.float16, 1, 512, [77]),
+                                          (torch.bfloat16, 1, 128, [50]), (torch.bfloat16, 3, 64, [5, 0, 130])])
+def test_prompt_chunk_layer_4096(act, B, T, past):
+    """A prompt chunk of 64..512 new tokens per sequence through one
+    4096-hidden layer (tensor-core tiles for the GEMMs, tiled flash attention
+    with the causal mask over the cache and the chunk), ragged cache lengths;
+    every output element and every new cache row against the oracle."""
+    H, nh, F = 4096, 32, 16384
+    L = DeviceLayer(H, nh, F, seed=1012, act_dtype=act, weight_dtype=act)
+    try:
+        res = run_layer(L, B, T, past, max_len=max(past) + T + 16, seed=16)
+        check_layer(L, res, B, T, past, f"prompt {act} B={B} T={T}")
+    finally:
+        L.close()
+
+
+def test_prompt_chunk_int8():
+    """A prompt chunk with MoQ int8 weights (streaming GEMV kernels, 48 rows)
+    and the tiled flash attention."""
+    L = DeviceLayer(1024, 8, 4096, seed=1013, weight_dtype=torch.int8)
+    try:
+        past = [9, 40]
+        res = run_layer(L, 2, 24, past, max_len=80, seed=17)
+        check_layer(L, res, 2, 24, past, "int8 prompt")
+    finally:
+        L.close()
+
+
 def test_quantizer_group32_bit_exact():
     """ds_quantize_int8 with groups of 32 (the layer takes 64 and 128): codes
     and scales bit-exact with the oracle's quantiser."""
@@ -269,6 +299,25 @@ def test_bad_arguments_rejected_before_launch():
             ds.ds_layer_forward(L.handle, x, out, 4097, 1, kc, kc, 8, past, ws, nbytes)
         assert e.value.code == ds.DS_ERR_UNSUPPORTED
         assert ds.ds_launch_count() == n0
+    finally:
+        L.close()
+
+
+def test_bounded_wait_runs_out_and_is_reported():
+    """A device wait that nothing satisfies gives up after its budget, records
+    DS_DEVFLAG_WAIT_TIMEOUT in the workspace status word (read and cleared by
+    ds_workspace_status) and returns; the context then still runs a layer."""
+    L = DeviceLayer(256, 4, 1024, seed=9)
+    try:
+        nbytes = ds.ds_layer_workspace_bytes(L.handle, 1, 1)
+        ws = new_workspace(nbytes)
+        ds.ds_selftest_wait_timeout(ws, 2000)   # 2 ms budget
+        code, flags = ds.ds_workspace_status(ws)
+        assert code == ds.DS_ERR_DEVICE and flags == ds.DS_DEVFLAG_WAIT_TIMEOUT
+        code, flags = ds.ds_workspace_status(ws)
+        assert code == ds.DS_OK and flags == 0
+        res = run_layer(L, 1, 1, [5], max_len=16)
+        check_layer(L, res, 1, 1, [5], "after the timeout")
     finally:
         L.close()
 

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import DeviceLayer, check_close, new_workspace, to64
+from helpers import DeviceLayer, cache_store, check_close, new_workspace, to64
 from transformer_layer_gb300 import ds, inputs
 
 pytestmark = pytest.mark.gpu
@@ -218,3 +218,45 @@ def test_rotating_hidden_buffers_reuse_the_graph(B):
             S.close()
     assert torch.equal(ys["graph"][0], ys["legacy"][0])
     assert torch.equal(ys["graph"][1], ys["legacy"][1])
+
+
+@pytest.mark.parametrize("act,B,T", [(torch.float16, 2, 40), (torch.bfloat16, 1, 96)])
+def test_stack_prompt_chunk(act, B, T):
+    """ds_stack_forward: a prompt chunk through a 3-layer stack.  Each layer
+    is checked against the oracle fed that layer's device input (the output of
+    a prefix stack on copies of the caches, bit-identical to the activation
+    inside the full stack) and its cache before the chunk; the chunk's keys and
+    values land in every layer's cache; past_len is not advanced."""
+    n_layers, H, nh, F, max_len = 3, 512, 8, 2048, 200
+    past = [11 * (b + 1) for b in range(B)]
+    S = DeviceStack(n_layers, H, nh, F, B, max_len, past, seed=1600, act=act, wdt=act)
+    try:
+        x = inputs.hidden(B, T, H, 1600, dtype=act, device="cuda")
+        K = [to64(k) for k in S.kc]
+        V = [to64(v) for v in S.vc]
+        nb = ds.ds_layer_workspace_bytes(S.layers[0].handle, B, T)
+        outs = []
+        for n in range(1, n_layers + 1):   # prefixes [0, n); the last is the full stack
+            h = ds.ds_stack_create([l.handle for l in S.layers[:n]])
+            try:
+                kc = [k.clone() for k in S.kc[:n]] if n < n_layers else S.kc
+                vc = [v.clone() for v in S.vc[:n]] if n < n_layers else S.vc
+                ws = new_workspace(nb)
+                o = torch.empty_like(x)
+                ds.ds_stack_forward(h, x, o, B, T, kc, vc, max_len, S.seq, ws, nb)
+                torch.cuda.synchronize()
+                outs.append(o)
+            finally:
+                ds.ds_stack_destroy(h)
+        assert S.seq.cpu().tolist() == past          # not advanced
+        for l in range(n_layers):
+            xin = x if l == 0 else outs[l - 1]
+            r = oracle.layer_forward(to64(xin), S.layers[l].oracle_params(), K[l], V[l], past, nh,
+                                     kv_store=cache_store(act))
+            check_close(outs[l], r["y"], act, what=f"stack prompt layer {l} y")
+            for b in range(B):
+                for t in range(T):
+                    check_close(S.kc[l][b, :, past[b] + t, :], r["k_new"][b, t], act, what=f"layer {l} k")
+                    check_close(S.vc[l][b, :, past[b] + t, :], r["v_new"][b, t], act, what=f"layer {l} v")
+    finally:
+        S.close()

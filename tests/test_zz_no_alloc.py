@@ -42,14 +42,16 @@ def test_noalloc_matches_workspace_forward_twice():
 def test_noalloc_refuses_workspace_beyond_static_size():
     L = DeviceLayer(4096, 32, 16384, seed=1501)
     try:
-        B = 64
-        assert ds.ds_layer_workspace_bytes(L.handle, B, 1) > (16 << 20)
-        x = torch.zeros(B, 1, 4096, dtype=torch.float16, device="cuda")
-        kc = torch.zeros(B, 32, 4, 128, dtype=torch.float16, device="cuda")
+        B, T = 16, 32   # a 512-row prompt chunk
+        assert ds.ds_layer_workspace_bytes(L.handle, B, T) > (16 << 20)
+        x = torch.zeros(B, T, 4096, dtype=torch.float16, device="cuda")
+        kc = torch.zeros(B, 32, T, 128, dtype=torch.float16, device="cuda")
         past = torch.zeros(B, dtype=torch.int32, device="cuda")
+        n0 = ds.ds_launch_count()
         with pytest.raises(ds.DSError) as e:
-            ds.ds_layer_forward_noalloc(L.handle, x, torch.empty_like(x), B, 1, kc, kc.clone(), 4, past)
+            ds.ds_layer_forward_noalloc(L.handle, x, torch.empty_like(x), B, T, kc, kc.clone(), T, past)
         assert e.value.code == ds.DS_ERR_UNSUPPORTED
+        assert ds.ds_launch_count() == n0
     finally:
         L.close()
 

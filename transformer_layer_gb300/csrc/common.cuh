@@ -101,13 +101,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase of `bar` with the given parity to complete, for at
-// most kWaitBudgetNs; on timeout records kFlagWaitTimeout and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+// most budget_ns (kWaitBudgetNs by default); on timeout records
+// kFlagWaitTimeout and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status,
+                                          unsigned long long budget_ns = kWaitBudgetNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (unsigned i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_ns() - t0 > kWaitBudgetNs) {
+    if ((i & 63u) == 0 && global_ns() - t0 > budget_ns) {
       atomicOr(status, kFlagWaitTimeout);
       return false;
     }

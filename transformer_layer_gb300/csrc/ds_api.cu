@@ -82,6 +82,8 @@ ds_status device_info(int* dev_out, DevInfo* out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(tile kernels)");
     e = prepare_attention_kernels(d.max_smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention kernel)");
+    e = prepare_attention_prefill_kernels(d.max_smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prompt attention kernel)");
     d.ready = true;
   }
   *dev_out = dev;
@@ -378,6 +380,10 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   ra.stage_keys = attn_stage_keys(d, max_len, ra.nsplit);
   ra.smem = attn_smem_bytes(d, ra.stage_keys);
   ra.status = bf.status;
+  // prompt chunks: tiled flash attention; decode and short chunks: split-KV
+  auto launch_attn = [&](const AttnArgs& x) {
+    return T >= kPrefillMinTokens ? launch_attention_prefill(ak, x, st, pdl) : launch_attention(ak, x, st, pdl);
+  };
 
   if (P.tile) {
     // (no L2 prefetch of the next GEMM's weights on this path: the tile
@@ -427,7 +433,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     ra.out_hi = bf.op_b_hi;
     ra.out_lo = bf.op_b_lo;
     if ((e = record(es, st)) != cudaSuccess) return e;
-    if ((e = launch_attention(ak, ra, st, pdl)) != cudaSuccess) return e;
+    if ((e = launch_attn(ra)) != cudaSuccess) return e;
     if ((e = record(es, st)) != cudaSuccess) return e;
     // R3: O-proj + bias + residual + LayerNorm2 statistics
     DenseArgs r3 = base;
@@ -532,7 +538,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   // R2: attention
   ra.out = bf.o;
   if ((e = record(es, st)) != cudaSuccess) return e;
-  if ((e = launch_attention(ak, ra, st, pdl)) != cudaSuccess) return e;
+  if ((e = launch_attn(ra)) != cudaSuccess) return e;
   if ((e = record(es, st)) != cudaSuccess) return e;
 
   // R3: O-proj + bias + residual + LayerNorm2 statistics
@@ -643,7 +649,8 @@ ds_status check_device(const ds_layer& L) {
 
 ds_status check_attn_smem(const ds_layer& L) {
   const int d = L.cfg.hidden / L.cfg.heads;
-  if (attn_smem_bytes(d, attn_stage_keys(d, 1 << 30, 1)) > (size_t)L.max_smem)
+  if (attn_smem_bytes(d, attn_stage_keys(d, 1 << 30, 1)) > (size_t)L.max_smem ||
+      attn_prefill_smem_bytes(akind(L.cfg.act_dtype), d) > (size_t)L.max_smem)
     return fail(DS_ERR_UNSUPPORTED, "attention kernel's shared memory exceeds the device limit");
   return DS_OK;
 }
@@ -900,9 +907,9 @@ void drop_graph(ds_stack* S) {
 
 cudaError_t enqueue_stack(ds_stack* S, const Plans& p, const Bufs& bf, const XMaps* xm, const void* x_in, void* x_out,
                           int B, void* const* kc, void* const* vc, int max_len, int32_t* seq, cudaStream_t st,
-                          bool pdl, EventSink* es, std::vector<PatchNode>* rec) {
+                          bool pdl, EventSink* es, std::vector<PatchNode>* rec, int T = 1, bool advance = true) {
   const int L = (int)S->layers.size();
-  const size_t act_bytes = (size_t)B * S->layers[0]->cfg.hidden * 2;
+  const size_t act_bytes = (size_t)B * T * S->layers[0]->cfg.hidden * 2;
   for (int l = 0; l < L; ++l) {
     LayerIO io;
     io.x_in = (l == 0) ? x_in : static_cast<const void*>(bf.act + ((l - 1) & 1) * act_bytes);
@@ -911,9 +918,9 @@ cudaError_t enqueue_stack(ds_stack* S, const Plans& p, const Bufs& bf, const XMa
     io.out_is_caller = (l == L - 1);
     const float* sin = (l == 0) ? nullptr : bf.stats_b;
     float* sout = (l == L - 1) ? nullptr : bf.stats_b;
-    cudaError_t e = enqueue_layer(*S->layers[l], p, bf, xm, io, B, 1, kc[l], vc[l], max_len, seq, sin, sout,
-                                  (l == L - 1) ? seq : nullptr, (l + 1 < L) ? S->layers[l + 1] : nullptr, l == 0, st,
-                                  pdl, es, rec);
+    cudaError_t e = enqueue_layer(*S->layers[l], p, bf, xm, io, B, T, kc[l], vc[l], max_len, seq, sin, sout,
+                                  (l == L - 1 && advance) ? seq : nullptr, (l + 1 < L) ? S->layers[l + 1] : nullptr,
+                                  l == 0, st, pdl, es, rec);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -1070,6 +1077,38 @@ ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x_out, i
   return DS_OK;
 }
 
+ds_status ds_stack_forward(ds_stack* stack, const void* x_in, void* x_out, int batch, int new_tokens,
+                           void* const* k_caches, void* const* v_caches, int max_len, const int32_t* past_len,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  if (stack == nullptr) return fail(DS_ERR_INVALID_ARG, "stack is null");
+  if (k_caches == nullptr || v_caches == nullptr) return fail(DS_ERR_INVALID_ARG, "cache arrays are null");
+  const int L = (int)stack->layers.size();
+  const ds_layer& L0 = *stack->layers[0];
+  for (int l = 0; l < L; ++l) {
+    ds_status s = check_forward_args(L0, x_in, x_out, batch, new_tokens, k_caches[l], v_caches[l], max_len, past_len,
+                                     workspace);
+    if (s != DS_OK) return s;
+  }
+  ds_status s = check_device(L0);
+  if (s != DS_OK) return s;
+  if ((s = check_attn_smem(L0)) != DS_OK) return s;
+  const int M = batch * new_tokens;
+  Plans p;
+  if (!make_plans(L0, M, &p)) return fail(DS_ERR_UNSUPPORTED, "no GEMM work split for this shape");
+  const WsLayout wl = ws_layout(L0, batch, new_tokens, p);
+  if (ws_bytes < wl.total) return fail(DS_ERR_WORKSPACE, "workspace smaller than ds_layer_workspace_bytes()");
+  const Bufs bf = bufs_of(workspace, wl);
+  XMaps xm;
+  if (p.tile && !make_xmaps(L0, p, bf, M, &xm))
+    return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation operand");
+  cudaError_t e = enqueue_stack(stack, p, bf, &xm, x_in, x_out, batch, k_caches, v_caches, max_len,
+                                const_cast<int32_t*>(past_len), static_cast<cudaStream_t>(stream), true, nullptr,
+                                nullptr, new_tokens, /*advance=*/false);
+  if (e != cudaSuccess) return cuda_fail(e, "region kernel launch");
+  g_launches += kernels_per_layer(p) * L;
+  return DS_OK;
+}
+
 ds_status ds_stack_decode_host(ds_stack* stack, const void* x_host, void* y_host, void* x_dev_in,
                                void* x_dev_out, int batch, void* const* k_caches,
                                void* const* v_caches, int max_len, int32_t* seq_len,
@@ -1125,6 +1164,17 @@ ds_status ds_quantize_int8(const void* w_f16, int n, int k, int group, int8_t* c
     return fail(DS_ERR_INVALID_ARG, "n >= 1 and k a positive multiple of group required");
   cudaError_t e = launch_quantize_int8(w_f16, n, k, group, codes, scales_f16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize_int8 launch");
+  g_launches += 1;
+  return DS_OK;
+}
+
+ds_status ds_selftest_wait_timeout(void* workspace, uint32_t budget_us, void* stream) {
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DS_ERR_INVALID_ARG, "workspace must be non-null and 256-byte aligned");
+  if (budget_us < 1 || budget_us > 1000000) return fail(DS_ERR_INVALID_ARG, "budget_us must be in 1 .. 1000000");
+  cudaError_t e = launch_wait_timeout_selftest(static_cast<unsigned*>(workspace), (unsigned long long)budget_us * 1000ull,
+                                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait-timeout self-test launch");
   g_launches += 1;
   return DS_OK;
 }

@@ -194,6 +194,12 @@ size_t attn_smem_bytes(int head_dim, int stage_keys);
 int attn_stage_keys(int head_dim, int max_len, int nsplit);
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl);
 cudaError_t prepare_attention_kernels(int max_smem);
+// Prompt chunks: tiled tensor-core (flash) attention, used from this many new
+// tokens per sequence on.
+constexpr int kPrefillMinTokens = 16;
+size_t attn_prefill_smem_bytes(ActKind ak, int head_dim);
+cudaError_t launch_attention_prefill(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl);
+cudaError_t prepare_attention_prefill_kernels(int max_smem);
 
 }  // namespace ds
 
@@ -214,6 +220,7 @@ void set_last_error(const char* msg);
 // The device a layer was created on.
 int layer_device(const ds_layer* layer);
 
+cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned long long budget_ns, cudaStream_t st);
 cudaError_t launch_quantize_int8(const void* w, int n, int k, int group, int8_t* codes, void* scales,
                                  cudaStream_t st);
 

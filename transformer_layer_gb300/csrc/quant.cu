@@ -61,4 +61,23 @@ cudaError_t launch_quantize_int8(const void* w, int n, int k, int group, int8_t*
   return cudaGetLastError();
 }
 
+// Self-test of the bounded-wait path: one thread waits on an mbarrier that
+// nothing arrives on, with the same wait routine as the pipeline kernels and
+// a budget of budget_ns.  The wait runs out, records kFlagWaitTimeout in
+// *status and the kernel returns (no copy is in flight into its shared memory).
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(unsigned* status, unsigned long long budget_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, status, budget_ns);
+}
+
+cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned long long budget_ns, cudaStream_t st) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(status, budget_ns);
+  return cudaGetLastError();
+}
+
 }  // namespace ds

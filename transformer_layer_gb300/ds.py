@@ -35,6 +35,8 @@ _SIGS = {
     "ds_stack_workspace_bytes": (C.c_size_t, [_vp, C.c_int]),
     "ds_stack_decode_step": (C.c_int, [_vp, _vp, _vp, C.c_int, C.POINTER(_vp), C.POINTER(_vp),
                                        C.c_int, _vp, _vp, C.c_size_t, _vp]),
+    "ds_stack_forward": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, C.POINTER(_vp), C.POINTER(_vp), C.c_int, _vp,
+                                   _vp, C.c_size_t, _vp]),
     "ds_stack_decode_host": (C.c_int, [_vp, _vp, _vp, _vp, _vp, C.c_int, C.POINTER(_vp),
                                        C.POINTER(_vp), C.c_int, _vp, _vp, C.c_size_t, _vp]),
     "ds_stack_set_profiling": (C.c_int, [_vp, C.c_int]),
@@ -42,6 +44,7 @@ _SIGS = {
     "ds_stack_graph_captures": (C.c_uint64, [_vp]),
     "ds_quantize_int8": (C.c_int, [_vp, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp]),
     "ds_workspace_status": (C.c_int, [_vp, C.POINTER(C.c_uint32), _vp]),
+    "ds_selftest_wait_timeout": (C.c_int, [_vp, C.c_uint32, _vp]),
     "ds_launch_count": (C.c_uint64, []),
     "ds_status_string": (C.c_char_p, [C.c_int]),
     "ds_last_error": (C.c_char_p, []),
@@ -190,6 +193,13 @@ def ds_stack_decode_step(stack, x_in, x_out, batch, k_caches, v_caches, max_len,
                                        _stream(stream)), "ds_stack_decode_step")
 
 
+def ds_stack_forward(stack, x_in, x_out, batch, new_tokens, k_caches, v_caches, max_len, past_len, ws, ws_bytes,
+                     stream=None):
+    _check(load().ds_stack_forward(stack, _ptr(x_in), _ptr(x_out), batch, new_tokens, _ptr_array(k_caches),
+                                   _ptr_array(v_caches), max_len, _ptr(past_len), _ptr(ws), ws_bytes,
+                                   _stream(stream)), "ds_stack_forward")
+
+
 def ds_stack_decode_host(stack, x_host, y_host, x_dev_in, x_dev_out, batch, k_caches, v_caches, max_len,
                          seq_len, ws, ws_bytes, stream=None):
     _check(load().ds_stack_decode_host(stack, _ptr(x_host), _ptr(y_host), _ptr(x_dev_in), _ptr(x_dev_out),
@@ -227,6 +237,10 @@ def ds_workspace_status(ws, stream=None):
     if code not in (DS_OK, DS_ERR_DEVICE):
         raise DSError(code, "ds_workspace_status")
     return code, int(flags.value)
+
+
+def ds_selftest_wait_timeout(ws, budget_us, stream=None):
+    _check(load().ds_selftest_wait_timeout(_ptr(ws), budget_us, _stream(stream)), "ds_selftest_wait_timeout")
 
 
 def ds_launch_count():
