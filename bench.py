@@ -14,7 +14,17 @@ dominant region kernel (FFN) timed alone in profile mode; `step_roofline` is
 the whole step's algorithmic bytes over its time.
 
 --impl reference times the float64 CPU oracle (oracle/) on this machine's host
-cores on the same workload (bounded samples, see `cpu_baseline.sample`).
+cores: whole decode steps of the same stack (every layer sharing one layer's
+float64 weights; the oracle's time does not depend on their values).  The
+`cpu_baseline` leg does the same on a bounded number of steps.
+
+--prefill T times a prompt chunk of T new tokens per sequence through the
+7B-shaped stack (ds_stack_forward over an empty cache): tokens/s, and the
+tensor-core roofline of the dominant GEMM and of the whole chunk against the
+measured bf16 dense peak.
+
+`host_us_per_call` is the host time of one ds_stack_decode_step call with the
+input buffer rotating (the captured graph's x_in node is updated in place).
 
 Multi-GPU (torchrun, N > 1): every rank runs an independent replica (its own
 weights and caches; decode of independent sequences needs no exchange), the
@@ -71,6 +81,9 @@ def parse():
                     help="13b-int8: MoQ group length along K of the attention matrices")
     ap.add_argument("--mlp-extra-grouping", action="store_true",
                     help="13b-int8: FFN matrices in groups of half that length")
+    ap.add_argument("--prefill", type=int, default=0,
+                    help="prompt chunk of this many new tokens per sequence through the 7B-shaped stack "
+                         "(ds_stack_forward, empty cache); 0 = decode (the headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=4)
     return ap.parse_args()
@@ -217,30 +230,49 @@ def region_bytes(H, F, B, past, wbytes=2.0):
 REGIONS = ("ln_qkv", "attention", "oproj_res", "ffn_up", "ffn_down")
 
 
+class OracleStack:
+    """The float64 CPU oracle (oracle/) running whole decode steps of the
+    7B-shaped stack: every layer has its own KV cache and the output of layer l
+    feeds layer l + 1.  All layers share one layer's float64 weights, converted
+    once: the oracle's time does not depend on the weight values."""
+
+    def __init__(self, B, layers):
+        import numpy as np
+        from transformer_layer_gb300 import inputs
+        H, F, nh, d, past = 4096, 16384, 32, 128, 512
+        self.B, self.layers, self.nh, self.past, self.H = B, layers, nh, past, H
+        self.p = {k: v.double().numpy() for k, v in inputs.layer_params(H, F, 1002, 0, device="cpu").items()}
+        self.K, self.V = [], []
+        for l in range(layers):
+            kc, vc = inputs.kv_cache(B, nh, past + CYCLE, d, 1002, layer=l, device="cpu")
+            self.K.append(kc.double().numpy())
+            self.V.append(vc.double().numpy())
+        self.xs = [inputs.hidden(B, 1, H, 1002, step=i, device="cpu").double().numpy() for i in range(4)]
+        self.np = np
+
+    def step(self, i):
+        """One decode step (cache position past + i % 64); returns seconds."""
+        import oracle
+        t0 = time.perf_counter()
+        h = self.xs[i % 4]
+        for l in range(self.layers):
+            h = oracle.layer_forward(h, self.p, self.K[l], self.V[l], [self.past + (i % CYCLE)] * self.B, self.nh)["y"]
+        return time.perf_counter() - t0
+
+
 def cpu_baseline_sample(B, budget_s=10.0, layers=32):
-    """The oracle, as it stands, on one 7B-shaped layer at a time (float64 numpy);
-    returns (tokens/s for the whole stack, cores, sample description)."""
-    import numpy as np
-    import oracle
-    from transformer_layer_gb300 import inputs
-    H, F, nh, d, past = 4096, 16384, 32, 128, 512
-    p = {k: v.numpy() for k, v in inputs.layer_params(H, F, 1002, 0, device="cpu").items()}
-    kc, vc = inputs.kv_cache(B, nh, past + 1, d, 1002, device="cpu")
-    K0, V0 = kc.numpy(), vc.numpy()
-    x = inputs.hidden(B, 1, H, 1002, device="cpu").numpy()
+    """The oracle, as it stands, running whole decode steps of the 7B-shaped
+    stack on this host's cores; returns (tokens/s, cores, sample description)."""
+    st = OracleStack(B, layers)
     times = []
     t_end = time.perf_counter() + budget_s
-    while len(times) < 2 or (time.perf_counter() < t_end and len(times) < 16):
-        K, V = K0.astype(np.float64), V0.astype(np.float64)
-        t0 = time.perf_counter()
-        oracle.layer_forward(x, p, K, V, [past] * B, nh)
-        times.append(time.perf_counter() - t0)
-    per_layer = statistics.median(times)
+    while not times or (time.perf_counter() < t_end and len(times) < 16):
+        times.append(st.step(len(times)))
+    per_step = statistics.median(times)
     cores = len(os.sched_getaffinity(0))
-    sample = (f"{len(times)} single-layer forwards of the float64 oracle (numpy; BLAS threads "
-              f"over {cores} host cores) on one 7B-shaped layer, batch {B}, 512 cached positions; "
-              f"median {per_layer:.3f} s/layer scaled to {layers} layers per token")
-    return B / (per_layer * layers), cores, sample
+    sample = (f"{len(times)} whole decode steps ({layers} layers, batch {B}, 512 cached positions) of the "
+              f"float64 oracle (numpy; BLAS threads over {cores} host cores), median {per_step:.3f} s/step")
+    return B / per_step, cores, sample
 
 
 def max_over_ranks(x, world, device="cpu"):
@@ -259,39 +291,26 @@ def job_throughput(units_per_rank_step, steps, world, seconds):
 
 
 def run_reference(args):
-    """--impl reference: the float64 CPU oracle on this host's cores (rank 0 only)."""
+    """--impl reference: the float64 CPU oracle on this host's cores (rank 0
+    only), whole decode steps of the 7B-shaped stack."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import numpy as np
-    import oracle
-    from transformer_layer_gb300 import inputs
     B = args.batch
     layers = args.layers if args.layers is not None else MODELS["7b"]["layers"]
-    H, F, nh, d, past = 4096, 16384, 32, 128, 512   # the oracle arm times the 7B-shaped layer
-    p = {k: v.numpy() for k, v in inputs.layer_params(H, F, 1002, 0, device="cpu").items()}
-    kc, vc = inputs.kv_cache(B, nh, past + CYCLE, d, 1002, device="cpu")
-    K0, V0 = kc.numpy(), vc.numpy()
-    xs = [inputs.hidden(B, 1, H, 1002, step=i, device="cpu").numpy() for i in range(4)]
-
-    def one_layer(i):
-        K, V = K0.astype(np.float64), V0.astype(np.float64)
-        t0 = time.perf_counter()
-        oracle.layer_forward(xs[i % 4], p, K, V, [past + (i % CYCLE)] * B, nh)
-        return time.perf_counter() - t0
-
+    st = OracleStack(B, layers)
     for i in range(max(args.warmup, 0)):
-        one_layer(i)
-    ts = [one_layer(i) for i in range(args.steps)]
-    per_layer = sum(ts) / len(ts)
-    value = B / (per_layer * layers)
+        st.step(i)
+    ts = [st.step(args.warmup + i) for i in range(args.steps)]
+    per_step = sum(ts) / len(ts)
+    value = B / per_step
     cores = len(os.sched_getaffinity(0))
-    sample = (f"each step = one float64 oracle forward of one 7B-shaped layer (1/{layers} of a "
-              f"decode step), batch {B}, cache {past}+i positions; tokens/s scaled by {layers} layers")
+    sample = (f"each step = one whole decode step of the float64 oracle through {layers} 7B-shaped layers "
+              f"(one layer's weights shared by all layers), batch {B}, cache 512 + i positions")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_layer * layers * 1000.0, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": per_step * 1000.0, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": workload_config(B, layers),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -299,6 +318,140 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def prefill_flops(H, F, nh, layers, B, T, past=0):
+    """FLOPs of one prompt chunk: the four GEMMs (2 per multiply-add) and
+    attention (QK^T and PV: 4 d per query-key pair and head) of every layer,
+    query t seeing past + t + 1 keys; per region kernel and in total."""
+    M = B * T
+    pairs = B * (T * past + T * (T + 1) // 2)
+    reg = {"ln_qkv": 2.0 * M * 3 * H * H, "attention": 4.0 * H * pairs, "oproj_res": 2.0 * M * H * H,
+           "ffn_up": 2.0 * M * F * H, "ffn_down": 2.0 * M * H * F}
+    return reg, layers * sum(reg.values())
+
+
+def load_tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def run_prefill(args, torch, dist, world, rank, local, dev):
+    """--prefill T: one step = a prompt chunk of T new tokens per sequence
+    through the 7B-shaped stack (ds_stack_forward; cache empty)."""
+    from transformer_layer_gb300 import ds, inputs
+    m = MODELS["7b"]
+    B, T = args.batch, args.prefill
+    L = args.layers if args.layers is not None else m["layers"]
+    H, nh, F = m["H"], m["nh"], m["F"]
+    act = torch.bfloat16 if args.bf16 else torch.float16
+    seed = 1002 + rank
+    stream = torch.cuda.Stream(device=dev)
+    layers, params, kcs, vcs = [], [], [], []
+    for l in range(L):
+        p = inputs.layer_params(H, F, seed, l, dtype=act, device=dev)
+        params.append(p)
+        layers.append(ds.ds_layer_create(H, nh, F, p, act, act))
+        k, v = inputs.kv_cache(B, nh, T, H // nh, seed, l, dtype=act, device=dev)
+        kcs.append(k)
+        vcs.append(v)
+    stack = ds.ds_stack_create(layers)
+    nbytes = ds.ds_layer_workspace_bytes(layers[0], B, T)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ds.ds_workspace_init(ws, nbytes, stream)
+    past = torch.zeros((B,), dtype=torch.int32, device=dev)
+    xs = [inputs.hidden(B, T, H, seed, step=i, dtype=act, device=dev) for i in range(2)]
+    out = torch.empty_like(xs[0])
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        ds.ds_stack_forward(stack, xs[i % 2], out, B, T, kcs, vcs, T, past, ws, nbytes, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = ds.ds_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+    stream.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    launches = ds.ds_launch_count() - launches0
+    ms_max = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    value = job_throughput(B * T, args.steps, world, ms_max / 1000.0)
+    # end to end: prompt from pinned host memory, result back, synchronised
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = torch.empty(out.shape, dtype=act).pin_memory()
+    xd = torch.empty_like(xs[0])
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(4, min(args.steps, 16))
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            xd.copy_(xh[i % 2], non_blocking=True)
+        ds.ds_stack_forward(stack, xd, out, B, T, kcs, vcs, T, past, ws, nbytes, stream)
+        with torch.cuda.stream(stream):
+            yh.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_value = job_throughput(B * T, e2e_steps, world, max_over_ranks(time.perf_counter() - t0, world, dev))
+    # region kernels alone (profile mode)
+    ds.ds_stack_set_profiling(stack, True)
+    ds.ds_stack_region_times(stack)
+    with torch.cuda.stream(stream):
+        for i in range(max(1, args.profile_steps // 2)):
+            step(i)
+    us, _ = ds.ds_stack_region_times(stack)
+    ds.ds_stack_set_profiling(stack, False)
+    reg, total = prefill_flops(H, F, nh, L, B, T)
+    burst, sustained, kind = load_tensor_peak()
+    shares = {r: us[i] for i, r in enumerate(REGIONS)}
+    dom = max(("ffn_up", "ffn_down", "ln_qkv", "oproj_res"), key=lambda r: shares[r])
+    achieved = reg[dom] / (shares[dom] * 1e-6) / 1e12
+    step_tf = total / (ms_max / args.steps / 1000.0) / 1e12
+    line = {
+        "metric": f"prefill tokens/sec ({m['title']}, prompt chunk of {T} tokens, batch {B})",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if args.bf16 else "f16",
+        "data": "synthetic (seeded: weights N(0,0.02), biases N(0,0.01), LN gamma 1+N(0,0.1), beta N(0,0.1), "
+                "inputs N(0,1))",
+        "config": {"workload": f"{m['title']}: {L} pre-LN layers, hidden {H}, {nh} heads, FFN {F}; prompt "
+                               f"chunk of {T} new tokens per sequence over an empty cache, batch {B}",
+                   "batch": B, "layers": L, "new_tokens": T,
+                   "l2": f"inputs larger than L2: {L * layer_bytes(H, F) / 1e9:.1f} GB of weights per step"},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+                     "frac": achieved / burst, "peak_source": f"{kind} bf16 dense (burst; fp16 runs at the same "
+                     f"tensor rate)", "flops_per_launch": reg[dom], "us_per_launch": shares[dom],
+                     "traffic": None},
+        "step_roofline": {"flops_per_step": total, "achieved": step_tf, "peak": sustained, "unit": "TFLOP/s",
+                          "frac": step_tf / sustained, "peak_source": f"{kind} bf16 dense (sustained)"},
+        "region_us": shares,
+        "cpu_baseline": None,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": B * T * H * 2,
+                "d2h_bytes_per_step": B * T * H * 2, "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ds.ds_stack_destroy(stack)
+    for l in layers:
+        ds.ds_layer_destroy(l)
 
 
 def main():
@@ -321,6 +474,11 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from transformer_layer_gb300 import ds, inputs
+    if args.prefill > 0:
+        run_prefill(args, torch, dist, world, rank, local, dev)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     m = MODELS[args.model]
     B = args.batch
@@ -406,6 +564,17 @@ def main():
     clocks = sampler.stop()
     launches = ds.ds_launch_count() - launches0
     ms = ev0.elapsed_time(ev1)
+    # host cost of one ds_stack_decode_step call (graph replay; the inputs
+    # rotate over 8 buffers, so the graph's x_in node is updated each call)
+    host_us = []
+    with torch.cuda.stream(stream):
+        for i in range(16):
+            if i % CYCLE == 0:
+                seq.copy_(seq0)
+            t0 = time.perf_counter()
+            ds.ds_stack_decode_step(stack, xs[i % n_x], out, B, kcs, vcs, max_len, seq, ws, nbytes, stream)
+            host_us.append((time.perf_counter() - t0) * 1e6)
+    stream.synchronize()
     ms_max = max_over_ranks(ms, world, dev)
     value = job_throughput(B, args.steps, world, ms_max / 1000.0)
 
@@ -472,6 +641,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": B * H * 2,
                 "d2h_bytes_per_step": B * H * 2, "steps": e2e_steps},
         "gpu_launches": launches,
+        "host_us_per_call": statistics.median(host_us),
+        "graph_captures": ds.ds_stack_graph_captures(stack),
         "clocks": clocks,
     }
     if rank == 0:

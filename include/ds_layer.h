@@ -215,7 +215,9 @@ DS_API ds_status ds_stack_decode_step(ds_stack* stack, const void* x_in, void* x
  *   x_in, x_out  [B][T][H] act_dtype (must not alias)
  *   past_len [B] int32 DEVICE array, read only (not advanced)
  *   workspace    at least ds_layer_workspace_bytes(layer 0, batch, new_tokens)
- * Launched directly (no graph capture), 5 or 7 kernels per layer. */
+ * Launched directly (no graph capture), 5 or 7 kernels per layer.  In
+ * profile mode (ds_stack_set_profiling) the region kernels are timed as for
+ * ds_stack_decode_step and the call synchronises the stream. */
 DS_API ds_status ds_stack_forward(ds_stack* stack, const void* x_in, void* x_out, int batch, int new_tokens,
                                   void* const* k_caches, void* const* v_caches, int max_len,
                                   const int32_t* past_len, void* workspace, size_t ws_bytes, void* stream);

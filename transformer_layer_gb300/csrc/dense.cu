@@ -34,7 +34,7 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   DensePlan p;
   p.row_tiles = N / 128;
   int ntok = (M + 15) / 16 * 16;
-  const int ntok_max = split ? 128 : 256;  // (bf16 stages carry hi and lo operands)
+  const int ntok_max = 128;  // (wider token tiles re-stream more X through L2 per FLOP)
   if (ntok > ntok_max) ntok = ntok_max;
   p.ntok = ntok;
   p.tok_tiles = (M + ntok - 1) / ntok;

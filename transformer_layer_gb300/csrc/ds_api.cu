@@ -1101,11 +1101,33 @@ ds_status ds_stack_forward(ds_stack* stack, const void* x_in, void* x_out, int b
   XMaps xm;
   if (p.tile && !make_xmaps(L0, p, bf, M, &xm))
     return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation operand");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  EventSink es;
+  if (stack->profiling) {
+    while (stack->events.size() < (size_t)2 * 5 * L) {
+      cudaEvent_t ev;
+      cudaError_t e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+      stack->events.push_back(ev);
+    }
+    es.ev = &stack->events;
+  }
   cudaError_t e = enqueue_stack(stack, p, bf, &xm, x_in, x_out, batch, k_caches, v_caches, max_len,
-                                const_cast<int32_t*>(past_len), static_cast<cudaStream_t>(stream), true, nullptr,
-                                nullptr, new_tokens, /*advance=*/false);
+                                const_cast<int32_t*>(past_len), st, !stack->profiling,
+                                stack->profiling ? &es : nullptr, nullptr, new_tokens, /*advance=*/false);
   if (e != cudaSuccess) return cuda_fail(e, "region kernel launch");
   g_launches += kernels_per_layer(p) * L;
+  if (stack->profiling) {
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize (profile)");
+    for (int k = 0; k < 5 * L; ++k) {
+      float ms = 0.f;
+      e = cudaEventElapsedTime(&ms, stack->events[2 * k], stack->events[2 * k + 1]);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+      stack->acc_ms[k % 5] += ms;
+      stack->acc_n[k % 5] += 1;
+    }
+  }
   return DS_OK;
 }
 
