@@ -256,6 +256,47 @@ DS_API uint64_t ds_stack_graph_captures(const ds_stack* stack);
 DS_API ds_status ds_quantize_int8(const void* w_f16, int n, int k, int group, int8_t* codes,
                            void* scales_f16, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Residual-MoE (PR-MoE) FFN block ([P3] section "用 PR-MoE 结构进一步提速并降低推理
+ * 成本": mlp_type 'residual', per-layer expert counts; configuration table:
+ * moe.type standard / residual, moe_experts).  The page gives no formula; the
+ * reading implemented, for R rows of hidden states x:
+ *   h = LayerNorm2(x);  p = softmax(h W_g^T) over E experts;
+ *   e = argmax p (ties: the lowest index);
+ *   y = x + MLP(h) + p_e * Expert_e(h),
+ * MLP and every expert being GeLU FFNs of the layer's shape (W1 [F][H] + b1,
+ * GeLU, W2 [H][F] + b2) and W_g [E][H] having no bias.  The expert of each
+ * row is chosen on the device (no host synchronisation). */
+typedef struct ds_moe_ffn ds_moe_ffn;
+typedef struct {
+  int hidden;          /* H, a multiple of 256                          */
+  int ffn;             /* F, a multiple of 256 (MLP and experts)        */
+  int experts;         /* E, 1 .. 1024                                  */
+  float ln_eps;        /* LayerNorm epsilon                             */
+  ds_dtype act_dtype;  /* DS_F16 or DS_BF16: activations and weights    */
+} ds_moe_config;
+/* Device pointers (act_dtype): ln2_g/ln2_b [H]; w_gate [E][H]; the dense MLP
+ * w_fc1 [F][H], b_fc1 [F], w_fc2 [H][F], b_fc2 [H]; the experts stacked:
+ * we_fc1 [E][F][H], be_fc1 [E][F], we_fc2 [E][H][F], be_fc2 [E][H].  Stored,
+ * not copied: keep them alive and unchanged until ds_moe_ffn_destroy. */
+typedef struct {
+  const void *ln2_g, *ln2_b, *w_gate, *w_fc1, *b_fc1, *w_fc2, *b_fc2;
+  const void *we_fc1, *be_fc1, *we_fc2, *be_fc2;
+} ds_moe_weights;
+
+DS_API ds_status ds_moe_ffn_create(const ds_moe_config* cfg, const ds_moe_weights* w, ds_moe_ffn** out);
+DS_API ds_status ds_moe_ffn_destroy(ds_moe_ffn* moe);
+/* Workspace bytes for `rows` rows (1 .. 4096); 0 for invalid arguments.  The
+ * workspace is zero-filled once (ds_workspace_init) before first use. */
+DS_API size_t ds_moe_ffn_workspace_bytes(const ds_moe_ffn* moe, int rows);
+/* y = x + MLP(h) + p_e Expert_e(h) for x_in [rows][H] -> x_out [rows][H]
+ * (act_dtype, not aliasing).  expert_out: optional DEVICE int32 [rows]
+ * receiving each row's expert.  Asynchronous on `stream`: 4 + 2 rows kernels
+ * (row LayerNorm, gate, dense MLP up / down, per row the chosen expert's
+ * up / down), the device status flags in the workspace as for a layer. */
+DS_API ds_status ds_moe_ffn_forward(ds_moe_ffn* moe, const void* x_in, void* x_out, int rows,
+                                    int32_t* expert_out, void* workspace, size_t ws_bytes, void* stream);
+
 /* Device-side status flags recorded in the workspace. */
 #define DS_DEVFLAG_CACHE_OVERFLOW 0x1  /* past_len[b] + T > max_len for some row */
 #define DS_DEVFLAG_WAIT_TIMEOUT 0x2    /* an in-kernel pipeline wait gave up (outputs invalid) */

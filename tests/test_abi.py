@@ -111,10 +111,14 @@ def test_null_arguments(lib):
     assert lib.ds_quantize_int8(None, 4, 128, 64, None, None, None) == ds.DS_ERR_INVALID_ARG
     assert lib.ds_stack_set_profiling(None, 1) == ds.DS_ERR_INVALID_ARG
     assert lib.ds_workspace_init(None, 0, None) == ds.DS_ERR_INVALID_ARG
+    assert lib.ds_moe_ffn_create(None, None, None) == ds.DS_ERR_INVALID_ARG
+    assert lib.ds_moe_ffn_workspace_bytes(None, 1) == 0
+    assert lib.ds_moe_ffn_forward(None, None, None, 1, None, None, 0, None) == ds.DS_ERR_INVALID_ARG
+    assert lib.ds_selftest_wait_timeout(None, 10, None) == ds.DS_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs a C compiler")
-@pytest.mark.parametrize("struct", ["ds_layer_config", "ds_layer_weights"])
+@pytest.mark.parametrize("struct", ["ds_layer_config", "ds_layer_weights", "ds_moe_config", "ds_moe_weights"])
 def test_binding_structs_match_the_header(struct, tmp_path):
     """The ctypes mirrors of the header's structs have the C layout: a C program
     compiled against include/ds_layer.h prints each field's offset and the

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 32) {  // the descriptors' first use is the TMA warp's first copy
-    asm volatile("prefetch.tensormap [%0];" ::"l"(a.tmap_w) : "memory");
+    if (a.sel_idx == nullptr) asm volatile("prefetch.tensormap [%0];" ::"l"(a.tmap_w) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap_hi) : "memory");
     if (kSplit) asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap_lo) : "memory");
   }
@@ -221,6 +221,12 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   if (warp == kDenseTmaWarp) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
+      // the weights of an expert chosen by the previous kernels: wait first
+      const void* tmap_w = a.tmap_w;
+      if (a.sel_idx != nullptr) {
+        pdl_wait();
+        tmap_w = a.tmap_table + (size_t)128 * (size_t)(*a.sel_idx);
+      }
       const uint64_t pol_w = l2_evict_first_policy();
       const uint64_t pol_x = l2_evict_normal_policy();
       const uint32_t tx = (uint32_t)(WB + (kSplit ? 2 : 1) * XB);
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
         const int trow = q.t % row_tiles;
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
-        tma_load_3d(stage, a.tmap_w, 0, trow * 128, (q.s * P.C + q.kc) * (KC / 64), full_bar(rp.st), pol_w);
+        tma_load_3d(stage, tmap_w, 0, trow * 128, (q.s * P.C + q.kc) * (KC / 64), full_bar(rp.st), pol_w);
         last_ph[rp.st] = rp.ph;
         issued |= 1u << rp.st;
         ws_cursor_next(q, P, dp_b);
@@ -255,7 +261,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       int fpre = pre;
       auto l2_ahead = [&](int upto) {
         for (; fpre < upto && fpre < nchunks; ++fpre) {
-          tma_prefetch_3d(a.tmap_w, 0, (qp.t % row_tiles) * 128, (qp.s * P.C + qp.kc) * (KC / 64));
+          tma_prefetch_3d(tmap_w, 0, (qp.t % row_tiles) * 128, (qp.s * P.C + qp.kc) * (KC / 64));
           ws_cursor_next(qp, P, dp_b);
         }
       };
@@ -283,7 +289,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         const int trow = q.t % row_tiles, jt = q.t / row_tiles;
         const int kseg = (q.s * P.C + q.kc) * (KC / 64);
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
-        tma_load_3d(stage, a.tmap_w, 0, trow * 128, kseg, full_bar(rp.st), pol_w);
+        tma_load_3d(stage, tmap_w, 0, trow * 128, kseg, full_bar(rp.st), pol_w);
         tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
         if constexpr (kSplit)
           tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
@@ -367,6 +373,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     struct TileCtx {
       int t, n, m0, mrows;
       float bias;
+      float scale;      // expert output weight (residual-MoE), else 1
       ACT* dst;         // R1: the row's KV-cache element of (b, position) 0; R4a / R4b: output column n
       ACT* dst_lo;      // R4a, bf16: operand lo column n
       float* dst_f32;   // R1 (q rows): q column; R3: x1 column n
@@ -378,7 +385,9 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       c.n = (t % row_tiles) * 128 + r;
       c.m0 = (t / row_tiles) * NTOK;
       c.mrows = min(NTOK, M - c.m0);
-      c.bias = Act<ACT>::to_f(static_cast<const ACT*>(a.bias)[c.n]);
+      const int bsel = a.sel_idx != nullptr ? a.sel_bias_stride * (*a.sel_idx) : 0;
+      c.bias = Act<ACT>::to_f(static_cast<const ACT*>(a.bias)[bsel + c.n]);
+      c.scale = a.sel_scale != nullptr ? *a.sel_scale : 1.0f;
       c.dst = nullptr;
       c.dst_lo = nullptr;
       c.dst_f32 = nullptr;
@@ -426,7 +435,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         const int mi = c8 + i;  // column within the tile
         const bool ok = mi < c.mrows;
         const int m = c.m0 + mi;
-        float y = v[i] + c.bias;
+        float y = (v[i] + c.bias) * c.scale;
         if constexpr (R == Region::LnQkv) {
           if (ok) {
             if (!c.to_cache) {

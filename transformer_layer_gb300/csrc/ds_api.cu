@@ -733,6 +733,7 @@ struct ds_stack {
 namespace ds {
 void set_last_error(const char* msg) { g_err = msg; }
 int layer_device(const ds_layer* layer) { return layer->device; }
+void add_launches(unsigned long long n) { g_launches += n; }
 
 // Validates a ds_layer_forward call (nothing is enqueued).  On success
 // *zero_prefix is the number of leading workspace bytes (status word and

@@ -135,6 +135,14 @@ struct DenseArgs {
   int32_t* seq_len_inc = nullptr;  // R4b of a stack step's last layer
   const void* next_tmap_w = nullptr;  // the next tile GEMM (L2 prefetch), or null
   DensePlan next_plan;
+  // Expert selection (residual-MoE FFN): when sel_idx is set, W is expert
+  // *sel_idx -- its tensor map at tmap_table + 128 * idx, its bias at
+  // bias + sel_bias_stride * idx -- read after the dependency wait; when
+  // sel_scale is set, the epilogue takes (acc + bias) * *sel_scale.
+  const unsigned char* tmap_table = nullptr;
+  const int32_t* sel_idx = nullptr;
+  const float* sel_scale = nullptr;
+  int sel_bias_stride = 0;
 };
 
 // Row normalisation ahead of a tile GEMM (regions 1 and 4a): out = LN(x) in
@@ -186,6 +194,7 @@ cudaError_t launch_dense(Region r, ActKind ak, const DenseArgs& a, const void* x
                          cudaStream_t st, bool pdl);
 cudaError_t launch_ln_prep(ActKind ak, const LnPrepArgs& a, cudaStream_t st, bool pdl);
 cudaError_t prepare_dense_kernels(int max_smem);
+cudaError_t prepare_moe_kernels(int max_smem);
 
 int attn_nsplit(int B, int heads, int max_len, int num_sms);
 // Shared memory of the attention kernel, and the cached keys per split it
@@ -219,6 +228,8 @@ ds_status layer_forward_enqueue(ds_layer* layer, const void* x_in, void* x_out, 
 void set_last_error(const char* msg);
 // The device a layer was created on.
 int layer_device(const ds_layer* layer);
+// Adds n to the count ds_launch_count() reports.
+void add_launches(unsigned long long n);
 
 cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned long long budget_ns, cudaStream_t st);
 cudaError_t launch_quantize_int8(const void* w, int n, int k, int group, int8_t* codes, void* scales,

@@ -55,10 +55,14 @@ cudaError_t launch_quantize_int8(const void* w, int n, int k, int group, int8_t*
   if (blocks < 1) blocks = 1;
   const __half* wh = static_cast<const __half*>(w);
   __half* sh = static_cast<__half*>(scales);
-  if (group == 32) quantize_int8_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(wh, n, k, codes, sh);
-  else if (group == 64) quantize_int8_kernel<2><<<(unsigned)blocks, 256, 0, st>>>(wh, n, k, codes, sh);
-  else quantize_int8_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(wh, n, k, codes, sh);
-  return cudaGetLastError();
+  // (cudaLaunchKernelEx returns this launch's own error, not an earlier one)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  if (group == 32) return cudaLaunchKernelEx(&cfg, quantize_int8_kernel<1>, wh, n, k, codes, sh);
+  if (group == 64) return cudaLaunchKernelEx(&cfg, quantize_int8_kernel<2>, wh, n, k, codes, sh);
+  return cudaLaunchKernelEx(&cfg, quantize_int8_kernel<4>, wh, n, k, codes, sh);
 }
 
 // Self-test of the bounded-wait path: one thread waits on an mbarrier that
@@ -76,8 +80,11 @@ __global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(unsigned* sta
 }
 
 cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned long long budget_ns, cudaStream_t st) {
-  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(status, budget_ns);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, wait_timeout_selftest_kernel, status, budget_ns);
 }
 
 }  // namespace ds

@@ -44,6 +44,10 @@ _SIGS = {
     "ds_stack_graph_captures": (C.c_uint64, [_vp]),
     "ds_quantize_int8": (C.c_int, [_vp, C.c_int, C.c_int, C.c_int, _vp, _vp, _vp]),
     "ds_workspace_status": (C.c_int, [_vp, C.POINTER(C.c_uint32), _vp]),
+    "ds_moe_ffn_create": (C.c_int, [_vp, _vp, C.POINTER(_vp)]),
+    "ds_moe_ffn_destroy": (C.c_int, [_vp]),
+    "ds_moe_ffn_workspace_bytes": (C.c_size_t, [_vp, C.c_int]),
+    "ds_moe_ffn_forward": (C.c_int, [_vp, _vp, _vp, C.c_int, _vp, _vp, C.c_size_t, _vp]),
     "ds_selftest_wait_timeout": (C.c_int, [_vp, C.c_uint32, _vp]),
     "ds_launch_count": (C.c_uint64, []),
     "ds_status_string": (C.c_char_p, [C.c_int]),
@@ -64,6 +68,19 @@ _WNAMES = ("ln1_g", "ln1_b", "w_qkv", "b_qkv", "w_o", "b_o", "ln2_g", "ln2_b", "
 
 class ds_layer_weights(C.Structure):
     _fields_ = [(n, _vp) for n in _WNAMES]
+
+
+class ds_moe_config(C.Structure):
+    _fields_ = [("hidden", C.c_int), ("ffn", C.c_int), ("experts", C.c_int), ("ln_eps", C.c_float),
+                ("act_dtype", C.c_int)]
+
+
+_MOE_WNAMES = ("ln2_g", "ln2_b", "w_gate", "w_fc1", "b_fc1", "w_fc2", "b_fc2", "we_fc1", "be_fc1", "we_fc2",
+               "be_fc2")
+
+
+class ds_moe_weights(C.Structure):
+    _fields_ = [(n, _vp) for n in _MOE_WNAMES]
 
 
 class DSError(RuntimeError):
@@ -241,6 +258,28 @@ def ds_workspace_status(ws, stream=None):
 
 def ds_selftest_wait_timeout(ws, budget_us, stream=None):
     _check(load().ds_selftest_wait_timeout(_ptr(ws), budget_us, _stream(stream)), "ds_selftest_wait_timeout")
+
+
+def ds_moe_ffn_create(hidden, ffn, experts, weights: dict, act_dtype, ln_eps=1e-5):
+    """weights: dict of device tensors keyed like ds_moe_weights' fields."""
+    cfg = ds_moe_config(hidden, ffn, experts, ln_eps, _dtype_code(act_dtype))
+    w = ds_moe_weights(*[_ptr(weights.get(n)) for n in _MOE_WNAMES])
+    out = C.c_void_p()
+    _check(load().ds_moe_ffn_create(C.byref(cfg), C.byref(w), C.byref(out)), "ds_moe_ffn_create")
+    return out
+
+
+def ds_moe_ffn_destroy(moe):
+    _check(load().ds_moe_ffn_destroy(moe), "ds_moe_ffn_destroy")
+
+
+def ds_moe_ffn_workspace_bytes(moe, rows):
+    return int(load().ds_moe_ffn_workspace_bytes(moe, rows))
+
+
+def ds_moe_ffn_forward(moe, x_in, x_out, rows, expert_out, ws, ws_bytes, stream=None):
+    _check(load().ds_moe_ffn_forward(moe, _ptr(x_in), _ptr(x_out), rows, _ptr(expert_out), _ptr(ws), ws_bytes,
+                                     _stream(stream)), "ds_moe_ffn_forward")
 
 
 def ds_launch_count():
