@@ -297,6 +297,97 @@ DS_API size_t ds_moe_ffn_workspace_bytes(const ds_moe_ffn* moe, int rows);
 DS_API ds_status ds_moe_ffn_forward(ds_moe_ffn* moe, const void* x_in, void* x_out, int rows,
                                     int32_t* expert_out, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Tensor-sliced (Megatron-style) layer.  [P1] §3.2: the Attn and FF blocks
+ * of a layer are split across GPUs in the Megatron-LM manner, so each block
+ * ends in one cross-GPU all-reduce; §3.1, second fusion principle: every
+ * all-reduce is a fusion boundary; the page's injection-policy passage: the
+ * attention output GEMM and the layer output GEMM are the two linear layers
+ * whose partial results are reduced across ranks.  The page gives no
+ * formula; the split implemented, for W ranks (Hl = H/W, Fl = F/W, rank r):
+ *   - rank r owns heads r*nh/W .. (r+1)*nh/W-1: their q, k and v rows of
+ *     W_qkv / b_qkv, their KV caches, and columns r*Hl .. (r+1)*Hl-1 of W_o;
+ *   - rank r owns FFN features r*Fl .. (r+1)*Fl-1: those rows of W_1 / b_1
+ *     and those columns of W_2;
+ *   - LayerNorm parameters are replicated; b_o, b_fc2 and the residuals are
+ *     added by rank 0 only, inside its partial sums.
+ * One layer step, on every rank, around two all-reduces (sum, fp32) that
+ * the caller performs with its collective library (NCCL, torch.distributed):
+ *   ds_tp_attention_partial   x1_r = [r==0](x + b_o) + o_r W_o[:, cols_r]^T
+ *                             (LayerNorm1 + QKV of the rank's heads + KV
+ *                             append + attention + O-proj, 4 kernels)
+ *   all-reduce                x1 = sum over ranks of x1_r
+ *   ds_tp_ffn_partial         y_r = [r==0](x1 + b_fc2)
+ *                                   + GeLU(LN2(x1) W_1[rows_r]^T + b_1[rows_r]) W_2[:, rows_r]^T
+ *                             (LayerNorm2 + FFN-up + GeLU + FFN-down, 3 kernels)
+ *   all-reduce                y = sum over ranks of y_r
+ *   ds_tp_finish              x_out = y in the activation dtype (1 kernel)
+ * The partial sums are written by the epilogues of the two reduced GEMMs
+ * (the reduction boundary), in fp32, so the all-reduce is the only step
+ * between the fused regions.  fp16 / bf16 weights only (the tensor-core tile
+ * kernels run every GEMM, at any row count 1..4096).  No device-to-device
+ * traffic happens inside the library. */
+typedef struct ds_tp_layer ds_tp_layer;
+typedef struct {
+  ds_layer_config layer; /* the FULL layer: hidden H, heads nh, ffn F, ln_eps,
+                          * act_dtype; weight_dtype == act_dtype (fp16 / bf16) */
+  int tp_size;           /* W, 1 .. 64, dividing nh; H/W and F/W multiples of 128 */
+  int tp_rank;           /* r, 0 .. W-1 */
+} ds_tp_config;
+
+/* Where a rank's weights come from in the full layer: block i copies rows
+ * src_row .. src_row+rows-1, columns src_col .. src_col+cols-1 of the full
+ * matrix (row pitch src_cols elements) to rows dst_row .. dst_row+rows-1 of
+ * the rank's matrix (row pitch cols elements).  Vectors are one-column
+ * matrices.  Matrices not listed (LayerNorm parameters, b_o, b_fc2) are
+ * replicated. */
+typedef enum { DS_TP_W_QKV = 0, DS_TP_B_QKV = 1, DS_TP_W_O = 2, DS_TP_W_FC1 = 3,
+               DS_TP_B_FC1 = 4, DS_TP_W_FC2 = 5 } ds_tp_matrix;
+typedef struct {
+  int matrix;    /* ds_tp_matrix */
+  int src_row, src_col, rows, cols, src_cols, dst_row;
+} ds_tp_block;
+
+/* HOST only, no device needed: writes the rank's blocks (10: three each for
+ * w_qkv and b_qkv, one for each other sliced matrix) to out[0 .. cap-1] and
+ * returns their number, or -1 for an invalid config (ds_last_error says why)
+ * or cap < 10. */
+DS_API int ds_tp_shard_blocks(const ds_tp_config* cfg, ds_tp_block* out, int cap);
+/* Copies the rank's slices of the FULL layer weights `full` (host or device
+ * memory, [out][in] as for ds_layer_create) into the caller's buffers
+ * `shard` (device memory, shapes: w_qkv [3Hl][H], b_qkv [3Hl], w_o [H][Hl],
+ * w_fc1 [Fl][H], b_fc1 [Fl], w_fc2 [H][Fl]; only these six fields are
+ * written, the others are ignored).  Asynchronous on `stream`
+ * (cudaMemcpy2DAsync per block); the full weights must stay valid until the
+ * stream reaches this point. */
+DS_API ds_status ds_tp_shard_weights(const ds_tp_config* cfg, const ds_layer_weights* full,
+                                     const ds_layer_weights* shard, void* stream);
+/* The rank's layer over its shard: `w` holds the rank's device matrices in
+ * the shapes above, and the replicated ln1_g, ln1_b, b_o, ln2_g, ln2_b,
+ * b_fc2 [H] (b_o and b_fc2 are read on rank 0 only); s_* are ignored.
+ * Stored, not copied. */
+DS_API ds_status ds_tp_layer_create(const ds_tp_config* cfg, const ds_layer_weights* w, ds_tp_layer** out);
+DS_API ds_status ds_tp_layer_destroy(ds_tp_layer* layer);
+/* Workspace bytes for batch x new_tokens rows (1 .. 4096 rows); 0 for
+ * invalid arguments.  Zero-filled once (ds_workspace_init) before first use;
+ * one workspace serves the three calls of a step. */
+DS_API size_t ds_tp_layer_workspace_bytes(const ds_tp_layer* layer, int batch, int new_tokens);
+/* x_in [B][T][H] act dtype -> x1_part [B*T][H] fp32 (this rank's share of
+ * x1).  k_cache / v_cache: the rank's caches [B][nh/W][max_len][d]; the new
+ * keys and values are written at past_len[b] .. past_len[b]+T-1 as for
+ * ds_layer_forward (past_len is not advanced). */
+DS_API ds_status ds_tp_attention_partial(ds_tp_layer* layer, const void* x_in, float* x1_part, int batch,
+                                         int new_tokens, void* k_cache, void* v_cache, int max_len,
+                                         const int32_t* past_len, void* workspace, size_t ws_bytes,
+                                         void* stream);
+/* x1 [rows][H] fp32 (the all-reduced x1) -> y_part [rows][H] fp32 (this
+ * rank's share of the layer output).  x1 and y_part must not alias. */
+DS_API ds_status ds_tp_ffn_partial(ds_tp_layer* layer, const float* x1, float* y_part, int rows,
+                                   void* workspace, size_t ws_bytes, void* stream);
+/* y [rows][H] fp32 (the all-reduced layer output) -> x_out [rows][H] in the
+ * activation dtype (round to nearest even). */
+DS_API ds_status ds_tp_finish(ds_tp_layer* layer, const float* y, void* x_out, int rows, void* stream);
+
 /* Device-side status flags recorded in the workspace. */
 #define DS_DEVFLAG_CACHE_OVERFLOW 0x1  /* past_len[b] + T > max_len for some row */
 #define DS_DEVFLAG_WAIT_TIMEOUT 0x2    /* an in-kernel pipeline wait gave up (outputs invalid) */

@@ -18,14 +18,18 @@ layer   LayerNorm, linear, GeLU(tanh), softmax, KV-cache decode attention and
         the whole layer / stack forward.
 quant   MoQ-style symmetric per-group int8 quantisation and dequantisation.
 moe     the residual-MoE (PR-MoE) FFN block with top-1 routing.
+tp      the tensor-sliced (Megatron-style) layer: shards, per-rank partial
+        sums and their reduction.
 """
 from .layer import (layer_norm, linear, gelu_tanh, softmax, decode_attention,
                     layer_forward, stack_forward, LAYER_PARAM_NAMES)
 from .quant import quantize_int8, dequantize_int8, fp16_scale_from_amax
 from .moe import ffn, residual_moe_ffn
+from .tp import shard_layer_params, tp_attention_partial, tp_ffn_partial, tp_layer_forward
 
 __all__ = [
     "layer_norm", "linear", "gelu_tanh", "softmax", "decode_attention",
     "layer_forward", "stack_forward", "LAYER_PARAM_NAMES",
     "quantize_int8", "dequantize_int8", "fp16_scale_from_amax", "ffn", "residual_moe_ffn",
+    "shard_layer_params", "tp_attention_partial", "tp_ffn_partial", "tp_layer_forward",
 ]

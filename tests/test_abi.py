@@ -115,10 +115,25 @@ def test_null_arguments(lib):
     assert lib.ds_moe_ffn_workspace_bytes(None, 1) == 0
     assert lib.ds_moe_ffn_forward(None, None, None, 1, None, None, 0, None) == ds.DS_ERR_INVALID_ARG
     assert lib.ds_selftest_wait_timeout(None, 10, None) == ds.DS_ERR_INVALID_ARG
+    assert lib.ds_tp_layer_create(None, None, None) == ds.DS_ERR_INVALID_ARG
+    assert lib.ds_tp_layer_workspace_bytes(None, 1, 1) == 0
+    assert lib.ds_tp_attention_partial(None, None, None, 1, 1, None, None, 1, None, None, 0, None) == \
+        ds.DS_ERR_INVALID_ARG
+    assert lib.ds_tp_ffn_partial(None, None, None, 1, None, 0, None) == ds.DS_ERR_INVALID_ARG
+    assert lib.ds_tp_finish(None, None, None, 1, None) == ds.DS_ERR_INVALID_ARG
+    assert lib.ds_tp_shard_weights(None, None, None, None) == ds.DS_ERR_INVALID_ARG
+    assert lib.ds_tp_shard_blocks(None, None, 0) == -1
+    # an invalid split is refused before any device call
+    bad = ds.ds_tp_config(ds.ds_layer_config(1024, 8, 4096, 1e-5, ds.DS_F16, ds.DS_F16, 64, 0), 3, 0)
+    out = C.c_void_p()
+    assert lib.ds_tp_layer_create(C.byref(bad), C.byref(ds.ds_layer_weights()), C.byref(out)) == \
+        ds.DS_ERR_INVALID_ARG
+    assert "divide heads" in lib.ds_last_error().decode()
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs a C compiler")
-@pytest.mark.parametrize("struct", ["ds_layer_config", "ds_layer_weights", "ds_moe_config", "ds_moe_weights"])
+@pytest.mark.parametrize("struct", ["ds_layer_config", "ds_layer_weights", "ds_moe_config", "ds_moe_weights",
+                                    "ds_tp_config", "ds_tp_block"])
 def test_binding_structs_match_the_header(struct, tmp_path):
     """The ctypes mirrors of the header's structs have the C layout: a C program
     compiled against include/ds_layer.h prints each field's offset and the

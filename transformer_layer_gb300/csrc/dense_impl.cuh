@@ -386,7 +386,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       c.m0 = (t / row_tiles) * NTOK;
       c.mrows = min(NTOK, M - c.m0);
       const int bsel = a.sel_idx != nullptr ? a.sel_bias_stride * (*a.sel_idx) : 0;
-      c.bias = Act<ACT>::to_f(static_cast<const ACT*>(a.bias)[bsel + c.n]);
+      c.bias = a.bias != nullptr ? Act<ACT>::to_f(static_cast<const ACT*>(a.bias)[bsel + c.n]) : 0.f;
       c.scale = a.sel_scale != nullptr ? *a.sel_scale : 1.0f;
       c.dst = nullptr;
       c.dst_lo = nullptr;
@@ -403,6 +403,8 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         }
       } else if constexpr (R == Region::OprojRes) {
         c.dst_f32 = a.out_f32 + c.n;
+      } else if (R == Region::FfnDown && a.out_f32 != nullptr) {
+        c.dst_f32 = a.out_f32 + c.n;  // a tensor-sliced rank's partial sum (fp32)
       } else {
         c.dst = static_cast<ACT*>(a.out_act) + c.n;
         if constexpr (R == Region::FfnUp && kSplit) c.dst_lo = static_cast<ACT*>(a.out_lo) + c.n;
@@ -420,9 +422,9 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           const int b = a.T == 1 ? m : m / a.T;
           o[i] = __int_as_float(a.past_len[b] + (m - b * a.T));
         } else if constexpr (R == Region::OprojRes) {
-          o[i] = Act<ACT>::to_f(static_cast<const ACT*>(a.resid_act)[(size_t)m * N + c.n]);
+          o[i] = a.resid_act != nullptr ? Act<ACT>::to_f(static_cast<const ACT*>(a.resid_act)[(size_t)m * N + c.n]) : 0.f;
         } else if constexpr (R == Region::FfnDown) {
-          o[i] = a.resid_f32[(size_t)m * N + c.n];
+          o[i] = a.resid_f32 != nullptr ? a.resid_f32[(size_t)m * N + c.n] : 0.f;
         } else {
           o[i] = 0.f;
         }
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           }
         } else {
           y += op[i];
-          if constexpr (R == Region::OprojRes) {
+          if (R == Region::OprojRes || c.dst_f32 != nullptr) {
             if (ok) c.dst_f32[(size_t)m * N] = y;
           } else {
             const ACT h = Act<ACT>::from_f(y);
@@ -645,7 +647,9 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           uint32_t ops_sm = 0;
           if constexpr (R == Region::OprojRes || R == Region::FfnDown) {
             const uint32_t off = (uint32_t)(dst0 + nr) * slot_stride;
-            if (js + nr == contrib && (size_t)off + (size_t)c.mrows * kResidRowBytes <= (size_t)S * SB) ops_sm = st + off;
+            const bool has_resid = R == Region::OprojRes ? a.resid_act != nullptr : a.resid_f32 != nullptr;
+            if (has_resid && js + nr == contrib && (size_t)off + (size_t)c.mrows * kResidRowBytes <= (size_t)S * SB)
+              ops_sm = st + off;
           }
           if (et < 32) {  // the first epilogue warp issues the copies
             // this thread's acquire (the arrival counter) orders the other

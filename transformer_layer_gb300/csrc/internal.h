@@ -119,13 +119,13 @@ struct DenseArgs {
   DensePlan plan;
   float* partials = nullptr;       // [tiles - U_dp][maxc][ntok][128] partial sums of the leftover tiles
   int* counters = nullptr;         // [tiles] arrival counters (self-resetting)
-  const void* bias = nullptr;      // [N] act dtype
+  const void* bias = nullptr;      // [N] act dtype, or null (no bias: a tensor-sliced rank other than 0)
   // epilogue
-  float* out_f32 = nullptr;        // R1: q [M][H]; R3: x1
+  float* out_f32 = nullptr;        // R1: q [M][H]; R3: x1; R4b: a tensor-sliced rank's partial sum (else null)
   void* out_act = nullptr;         // R4a: GeLU output (operand hi); R4b: layer output
   void* out_lo = nullptr;          // R4a, bf16: operand lo
-  const void* resid_act = nullptr; // R3: layer input
-  const float* resid_f32 = nullptr;// R4b: x1
+  const void* resid_act = nullptr; // R3: layer input, or null (no residual)
+  const float* resid_f32 = nullptr;// R4b: x1, or null (no residual)
   float* stats_out = nullptr;      // R3 / R4b: [N/16][M][2] (sum, M2) partials, or null
   void* k_cache = nullptr;         // R1 cache append
   void* v_cache = nullptr;

@@ -49,6 +49,15 @@ _SIGS = {
     "ds_moe_ffn_workspace_bytes": (C.c_size_t, [_vp, C.c_int]),
     "ds_moe_ffn_forward": (C.c_int, [_vp, _vp, _vp, C.c_int, _vp, _vp, C.c_size_t, _vp]),
     "ds_selftest_wait_timeout": (C.c_int, [_vp, C.c_uint32, _vp]),
+    "ds_tp_shard_blocks": (C.c_int, [_vp, _vp, C.c_int]),
+    "ds_tp_shard_weights": (C.c_int, [_vp, _vp, _vp, _vp]),
+    "ds_tp_layer_create": (C.c_int, [_vp, _vp, C.POINTER(_vp)]),
+    "ds_tp_layer_destroy": (C.c_int, [_vp]),
+    "ds_tp_layer_workspace_bytes": (C.c_size_t, [_vp, C.c_int, C.c_int]),
+    "ds_tp_attention_partial": (C.c_int, [_vp, _vp, _vp, C.c_int, C.c_int, _vp, _vp, C.c_int, _vp, _vp,
+                                          C.c_size_t, _vp]),
+    "ds_tp_ffn_partial": (C.c_int, [_vp, _vp, _vp, C.c_int, _vp, C.c_size_t, _vp]),
+    "ds_tp_finish": (C.c_int, [_vp, _vp, _vp, C.c_int, _vp]),
     "ds_launch_count": (C.c_uint64, []),
     "ds_status_string": (C.c_char_p, [C.c_int]),
     "ds_last_error": (C.c_char_p, []),
@@ -81,6 +90,18 @@ _MOE_WNAMES = ("ln2_g", "ln2_b", "w_gate", "w_fc1", "b_fc1", "w_fc2", "b_fc2", "
 
 class ds_moe_weights(C.Structure):
     _fields_ = [(n, _vp) for n in _MOE_WNAMES]
+
+
+class ds_tp_config(C.Structure):
+    _fields_ = [("layer", ds_layer_config), ("tp_size", C.c_int), ("tp_rank", C.c_int)]
+
+
+DS_TP_W_QKV, DS_TP_B_QKV, DS_TP_W_O, DS_TP_W_FC1, DS_TP_B_FC1, DS_TP_W_FC2 = range(6)
+TP_MATRIX_NAMES = ("w_qkv", "b_qkv", "w_o", "w_fc1", "b_fc1", "w_fc2")
+
+
+class ds_tp_block(C.Structure):
+    _fields_ = [(n, C.c_int) for n in ("matrix", "src_row", "src_col", "rows", "cols", "src_cols", "dst_row")]
 
 
 class DSError(RuntimeError):
@@ -280,6 +301,84 @@ def ds_moe_ffn_workspace_bytes(moe, rows):
 def ds_moe_ffn_forward(moe, x_in, x_out, rows, expert_out, ws, ws_bytes, stream=None):
     _check(load().ds_moe_ffn_forward(moe, _ptr(x_in), _ptr(x_out), rows, _ptr(expert_out), _ptr(ws), ws_bytes,
                                      _stream(stream)), "ds_moe_ffn_forward")
+
+
+def _tp_config(hidden, heads, ffn, act_dtype, tp_size, tp_rank, ln_eps=1e-5):
+    code = _dtype_code(act_dtype)
+    return ds_tp_config(ds_layer_config(hidden, heads, ffn, ln_eps, code, code, 64, 0), tp_size, tp_rank)
+
+
+def ds_tp_shard_blocks(hidden, heads, ffn, act_dtype, tp_size, tp_rank, ln_eps=1e-5):
+    """The rank's blocks of the full matrices, as dicts of ds_tp_block's fields
+    (host-only call: no device is needed)."""
+    cfg = _tp_config(hidden, heads, ffn, act_dtype, tp_size, tp_rank, ln_eps)
+    out = (ds_tp_block * 16)()
+    n = load().ds_tp_shard_blocks(C.byref(cfg), out, 16)
+    if n < 0:
+        raise DSError(DS_ERR_INVALID_ARG, "ds_tp_shard_blocks")
+    return [{f: getattr(out[i], f) for f, _ in ds_tp_block._fields_} for i in range(n)]
+
+
+def ds_tp_shard_weights(hidden, heads, ffn, act_dtype, tp_size, tp_rank, full: dict, shard: dict, stream=None):
+    """Copies the rank's slices of `full` into the buffers of `shard` (dicts
+    keyed like ds_layer_weights' fields)."""
+    cfg = _tp_config(hidden, heads, ffn, act_dtype, tp_size, tp_rank)
+    wf = ds_layer_weights(*[_ptr(full.get(n)) for n in _WNAMES])
+    ws = ds_layer_weights(*[_ptr(shard.get(n)) for n in _WNAMES])
+    _check(load().ds_tp_shard_weights(C.byref(cfg), C.byref(wf), C.byref(ws), _stream(stream)),
+           "ds_tp_shard_weights")
+
+
+def ds_tp_layer_create(hidden, heads, ffn, weights: dict, act_dtype, tp_size, tp_rank, ln_eps=1e-5):
+    """weights: the rank's device tensors keyed like ds_layer_weights' fields."""
+    cfg = _tp_config(hidden, heads, ffn, act_dtype, tp_size, tp_rank, ln_eps)
+    w = ds_layer_weights(*[_ptr(weights.get(n)) for n in _WNAMES])
+    out = C.c_void_p()
+    _check(load().ds_tp_layer_create(C.byref(cfg), C.byref(w), C.byref(out)), "ds_tp_layer_create")
+    return out
+
+
+def ds_tp_layer_destroy(layer):
+    _check(load().ds_tp_layer_destroy(layer), "ds_tp_layer_destroy")
+
+
+def ds_tp_layer_workspace_bytes(layer, batch, new_tokens):
+    return int(load().ds_tp_layer_workspace_bytes(layer, batch, new_tokens))
+
+
+def ds_tp_attention_partial(layer, x_in, x1_part, batch, new_tokens, k_cache, v_cache, max_len, past_len, ws,
+                            ws_bytes, stream=None):
+    _check(load().ds_tp_attention_partial(layer, _ptr(x_in), _ptr(x1_part), batch, new_tokens, _ptr(k_cache),
+                                          _ptr(v_cache), max_len, _ptr(past_len), _ptr(ws), ws_bytes,
+                                          _stream(stream)), "ds_tp_attention_partial")
+
+
+def ds_tp_ffn_partial(layer, x1, y_part, rows, ws, ws_bytes, stream=None):
+    _check(load().ds_tp_ffn_partial(layer, _ptr(x1), _ptr(y_part), rows, _ptr(ws), ws_bytes, _stream(stream)),
+           "ds_tp_ffn_partial")
+
+
+def ds_tp_finish(layer, y, x_out, rows, stream=None):
+    _check(load().ds_tp_finish(layer, _ptr(y), _ptr(x_out), rows, _stream(stream)), "ds_tp_finish")
+
+
+def tp_layer_forward(layer, x_in, x_out, batch, new_tokens, k_cache, v_cache, max_len, past_len, ws, ws_bytes,
+                     x1, y, group=None, stream=None):
+    """One tensor-sliced layer step of this rank: the three library calls with
+    a sum all-reduce of the fp32 buffers x1 and y [rows][H] (caller-owned
+    device tensors) between them, over torch.distributed's `group` (NCCL on
+    GPUs).  The collective runs on torch's current stream, so `stream` must be
+    that stream (or None)."""
+    import torch
+    import torch.distributed as dist
+    if stream is not None and stream != torch.cuda.current_stream():
+        raise ValueError("tp_layer_forward runs on torch's current stream")
+    rows = batch * new_tokens
+    ds_tp_attention_partial(layer, x_in, x1, batch, new_tokens, k_cache, v_cache, max_len, past_len, ws, ws_bytes)
+    dist.all_reduce(x1, op=dist.ReduceOp.SUM, group=group)
+    ds_tp_ffn_partial(layer, x1, y, rows, ws, ws_bytes)
+    dist.all_reduce(y, op=dist.ReduceOp.SUM, group=group)
+    ds_tp_finish(layer, y, x_out, rows)
 
 
 def ds_launch_count():
