@@ -16,7 +16,10 @@
 //
 // GB300 design (not the pages'): a layer has only nh (20-40) heads at batch
 // 1, far fewer than 152 SMs, so each (b, h) is split along the keys over a
-// thread-block cluster of `nsplit` (<= 8) CTAs.  Before griddepcontrol.wait a
+// thread-block cluster of `nsplit` (<= 8) CTAs, as many as keep the grid
+// within one CTA per SM; such a grid asks for more than half of an SM's
+// shared memory, so that no two CTAs share an SM (the block scheduler would
+// otherwise pack them onto a fraction of the SMs).  Before griddepcontrol.wait a
 // CTA copies the cached K and V rows of its keys that the previous kernel
 // does not write (positions < past_len) into shared memory with two TMA bulk
 // copies, so that once the QKV kernel completes only q and the new rows come
@@ -34,7 +37,7 @@
 
 namespace ds {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
 constexpr int kAttnMaxSplit = 8;  // portable cluster size
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -59,6 +62,71 @@ __host__ __device__ inline size_t attn_floats(int D) {
   return (size_t)kpi * D + 2 * kpi + (size_t)(1 + kAttnMaxSplit) * (D + 2);
 }
 __host__ __device__ inline size_t attn_stage_offset(int D) { return (attn_floats(D) * 4 + 127) & ~(size_t)127; }
+
+// Keys [j0, j1) of this CTA (relative to its first key), NBX per key group
+// and pass, folded into the group's running max m, sum l and p.V o8 (log2
+// domain).  Rows j < n_sm come from shared memory (Ks, Vs), the others from
+// global memory (Kg, Vg).
+template <typename ACT, int D, int NBX>
+__device__ __forceinline__ void attn_keys(int j0, int j1, int kr, int kq, int n_sm, const ACT* Ks, const ACT* Vs,
+                                          const ACT* Kg, const ACT* Vg, const float (&qv)[8], float& m, float& l,
+                                          float (&o8)[8]) {
+  constexpr int LPK = D / 8;
+  constexpr int KPI = kAttnThreads / LPK;
+  for (int base = j0; base < j1; base += NBX * KPI) {
+    uint4 kk[NBX], vv[NBX];
+#pragma unroll
+    for (int i = 0; i < NBX; ++i) {
+      const int j = base + i * KPI + kr;
+      if (j < j1) {
+        if (j < n_sm) {
+          kk[i] = lds_u128(smem_u32(Ks + (size_t)j * D + kq * 8));
+          vv[i] = lds_u128(smem_u32(Vs + (size_t)j * D + kq * 8));
+        } else {
+          kk[i] = *reinterpret_cast<const uint4*>(Kg + (size_t)j * D + kq * 8);
+          vv[i] = *reinterpret_cast<const uint4*>(Vg + (size_t)j * D + kq * 8);
+        }
+      } else {
+        kk[i] = make_uint4(0u, 0u, 0u, 0u);
+        vv[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float s[NBX];
+    float bm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NBX; ++i) {
+      const uint32_t kw[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
+      float d = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float2 f = Act<ACT>::unpack2(kw[w]);
+        d += f.x * qv[2 * w] + f.y * qv[2 * w + 1];
+      }
+#pragma unroll
+      for (int o = LPK / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      s[i] = (base + i * KPI + kr < j1) ? d : -INFINITY;
+      bm = fmaxf(bm, s[i]);
+    }
+    const float m_new = fmaxf(m, bm);
+    const float scale = (m_new == -INFINITY) ? 1.f : exp2f(m - m_new);
+    l *= scale;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o8[i] *= scale;
+#pragma unroll
+    for (int i = 0; i < NBX; ++i) {
+      const float p = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_new);
+      l += p;
+      const uint32_t vw[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float2 f = Act<ACT>::unpack2(vw[w]);
+        o8[2 * w] += p * f.x;
+        o8[2 * w + 1] += p * f.y;
+      }
+    }
+    m = m_new;
+  }
+}
 
 template <typename ACT, int D>
 __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs a) {
@@ -137,57 +205,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
     }
     float m = -INFINITY, l = 0.f;
     float o8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int base = 0; base < n_keys; base += NB * KPI) {
-      uint4 kk[NB], vv[NB];
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        const int j = base + i * KPI + kr;
-        if (j < n_keys) {
-          // staged rows from shared memory, the rest (new rows) from global
-          const ACT* kp = (j < n_sm) ? Ks + (size_t)j * D : Kc + (size_t)(lo + j) * D;
-          const ACT* vp = (j < n_sm) ? Vs + (size_t)j * D : Vc + (size_t)(lo + j) * D;
-          kk[i] = *reinterpret_cast<const uint4*>(kp + kq * 8);
-          vv[i] = *reinterpret_cast<const uint4*>(vp + kq * 8);
-        } else {
-          kk[i] = make_uint4(0u, 0u, 0u, 0u);
-          vv[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      float s[NB];
-      float bm = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        const uint32_t kw[4] = {kk[i].x, kk[i].y, kk[i].z, kk[i].w};
-        float d = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float2 f = Act<ACT>::unpack2(kw[w]);
-          d += f.x * qv[2 * w] + f.y * qv[2 * w + 1];
-        }
-#pragma unroll
-        for (int o = LPK / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        s[i] = (base + i * KPI + kr < n_keys) ? d : -INFINITY;
-        bm = fmaxf(bm, s[i]);
-      }
-      const float m_new = fmaxf(m, bm);
-      const float scale = (m_new == -INFINITY) ? 1.f : exp2f(m - m_new);
-      l *= scale;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o8[i] *= scale;
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        const float p = (s[i] == -INFINITY) ? 0.f : exp2f(s[i] - m_new);
-        l += p;
-        const uint32_t vw[4] = {vv[i].x, vv[i].y, vv[i].z, vv[i].w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float2 f = Act<ACT>::unpack2(vw[w]);
-          o8[2 * w] += p * f.x;
-          o8[2 * w + 1] += p * f.y;
-        }
-      }
-      m = m_new;
-    }
+    // whole passes of NB keys per group, then the remainder two at a time
+    const int n_full = n_keys - n_keys % (NB * KPI);
+    attn_keys<ACT, D, NB>(0, n_full, kr, kq, n_sm, Ks, Vs, Kc + (size_t)lo * D, Vc + (size_t)lo * D, qv, m, l, o8);
+    attn_keys<ACT, D, 2>(n_full, n_keys, kr, kq, n_sm, Ks, Vs, Kc + (size_t)lo * D, Vc + (size_t)lo * D, qv, m, l, o8);
     // Merge the key groups of this CTA, then push (O, M, L) to rank 0.
 #pragma unroll
     for (int i = 0; i < 8; ++i) og[kr * D + kq * 8 + i] = o8[i];
@@ -242,24 +263,38 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
   if (!staged) mbar_wait(smem_u32(bar), 0, a.status);  // no copy may land after the CTA exits
 }
 
-int attn_nsplit(int B, int heads, int max_len, int num_sms) {
-  const int bh = B * heads;
-  int ns = (2 * num_sms + bh - 1) / bh;
-  if (ns < 1) ns = 1;
-  if (ns > kAttnMaxSplit) ns = kAttnMaxSplit;
-  const int cap = (max_len + 15) / 16;  // at least ~16 keys per split
-  if (ns > cap) ns = cap < 1 ? 1 : cap;
-  return ns;
-}
-
-int attn_stage_keys(int head_dim, int max_len, int nsplit) {
-  const int per_split = (max_len + nsplit - 1) / nsplit;
-  const int budget = (48 * 1024) / (2 * head_dim * 2);  // K and V rows of 16-bit values
-  return per_split < budget ? per_split : budget;
-}
-
 size_t attn_smem_bytes(int head_dim, int stage_keys) {
   return attn_stage_offset(head_dim) + (size_t)2 * stage_keys * head_dim * 2 + 16;
+}
+
+// Launch shape of the decode attention for a.B, a.heads, a.max_len and
+// a.head_dim: nsplit CTAs (one cluster) per (b, h), as many as keep the
+// grid within one CTA per SM (at most 8, at least ~32 keys each); such a
+// grid stages up to all of a split's keys and asks for more than half of an
+// SM's shared memory so that the CTAs spread over the SMs.  Larger grids
+// (many sequences) take one CTA per (b, h) and a 48 KB staging budget, and
+// several share an SM.
+void attn_configure(AttnArgs& a, int num_sms, int max_smem) {
+  const int bh = a.B * a.heads, D = a.head_dim;
+  int ns = num_sms / (bh > 0 ? bh : 1);
+  if (ns > kAttnMaxSplit) ns = kAttnMaxSplit;
+  const int cap = a.max_len / 32;
+  if (ns > cap) ns = cap;
+  if (ns < 1) ns = 1;
+  const bool spread = (long long)bh * ns <= num_sms;
+  const int per_split = (a.max_len + ns - 1) / ns;
+  const size_t fixed = attn_smem_bytes(D, 0);
+  const size_t budget = spread ? ((size_t)max_smem > fixed + 1024 ? (size_t)max_smem - fixed - 1024 : 0) : 48 * 1024;
+  int sk = (int)(budget / ((size_t)4 * D));  // K and V rows of 16-bit values
+  if (sk > per_split) sk = per_split;
+  size_t smem = attn_smem_bytes(D, sk);
+  if (spread) {
+    const size_t half = (size_t)max_smem / 2 + 1024;
+    if (smem < half && half <= (size_t)max_smem) smem = half;
+  }
+  a.nsplit = ns;
+  a.stage_keys = sk;
+  a.smem = smem;
 }
 
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl) {

@@ -375,10 +375,8 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   ra.head_dim = d;
   ra.max_len = max_len;
   ra.H = H;
-  ra.nsplit = attn_nsplit(B, nh, max_len, L.sms);
   ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  ra.stage_keys = attn_stage_keys(d, max_len, ra.nsplit);
-  ra.smem = attn_smem_bytes(d, ra.stage_keys);
+  attn_configure(ra, L.sms, L.max_smem);
   ra.status = bf.status;
   // prompt chunks: tiled flash attention; decode and short chunks: split-KV
   auto launch_attn = [&](const AttnArgs& x) {
@@ -649,7 +647,7 @@ ds_status check_device(const ds_layer& L) {
 
 ds_status check_attn_smem(const ds_layer& L) {
   const int d = L.cfg.hidden / L.cfg.heads;
-  if (attn_smem_bytes(d, attn_stage_keys(d, 1 << 30, 1)) > (size_t)L.max_smem ||
+  if (attn_smem_bytes(d, 0) + 1024 > (size_t)L.max_smem ||
       attn_prefill_smem_bytes(akind(L.cfg.act_dtype), d) > (size_t)L.max_smem)
     return fail(DS_ERR_UNSUPPORTED, "attention kernel's shared memory exceeds the device limit");
   return DS_OK;

@@ -196,11 +196,11 @@ cudaError_t launch_ln_prep(ActKind ak, const LnPrepArgs& a, cudaStream_t st, boo
 cudaError_t prepare_dense_kernels(int max_smem);
 cudaError_t prepare_moe_kernels(int max_smem);
 
-int attn_nsplit(int B, int heads, int max_len, int num_sms);
-// Shared memory of the attention kernel, and the cached keys per split it
-// stages there (all of a split's keys when they fit a 48 KB budget).
+// Sets a.nsplit, a.stage_keys and a.smem of the decode attention from a.B,
+// a.heads, a.max_len and a.head_dim.
+void attn_configure(AttnArgs& a, int num_sms, int max_smem);
+// Shared memory of the decode attention kernel staging stage_keys K and V rows.
 size_t attn_smem_bytes(int head_dim, int stage_keys);
-int attn_stage_keys(int head_dim, int max_len, int nsplit);
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl);
 cudaError_t prepare_attention_kernels(int max_smem);
 // Prompt chunks: tiled tensor-core (flash) attention, used from this many new

@@ -74,6 +74,9 @@ ds_status tp_fail(ds_status s, const std::string& msg) {
   set_last_error(msg.c_str());
   return s;
 }
+ds_status launch_fail(const char* what, cudaError_t e) {
+  return tp_fail(DS_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e));
+}
 bool al16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 constexpr int kTpMaxRows = 4096;
@@ -342,7 +345,7 @@ ds_status ds_tp_attention_partial(ds_tp_layer* L, const void* x_in, float* x1_pa
   lp.ln_b = L->w.ln1_b;
   lp.out_hi = a_hi;
   lp.out_lo = a_lo;
-  if ((e = launch_ln_prep(ak, lp, st, false)) != cudaSuccess) return tp_fail(DS_ERR_CUDA, "row LayerNorm launch");
+  if ((e = launch_ln_prep(ak, lp, st, false)) != cudaSuccess) return launch_fail("row LayerNorm launch", e);
   DenseArgs base;
   base.M = M;
   base.B = B;
@@ -366,7 +369,7 @@ ds_status ds_tp_attention_partial(ds_tp_layer* L, const void* x_in, float* x1_pa
   r1.max_len = max_len;
   r1.past_len = past_len;
   if ((e = launch_dense(Region::LnQkv, ak, r1, ma[0], split ? ma[1] : nullptr, st, true)) != cudaSuccess)
-    return tp_fail(DS_ERR_CUDA, "QKV launch");
+    return launch_fail("QKV launch", e);
   // attention over the rank's heads, output in the operand format
   AttnArgs ra;
   ra.q = q;
@@ -379,15 +382,13 @@ ds_status ds_tp_attention_partial(ds_tp_layer* L, const void* x_in, float* x1_pa
   ra.head_dim = d;
   ra.max_len = max_len;
   ra.H = Hl;
-  ra.nsplit = attn_nsplit(B, nhl, max_len, L->sms);
   ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  ra.stage_keys = attn_stage_keys(d, max_len, ra.nsplit);
-  ra.smem = attn_smem_bytes(d, ra.stage_keys);
+  attn_configure(ra, L->sms, L->max_smem);
   ra.status = status;
   ra.out_hi = b_hi;
   ra.out_lo = b_lo;
   e = T >= kPrefillMinTokens ? launch_attention_prefill(ak, ra, st, true) : launch_attention(ak, ra, st, true);
-  if (e != cudaSuccess) return tp_fail(DS_ERR_CUDA, "attention launch");
+  if (e != cudaSuccess) return launch_fail("attention launch", e);
   // O-proj over the rank's inputs: the fp32 partial sum (rank 0: + b_o + x)
   DenseArgs r3 = base;
   r3.tmap_w = L->map(1, p.to.kc);
@@ -398,7 +399,7 @@ ds_status ds_tp_attention_partial(ds_tp_layer* L, const void* x_in, float* x1_pa
   r3.resid_act = r == 0 ? x_in : nullptr;
   r3.out_f32 = x1_part;
   if ((e = launch_dense(Region::OprojRes, ak, r3, mb[0], split ? mb[1] : nullptr, st, true)) != cudaSuccess)
-    return tp_fail(DS_ERR_CUDA, "O-proj launch");
+    return launch_fail("O-proj launch", e);
   add_launches(4);
   return DS_OK;
 }
@@ -448,7 +449,7 @@ ds_status ds_tp_ffn_partial(ds_tp_layer* L, const float* x1, float* y_part, int 
   lp.ln_b = L->w.ln2_b;
   lp.out_hi = a_hi;
   lp.out_lo = a_lo;
-  if ((e = launch_ln_prep(ak, lp, st, false)) != cudaSuccess) return tp_fail(DS_ERR_CUDA, "row LayerNorm launch");
+  if ((e = launch_ln_prep(ak, lp, st, false)) != cudaSuccess) return launch_fail("row LayerNorm launch", e);
   DenseArgs base;
   base.M = M;
   base.B = M;
@@ -467,7 +468,7 @@ ds_status ds_tp_ffn_partial(ds_tp_layer* L, const float* x1, float* y_part, int 
   u.out_act = b_hi;
   u.out_lo = b_lo;
   if ((e = launch_dense(Region::FfnUp, ak, u, ma[0], split ? ma[1] : nullptr, st, true)) != cudaSuccess)
-    return tp_fail(DS_ERR_CUDA, "FFN-up launch");
+    return launch_fail("FFN-up launch", e);
   // FFN-down over the rank's features: the fp32 partial sum (rank 0: + b_2 + x1)
   DenseArgs dn = base;
   dn.tmap_w = L->map(3, p.td.kc);
@@ -478,7 +479,7 @@ ds_status ds_tp_ffn_partial(ds_tp_layer* L, const float* x1, float* y_part, int 
   dn.resid_f32 = r == 0 ? x1 : nullptr;
   dn.out_f32 = y_part;
   if ((e = launch_dense(Region::FfnDown, ak, dn, mb[0], split ? mb[1] : nullptr, st, true)) != cudaSuccess)
-    return tp_fail(DS_ERR_CUDA, "FFN-down launch");
+    return launch_fail("FFN-down launch", e);
   add_launches(3);
   return DS_OK;
 }
