@@ -71,6 +71,11 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   p.smem = smem;
   w.stages = p.stages;
   w.smem = smem;
+  // K-sliced tiles with one slice per CTA: the slices of a tile run as one
+  // cluster and are summed on chip (no partial sums through global memory);
+  // each CTA's partial tile is staged in its idle ring.
+  p.cluster = (KS > 1 && w.grid == w.units && w.q == 1 && w.R == 0 &&
+               (size_t)p.stages * SB >= (size_t)ntok * 128 * 4) ? KS : 1;
   *plan = p;
   return true;
 }

@@ -149,11 +149,12 @@ struct DRing {
   }
 };
 
-// Segment enumeration shared by the three roles: leftover segments of this
-// CTA, then its whole units.  f(u, kc0, kc1, j_slot) per segment.
+// Segment enumeration shared by the three roles: leftover segments of CTA
+// `cta` (its place in the work split), then its whole units.
+// f(u, kc0, kc1, j_slot) per segment.
 template <typename F>
-__device__ __forceinline__ void dense_for_segments(const GemvPlan& P, F&& f) {
-  const int cta = blockIdx.x, G = gridDim.x;
+__device__ __forceinline__ void dense_for_segments(const GemvPlan& P, int cta, F&& f) {
+  const int G = gridDim.x;
   long long ra, rb;
   ws_left_range(P, cta, G, &ra, &rb);
   for (long long i = ra; i < rb;) {
@@ -165,6 +166,21 @@ __device__ __forceinline__ void dense_for_segments(const GemvPlan& P, F&& f) {
     i = end;
   }
   for (int u = cta * P.q; u < cta * P.q + P.q; ++u) f(u, 0, P.C, 0);
+}
+
+// Distributed shared memory: a float of CTA `rank` of this cluster at the
+// offset of `local_addr` in this CTA.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+// Every thread of every CTA of the cluster arrives; shared-memory writes
+// before it are visible to the cluster's reads after it.
+__device__ __forceinline__ void dense_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
 template <Region R, typename ACT>
@@ -217,6 +233,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int row_tiles = DP.row_tiles;
+  // Place in the work split: with a cluster per tile, CTA rank s of cluster t
+  // takes K slice s of tile t (unit s * tiles + t).
+  const int KSC = DP.cluster;
+  const int vcta = KSC > 1 ? (int)(blockIdx.x % KSC) * P.tiles + (int)(blockIdx.x / KSC) : (int)blockIdx.x;
 
   if (warp == kDenseTmaWarp) {
     // ---------------------------------------------------------- TMA producer
@@ -231,8 +251,8 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       const uint64_t pol_x = l2_evict_normal_policy();
       const uint32_t tx = (uint32_t)(WB + (kSplit ? 2 : 1) * XB);
       long long ra, rb;
-      ws_left_range(P, blockIdx.x, gridDim.x, &ra, &rb);
-      const int dp_b = blockIdx.x * P.q;
+      ws_left_range(P, vcta, gridDim.x, &ra, &rb);
+      const int dp_b = vcta * P.q;
       const int nchunks = (int)(rb - ra) + P.q * P.C;
       bool dead = false;
       uint32_t last_ph[kDenseMaxStagesDev];  // parity of the last copy issued into each stage
@@ -320,6 +340,11 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         }
       }
     }
+    if (KSC > 1) {  // the cluster reduction's two barriers (every thread takes part)
+      __syncwarp();
+      dense_cluster_sync();
+      dense_cluster_sync();
+    }
   } else if (warp == kDenseMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     pdl_launch_dependents();
@@ -328,7 +353,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       DRing rp;
       int seg = 0;
       bool dead = false;
-      dense_for_segments(P, [&](int u, int kc0, int kc1, int) {
+      dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int) {
         (void)u;
         const int buf = seg & 1;
         if (seg >= 2 && !dead) dead = !mbar_wait(acce_bar(buf), ((seg >> 1) - 1) & 1, a.status);
@@ -358,6 +383,11 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         if (!dead) umma_commit(accf_bar(buf));
         ++seg;
       });
+    }
+    if (KSC > 1) {
+      __syncwarp();
+      dense_cluster_sync();
+      dense_cluster_sync();
     }
   } else {
     // ---------------------------------------------------------- epilogue
@@ -524,22 +554,25 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         }
       }
     };
-    // Finishes one tile: 8 columns at a time, the accumulator taken from
-    // tensor memory (src 0), from nk staged partial slots in shared memory
-    // (src 1) or from nk partials in global memory (src 2); the residual from
-    // shared memory when ops_sm != 0, else from global memory.
-    auto finish_tile = [&](const TileCtx& c, int src, uint32_t tbase, int nk, const float* pg, uint32_t ops_sm) {
+    // Finishes the 8-column groups c0, c0 + cstep, ... of one tile, the
+    // accumulator taken from tensor memory (src 0), from nk staged partial
+    // slots in shared memory (src 1), from nk partials in global memory
+    // (src 2) or from the partial tiles of the nk CTAs of this cluster (src 3,
+    // summed in rank order); the residual from shared memory when
+    // ops_sm != 0, else from global memory.
+    auto finish_tile = [&](const TileCtx& c, int src, uint32_t tbase, int nk, const float* pg, uint32_t ops_sm,
+                           int c0, int cstep) {
       float opn[8];
-      if (ops_sm == 0 && cbeg < c.mrows) ops_load(c, cbeg, opn);
+      if (ops_sm == 0 && c0 < c.mrows) ops_load(c, c0, opn);
 #pragma unroll 1
-      for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {
+      for (int c8 = c0; c8 < c.mrows; c8 += cstep) {
         float v[8], op[8];
         if (ops_sm != 0) {
           ops_from_smem(ops_sm, c8, op);
         } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) op[i] = opn[i];
-          if (c8 + 16 < c.mrows) ops_load(c, c8 + 16, opn);
+          if (c8 + cstep < c.mrows) ops_load(c, c8 + cstep, opn);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = 0.f;
@@ -552,12 +585,20 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] += lds_f32(e0 + (uint32_t)k * slot_stride + (uint32_t)i * 512u);
           }
-        } else {
+        } else if (src == 2) {
 #pragma unroll 1
           for (int k = 0; k < nk; ++k) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               if (c8 + i < c.mrows) v[i] += ld_cg(pg + (size_t)k * slot_floats + (size_t)(c8 + i) * 128 + r);
+          }
+        } else {
+          const uint32_t e0 = st + (uint32_t)(c8 * 128 + r) * 4u;
+#pragma unroll 1
+          for (int k = 0; k < nk; ++k) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (c8 + i < c.mrows) v[i] += ld_cluster_f32(e0 + (uint32_t)i * 512u, (uint32_t)k);
           }
         }
         epi8(c, c8, v, op);
@@ -566,11 +607,39 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     // Tiles this CTA finishes as their last contributor; done after its last
     // segment, when the ring is idle and can stage the partials (a CTA's
     // range has at most two partial segments: its first and its last unit).
+    if (KSC > 1) {
+      // One K slice of one tile per CTA; the cluster's slices are summed
+      // through distributed shared memory.  Each CTA stores its partial tile
+      // in its idle ring ([column][128 rows] fp32; every copy into the ring
+      // has been consumed by the MMAs the accumulator barrier waits for), then
+      // finishes the 8-column groups rank, rank + KSC, ... of the tile (the
+      // two warps of a lane quarter alternating) from all the partial tiles in
+      // rank order: deterministic, nothing through global memory.
+      const int t = (int)(blockIdx.x / KSC), rank = (int)(blockIdx.x % KSC);
+      const TileCtx c = tile_ctx(t);
+      bool dead = !mbar_wait(accf_bar(0), 0, a.status);
+      dead = __any_sync(0xffffffffu, dead);  // (the loads below are warp-collective either way)
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(32 * qd) << 16);
+#pragma unroll 1
+      for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {
+        float v[8];
+        tmem_ld8(tbase + (uint32_t)c8, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c8 + i < c.mrows) sts_f32(st + (uint32_t)((c8 + i) * 128 + r) * 4u, v[i]);
+      }
+      tc_fence_before();
+      dense_cluster_sync();  // every slice's partial tile is in place
+      const int half = (warp - kDenseEpiWarp0) >> 2;
+      finish_tile(c, 3, 0u, KSC, nullptr, 0u, 8 * (rank + KSC * half), 16 * KSC);
+      dense_cluster_sync();  // the other CTAs have read this CTA's partial tile
+    } else {
     int pend_t0 = 0, pend_c0 = 0, pend_t1 = 0, pend_c1 = 0, npend = 0;
     const int nstage_slots = (int)(((size_t)S * SB) / (slot_floats * 4));  // staging slots in the ring
     int seg = 0;
     bool dead = false;
-    dense_for_segments(P, [&](int u, int kc0, int kc1, int j_slot) {
+    dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int j_slot) {
       (void)kc0; (void)kc1;
       const int buf = seg & 1;
       const int sl = u / tiles, t = u - sl * tiles;   // K slice, output tile
@@ -581,7 +650,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * NTOK);
       if (target == 1) {
-        finish_tile(c, 0, tbase, 0, nullptr, 0u);
+        finish_tile(c, 0, tbase, 0, nullptr, 0u, cbeg, 16);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar(buf));
@@ -635,7 +704,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       if (nstage_slots < 2) {
         // a slot larger than half the ring: sum from global memory (the plans
         // give contiguous slots: one K slice, or one CTA per slice)
-        finish_tile(c, 2, 0u, contrib, pbase, 0u);
+        finish_tile(c, 2, 0u, contrib, pbase, 0u, cbeg, 16);
       } else {
         // Rounds of up to nstage_slots partials (one round in the common
         // case); with more, slot 0 carries the running sum between rounds.
@@ -693,13 +762,14 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
             }
             named_bar_sync(kDenseBarEpi, kDenseEpiThreads);  // staging slots free for the next round
           } else {
-            finish_tile(c, 1, 0u, nk, nullptr, ops_sm);
+            finish_tile(c, 1, 0u, nk, nullptr, ops_sm, cbeg, 16);
           }
         }
       }
       if (et == 0) a.counters[t] = 0;
       named_bar_sync(kDenseBarEpi, kDenseEpiThreads);  // the staging slots are read before the next fix-up
     }
+    }  // KSC == 1
     if constexpr (R == Region::FfnDown) {
       if (a.seq_len_inc != nullptr && blockIdx.x == 0 && warp == kDenseEpiWarp0)
         for (int b = lane; b < a.B; b += 32) a.seq_len_inc[b] += 1;

@@ -14,11 +14,22 @@ cudaError_t launch_dense_t(Region r, const DenseArgs& a, const CUtensorMap* xh, 
   cfg.blockDim = dim3(kDenseThreads);
   cfg.dynamicSmemBytes = a.plan.smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (a.plan.cluster > 1) {  // the K slices of one tile: consecutive CTAs, one cluster
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)a.plan.cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   switch (r) {
     case Region::LnQkv: return cudaLaunchKernelEx(&cfg, dense_region_kernel<Region::LnQkv, ACT>, *xh, *xl, a);
     case Region::OprojRes: return cudaLaunchKernelEx(&cfg, dense_region_kernel<Region::OprojRes, ACT>, *xh, *xl, a);

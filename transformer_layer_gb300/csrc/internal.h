@@ -111,6 +111,8 @@ struct DensePlan {
   int kc = 128;        // K per ring stage (64 or 128)
   int stages = 0;
   size_t smem = 0;
+  int cluster = 1;     // > 1: the K slices of each tile are one thread-block cluster of this many
+                       // CTAs (one slice each) whose partial sums meet in distributed shared memory
 };
 
 struct DenseArgs {
