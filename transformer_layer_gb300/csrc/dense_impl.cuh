@@ -285,7 +285,6 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           ws_cursor_next(qp, P, dp_b);
         }
       };
-      l2_ahead(pre + kL2Ahead);
       pdl_wait();
       pdl_launch_dependents();
       {
@@ -302,6 +301,8 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           r2.advance(S);
         }
       }
+      // (after the first X copies, which would otherwise queue behind it)
+      l2_ahead(pre + kL2Ahead);
       for (int j = pre; j < nchunks; ++j) {
         if (!dead) dead = !mbar_wait(empty_bar(rp.st), rp.ph ^ 1, a.status);
         if (dead) break;
@@ -559,11 +560,17 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     // slots in shared memory (src 1), from nk partials in global memory
     // (src 2) or from the partial tiles of the nk CTAs of this cluster (src 3,
     // summed in rank order); the residual from shared memory when
-    // ops_sm != 0, else from global memory.
+    // ops_sm != 0, else from global memory (group c0's operands already in
+    // `pre` when given: loaded before the accumulator was ready).
     auto finish_tile = [&](const TileCtx& c, int src, uint32_t tbase, int nk, const float* pg, uint32_t ops_sm,
-                           int c0, int cstep) {
+                           int c0, int cstep, const float* pre) {
       float opn[8];
-      if (ops_sm == 0 && c0 < c.mrows) ops_load(c, c0, opn);
+      if (pre != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) opn[i] = pre[i];
+      } else if (ops_sm == 0 && c0 < c.mrows) {
+        ops_load(c, c0, opn);
+      }
 #pragma unroll 1
       for (int c8 = c0; c8 < c.mrows; c8 += cstep) {
         float v[8], op[8];
@@ -617,6 +624,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       // rank order: deterministic, nothing through global memory.
       const int t = (int)(blockIdx.x / KSC), rank = (int)(blockIdx.x % KSC);
       const TileCtx c = tile_ctx(t);
+      const int half = (warp - kDenseEpiWarp0) >> 2;
+      const int g0 = 8 * (rank + KSC * half);  // this thread's first 8-column group to finish
+      float pre[8];
+      if (g0 < c.mrows) ops_load(c, g0, pre);  // residual / positions: before the accumulator is ready
       bool dead = !mbar_wait(accf_bar(0), 0, a.status);
       dead = __any_sync(0xffffffffu, dead);  // (the loads below are warp-collective either way)
       tc_fence_after();
@@ -631,8 +642,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       }
       tc_fence_before();
       dense_cluster_sync();  // every slice's partial tile is in place
-      const int half = (warp - kDenseEpiWarp0) >> 2;
-      finish_tile(c, 3, 0u, KSC, nullptr, 0u, 8 * (rank + KSC * half), 16 * KSC);
+      finish_tile(c, 3, 0u, KSC, nullptr, 0u, g0, 16 * KSC, g0 < c.mrows ? pre : nullptr);
       dense_cluster_sync();  // the other CTAs have read this CTA's partial tile
     } else {
     int pend_t0 = 0, pend_c0 = 0, pend_t1 = 0, pend_c1 = 0, npend = 0;
@@ -645,12 +655,16 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       const int sl = u / tiles, t = u - sl * tiles;   // K slice, output tile
       const int target = ws_tile_target(t, P, gridDim.x);  // contributions that complete the tile
       const TileCtx c = tile_ctx(t);
+      // a tile finished here: its first operands before the accumulator is ready
+      float pre[8];
+      const bool pre_ok = target == 1 && cbeg < c.mrows;
+      if (pre_ok) ops_load(c, cbeg, pre);
       if (!dead) dead = !mbar_wait(accf_bar(buf), (seg >> 1) & 1, a.status);
       dead = __any_sync(0xffffffffu, dead);  // tcgen05.ld below is warp-collective
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(buf * NTOK);
       if (target == 1) {
-        finish_tile(c, 0, tbase, 0, nullptr, 0u, cbeg, 16);
+        finish_tile(c, 0, tbase, 0, nullptr, 0u, cbeg, 16, pre_ok ? pre : nullptr);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar(buf));
@@ -704,7 +718,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       if (nstage_slots < 2) {
         // a slot larger than half the ring: sum from global memory (the plans
         // give contiguous slots: one K slice, or one CTA per slice)
-        finish_tile(c, 2, 0u, contrib, pbase, 0u, cbeg, 16);
+        finish_tile(c, 2, 0u, contrib, pbase, 0u, cbeg, 16, nullptr);
       } else {
         // Rounds of up to nstage_slots partials (one round in the common
         // case); with more, slot 0 carries the running sum between rounds.
@@ -762,7 +776,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
             }
             named_bar_sync(kDenseBarEpi, kDenseEpiThreads);  // staging slots free for the next round
           } else {
-            finish_tile(c, 1, 0u, nk, nullptr, ops_sm, cbeg, 16);
+            finish_tile(c, 1, 0u, nk, nullptr, ops_sm, cbeg, 16, nullptr);
           }
         }
       }
