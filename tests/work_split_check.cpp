@@ -32,7 +32,7 @@ static int verify(const GemvPlan& P, int N, int K, int M) {
   for (int cta = 0; cta < G; ++cta) {
     long long ra, rb;
     ws_left_range(P, cta, G, &ra, &rb);
-    const int dp_b = cta * P.q;
+    const int dp_b = ws_dp_first(P, cta);
     const int nch = (int)(rb - ra) + P.q * C;
     // streaming warps
     Cursor q;
@@ -57,7 +57,7 @@ static int verify(const GemvPlan& P, int N, int K, int M) {
       if (end <= i) return fail("leftover segment does not advance", N, K, M, G, cta, (int)i);
       i = end;
     }
-    for (int u = dp_b; u < dp_b + P.q; ++u) esegs.push_back(std::make_pair(u, 0));
+    for (int i = 0; i < P.q; ++i) esegs.push_back(std::make_pair(ws_dp_unit(P, cta, i), 0));
     if (esegs.size() != segs.size())
       return fail("segment count differs", N, K, M, G, (int)esegs.size(), (int)segs.size());
     for (size_t i = 0; i < segs.size(); ++i) {
@@ -123,9 +123,13 @@ static int check_tiles_sliced(int tiles, int K, int G0) {
   P.K_S = K / KS;
   P.C = P.K_S / 128;
   P.units = tiles * KS;
-  ws_distribute(P, G0, true);
+  // as the tile planner: more tiles than CTAs -> whole tiles, round-robin
+  const bool many = tiles > G0;
+  ws_distribute(P, G0, true, many);
+  P.interleave = many ? 1 : 0;
   if (P.units <= G0 && (P.grid != P.units || P.q != 1 || P.R != 0))
     return fail("one unit per CTA not kept", 128 * tiles, K, 0, P.grid, P.units, P.q);
+  if (many && P.R > 0 && !P.whole) return fail("leftover tiles split", 128 * tiles, K, 0, P.grid, P.units, P.q);
   return verify(P, 128 * tiles, K, 0);
 }
 

@@ -34,7 +34,10 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   DensePlan p;
   p.row_tiles = N / 128;
   int ntok = (M + 15) / 16 * 16;
-  const int ntok_max = 128;  // (wider token tiles re-stream more X through L2 per FLOP)
+  // Token tiles of up to 128 rows; fp16 prompt chunks of 256 rows and more
+  // take 256 (MMA N = 256: half the weight re-reads per FLOP; the bf16 hi/lo
+  // operand would leave too shallow a ring).
+  const int ntok_max = (!split && M >= 256) ? 256 : 128;
   if (ntok > ntok_max) ntok = ntok_max;
   p.ntok = ntok;
   p.tok_tiles = (M + ntok - 1) / ntok;
@@ -56,7 +59,13 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   w.K_S = K / KS;
   w.C = w.K_S / p.kc;
   w.units = w.tiles * KS;
-  ws_distribute(w, num_sms, /*one_unit_each=*/true);
+  // More tiles than SMs (prompt chunks): whole tiles only (no split-K
+  // fix-ups of large tiles), handed out round-robin, so that the CTAs running
+  // at the same time take the token tiles of the same weight rows and read
+  // those weights from DRAM once between them.
+  const bool many = w.tiles > num_sms;
+  ws_distribute(w, num_sms, /*one_unit_each=*/true, /*force_whole=*/many);
+  w.interleave = many ? 1 : 0;
   const size_t SB = (dense_stage_bytes(ntok, p.kc, split) + 1023) & ~(size_t)1023;
   const size_t fixed = 1024 + 8 * (2 * kDenseMaxStages + 6) + 16;
   if ((size_t)max_smem < fixed + 2 * SB) return false;

@@ -165,7 +165,7 @@ __device__ __forceinline__ void dense_for_segments(const GemvPlan& P, int cta, F
     f(u, kc0, kc0 + (int)(end - i), j_slot);
     i = end;
   }
-  for (int u = cta * P.q; u < cta * P.q + P.q; ++u) f(u, 0, P.C, 0);
+  for (int i = 0; i < P.q; ++i) f(ws_dp_unit(P, cta, i), 0, P.C, 0);
 }
 
 // Distributed shared memory: a float of CTA `rank` of this cluster at the
@@ -232,7 +232,11 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int row_tiles = DP.row_tiles;
+  // Tile t covers weight rows [128 (t / tok_tiles), +128) and X rows
+  // [NTOK (t % tok_tiles), +NTOK): the token tiles of one weight tile are
+  // consecutive units, so CTAs that run at the same time share its weights
+  // through L2.
+  const int tok_tiles = DP.tok_tiles;
   // Place in the work split: with a cluster per tile, CTA rank s of cluster t
   // takes K slice s of tile t (unit s * tiles + t).
   const int KSC = DP.cluster;
@@ -247,12 +251,13 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         pdl_wait();
         tmap_w = a.tmap_table + (size_t)128 * (size_t)(*a.sel_idx);
       }
-      const uint64_t pol_w = l2_evict_first_policy();
+      // weights read once: evict first; read again by other token tiles: keep
+      const uint64_t pol_w = tok_tiles > 1 ? l2_evict_normal_policy() : l2_evict_first_policy();
       const uint64_t pol_x = l2_evict_normal_policy();
       const uint32_t tx = (uint32_t)(WB + (kSplit ? 2 : 1) * XB);
       long long ra, rb;
       ws_left_range(P, vcta, gridDim.x, &ra, &rb);
-      const int dp_b = vcta * P.q;
+      const int dp_b = ws_dp_first(P, vcta);
       const int nchunks = (int)(rb - ra) + P.q * P.C;
       bool dead = false;
       uint32_t last_ph[kDenseMaxStagesDev];  // parity of the last copy issued into each stage
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       DRing rp;
       for (int j = 0; j < pre; ++j) {
         const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
-        const int trow = q.t % row_tiles;
+        const int trow = q.t / tok_tiles;
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
         tma_load_3d(stage, tmap_w, 0, trow * 128, (q.s * P.C + q.kc) * (KC / 64), full_bar(rp.st), pol_w);
         last_ph[rp.st] = rp.ph;
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       int fpre = pre;
       auto l2_ahead = [&](int upto) {
         for (; fpre < upto && fpre < nchunks; ++fpre) {
-          tma_prefetch_3d(tmap_w, 0, (qp.t % row_tiles) * 128, (qp.s * P.C + qp.kc) * (KC / 64));
+          tma_prefetch_3d(tmap_w, 0, (qp.t / tok_tiles) * 128, (qp.s * P.C + qp.kc) * (KC / 64));
           ws_cursor_next(qp, P, dp_b);
         }
       };
@@ -292,7 +297,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         Cursor c = q0;
         for (int j = 0; j < pre; ++j) {
           const uint32_t stage = smem_u32(sm + (size_t)r2.st * SB);
-          const int jt = c.t / row_tiles;
+          const int jt = c.t % tok_tiles;
           const int kseg = (c.s * P.C + c.kc) * (KC / 64);
           tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
           if constexpr (kSplit)
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         if (!dead) dead = !mbar_wait(empty_bar(rp.st), rp.ph ^ 1, a.status);
         if (dead) break;
         const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
-        const int trow = q.t % row_tiles, jt = q.t / row_tiles;
+        const int trow = q.t / tok_tiles, jt = q.t % tok_tiles;
         const int kseg = (q.s * P.C + q.kc) * (KC / 64);
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
         tma_load_3d(stage, tmap_w, 0, trow * 128, kseg, full_bar(rp.st), pol_w);
@@ -330,13 +335,13 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         const GemvPlan& Pn = a.next_plan.ws;
         long long na, nb;
         ws_left_range(Pn, blockIdx.x, Pn.grid, &na, &nb);
-        const int ndp = blockIdx.x * Pn.q;
+        const int ndp = ws_dp_first(Pn, blockIdx.x);
         int nn = (int)(nb - na) + Pn.q * Pn.C;
         if (nn > 16) nn = 16;
         Cursor c;
         ws_cursor_init(c, Pn, na, nb, ndp);
         for (int j = 0; j < nn; ++j) {
-          tma_prefetch_3d(a.next_tmap_w, 0, (c.t % a.next_plan.row_tiles) * 128, c.kc * a.next_plan.kc / 64);
+          tma_prefetch_3d(a.next_tmap_w, 0, (c.t / a.next_plan.tok_tiles) * 128, c.kc * a.next_plan.kc / 64);
           ws_cursor_next(c, Pn, ndp);
         }
       }
@@ -413,8 +418,8 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     auto tile_ctx = [&](int t) {
       TileCtx c;
       c.t = t;
-      c.n = (t % row_tiles) * 128 + r;
-      c.m0 = (t / row_tiles) * NTOK;
+      c.n = (t / tok_tiles) * 128 + r;
+      c.m0 = (t % tok_tiles) * NTOK;
       c.mrows = min(NTOK, M - c.m0);
       const int bsel = a.sel_idx != nullptr ? a.sel_bias_stride * (*a.sel_idx) : 0;
       c.bias = a.bias != nullptr ? Act<ACT>::to_f(static_cast<const ACT*>(a.bias)[bsel + c.n]) : 0.f;

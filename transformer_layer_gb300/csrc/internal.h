@@ -49,6 +49,7 @@ struct GemvPlan {
   long long R = 0;   // leftover chunks spread over the grid
   int maxc = 1;      // most CTAs contributing to one leftover unit
   int whole = 0;     // 1: leftover units go whole to CTAs (no split-K fix-up)
+  int interleave = 0;  // 1: CTA c's whole units are c, c + grid, c + 2 grid, ... (else c q .. c q + q - 1)
   int grid = 0;      // CTAs
   int nt = 1;        // n-tiles of 8 batch rows (1, 2, 4, 8)
   int nblk = 4;      // k-blocks per warp step (4, or 2 / 1 for narrow K)

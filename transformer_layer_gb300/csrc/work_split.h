@@ -69,6 +69,10 @@ DS_HD int ws_tile_target(int t, const GemvPlan& P, int G) {
   return n;
 }
 
+// First whole unit of CTA cta (the cursors' dp_b), and its i-th.
+DS_HD int ws_dp_first(const GemvPlan& P, int cta) { return P.interleave ? cta : cta * P.q; }
+DS_HD int ws_dp_unit(const GemvPlan& P, int cta, int i) { return P.interleave ? cta + i * P.grid : cta * P.q + i; }
+
 // Position in a CTA's chunk sequence: leftover chunks first, then whole units.
 struct Cursor {
   int s, t, kc;  // slice, row tile, chunk within the unit
@@ -102,7 +106,11 @@ DS_HD void ws_cursor_next(Cursor& q, const GemvPlan& P, int dp_b) {
   }
   if (++q.kc == P.C) {
     q.kc = 0;
-    if (++q.t == P.tiles) {
+    if (P.interleave) {  // next whole unit: grid units further on
+      const int u = q.s * P.tiles + q.t + P.grid;
+      q.s = u / P.tiles;
+      q.t = u - q.s * P.tiles;
+    } else if (++q.t == P.tiles) {
       q.t = 0;
       ++q.s;
     }
@@ -130,8 +138,9 @@ DS_HD void ws_leftover_segment(const GemvPlan& P, long long i, long long rb, int
 // p.grid, q whole units per CTA, and either whole leftover units or their
 // chunks spread evenly (p.whole, p.U_dp, p.R, p.maxc).  p.units and p.C must
 // be set.  one_unit_each: when there are no more units than CTAs, give each
-// CTA exactly one whole unit (grid = units, nothing split).
-inline void ws_distribute(GemvPlan& p, int num_ctas, bool one_unit_each = false) {
+// CTA exactly one whole unit (grid = units, nothing split).  force_whole:
+// leftover units always go whole to CTAs (no split-K fix-ups).
+inline void ws_distribute(GemvPlan& p, int num_ctas, bool one_unit_each = false, bool force_whole = false) {
   if (one_unit_each && p.units <= num_ctas) {
     p.grid = p.units;
     p.q = 1;
@@ -157,7 +166,7 @@ inline void ws_distribute(GemvPlan& p, int num_ctas, bool one_unit_each = false)
     if (qs > 0 && lu * p.C > 0 && lu * p.C < p.grid) qs -= 1;
     const long long rs = (p.units - qs * p.grid) * p.C;
     const long long split_max = qs * p.C + (rs + p.grid - 1) / p.grid;
-    if (lu > 0 && whole_max - split_max <= 3) p.whole = 1;
+    if (lu > 0 && (force_whole || whole_max - split_max <= 3)) p.whole = 1;
   }
   // Every CTA must own at least one leftover chunk when there are any (so the
   // CTAs sharing a leftover unit are consecutive, with no empty ranges in
