@@ -38,17 +38,21 @@
  *     that input width uses groups of 128 (H with quant_group 128; F with
  *     quant_group 128 and no extra MLP grouping).
  *   - Rows R = B*T (batch rows x new tokens) per call: 1..4096 with fp16 /
- *     bf16 weights, 1..64 with int8 weights.  Up to 8 rows (and always for
- *     int8) the GEMMs run as streaming skinny-GEMM kernels with the
- *     LayerNorm fused into their prologue; above 8 rows as tensor-core tile
- *     kernels (tcgen05, accumulators in tensor memory), each LayerNorm then
- *     running as a small row kernel ahead of its GEMM (seven kernels per
- *     layer instead of five).  With int8 weights the activations staged per
- *     GEMV slice (80 KB of shared memory) bound R further: up to 64 rows with
- *     fp16 activations and 39 with bf16 for groups of 64; 39 (fp16) and 19
- *     (bf16) once a matrix uses groups of 128.  Beyond the limits
- *     ds_layer_workspace_bytes and ds_stack_workspace_bytes return 0 and the
- *     forward calls return DS_ERR_UNSUPPORTED before any launch.
+ *     bf16 weights and with int8 weights under fp16 activations; 1..64 with
+ *     int8 weights under bf16 activations.  Up to 8 rows (and always for
+ *     int8 under bf16) the GEMMs run as streaming skinny-GEMM kernels with
+ *     the LayerNorm fused into their prologue; above 8 rows as tensor-core
+ *     tile kernels (tcgen05, accumulators in tensor memory), each LayerNorm
+ *     then running as a small row kernel ahead of its GEMM (seven kernels
+ *     per layer instead of five).  The int8 tile kernels dequantise each
+ *     stage of codes to fp16 in shared memory (q * s rounded once to fp16,
+ *     the MMA operand type); the int8 streaming kernels apply each group's
+ *     scale to its fp32 partial sum.  With int8 weights under bf16
+ *     activations the activations staged per GEMV slice (80 KB of shared
+ *     memory) bound R further: up to 39 rows for groups of 64, 19 once a
+ *     matrix uses groups of 128.  Beyond the limits ds_layer_workspace_bytes
+ *     and ds_stack_workspace_bytes return 0 and the forward calls return
+ *     DS_ERR_UNSUPPORTED before any launch.
  *   - The forward calls run on the device the layer was created on, which
  *     must be the current device (else DS_ERR_INVALID_ARG, nothing launched).
  *   - Calls are asynchronous on the given stream (never synchronising, except

@@ -129,10 +129,13 @@ def test_skinny_gemm_sweep_layer(act, B):
         L.close()
 
 
-@pytest.mark.parametrize("act,B", [(torch.float16, 32), (torch.float16, 64), (torch.bfloat16, 32)])
+@pytest.mark.parametrize("act,B", [(torch.float16, 9), (torch.float16, 32), (torch.float16, 64),
+                                   (torch.float16, 150), (torch.bfloat16, 32)])
 def test_int8_layer_many_rows(act, B):
-    """MoQ int8 weights at 32 and 64 batch rows (the streaming GEMV kernels
-    with four and eight MMA column tiles; bf16 activations up to 39 rows)."""
+    """MoQ int8 weights at 9..150 batch rows: with fp16 activations the
+    tensor-core tile kernels, whose converter warps dequantise each stage of
+    codes to fp16 in shared memory (several token tiles at 150 rows); with
+    bf16 activations the streaming GEMV kernels (up to 39 rows)."""
     H, nh, F = 1024, 8, 4096
     L = DeviceLayer(H, nh, F, seed=1011, act_dtype=act, weight_dtype=torch.int8)
     try:
@@ -220,14 +223,17 @@ def test_prompt_chunk_layer_4096(act, B, T, past):
         L.close()
 
 
-def test_prompt_chunk_int8():
-    """A prompt chunk with MoQ int8 weights (streaming GEMV kernels, 48 rows)
-    and the tiled flash attention."""
-    L = DeviceLayer(1024, 8, 4096, seed=1013, weight_dtype=torch.int8)
+@pytest.mark.parametrize("B,T,group,extra", [(2, 24, 64, 0), (1, 256, 64, 0), (2, 100, 128, 1)])
+def test_prompt_chunk_int8(B, T, group, extra):
+    """Prompt chunks with MoQ int8 weights (int8 tile kernels: 48 to 256 rows,
+    groups of 64, or 128 with the FFN in groups of 64) and the tiled flash
+    attention."""
+    L = DeviceLayer(1024, 8, 4096, seed=1013, weight_dtype=torch.int8, quant_group=group,
+                    mlp_extra_grouping=extra)
     try:
-        past = [9, 40]
-        res = run_layer(L, 2, 24, past, max_len=80, seed=17)
-        check_layer(L, res, 2, 24, past, "int8 prompt")
+        past = [9, 40][:B]
+        res = run_layer(L, B, T, past, max_len=max(past) + T + 8, seed=17)
+        check_layer(L, res, B, T, past, f"int8 prompt B={B} T={T} g{group}")
     finally:
         L.close()
 

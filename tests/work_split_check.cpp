@@ -123,8 +123,9 @@ static int check_tiles_sliced(int tiles, int K, int G0) {
   P.K_S = K / KS;
   P.C = P.K_S / 128;
   P.units = tiles * KS;
-  // as the tile planner: more tiles than CTAs -> whole tiles, round-robin
-  const bool many = tiles > G0;
+  // as the tile planner with several token tiles: more tiles than CTAs ->
+  // whole tiles, round-robin (the planner splits leftovers with one token tile)
+  const bool many = tiles > G0 && (tiles % 3) != 0;
   ws_distribute(P, G0, true, many);
   P.interleave = many ? 1 : 0;
   if (P.units <= G0 && (P.grid != P.units || P.q != 1 || P.R != 0))

@@ -20,28 +20,34 @@ cudaError_t launch_dense_f16(Region r, const DenseArgs& a, const CUtensorMap* xh
                              cudaStream_t st, bool pdl);
 cudaError_t launch_dense_bf16(Region r, const DenseArgs& a, const CUtensorMap* xh, const CUtensorMap* xl,
                               cudaStream_t st, bool pdl);
+cudaError_t launch_dense_i8(Region r, const DenseArgs& a, const CUtensorMap* xh, const CUtensorMap* xl,
+                            cudaStream_t st, bool pdl);
 cudaError_t prepare_dense_f16(int max_smem);
 cudaError_t prepare_dense_bf16(int max_smem);
+cudaError_t prepare_dense_i8(int max_smem);
 
 namespace {
 constexpr size_t kDenseMinSmem = 120 * 1024;  // two tile CTAs never share an SM (nor its TMEM)
 constexpr int kDenseMaxStages = kDenseMaxStagesDev;
 }  // namespace
 
-bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem, DensePlan* plan) {
+bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem, DensePlan* plan, bool i8) {
   if (N <= 0 || K <= 0 || M < 1 || (N % 128) != 0 || (K % 128) != 0 || num_sms < 1) return false;
   const bool split = (ak == ActKind::BF16);
+  if (i8 && split) return false;  // int8 tiles take fp16 activations
   DensePlan p;
+  p.i8 = i8 ? 1 : 0;
   p.row_tiles = N / 128;
   int ntok = (M + 15) / 16 * 16;
   // Token tiles of up to 128 rows; fp16 prompt chunks of 256 rows and more
   // take 256 (MMA N = 256: half the weight re-reads per FLOP; the bf16 hi/lo
-  // operand would leave too shallow a ring).
-  const int ntok_max = (!split && M >= 256) ? 256 : 128;
+  // operand would leave too shallow a ring).  int8: up to 64 rows (its two
+  // fp16 W tiles take 64 KB beside the ring).
+  const int ntok_max = i8 ? 64 : ((!split && M >= 256) ? 256 : 128);
   if (ntok > ntok_max) ntok = ntok_max;
   p.ntok = ntok;
   p.tok_tiles = (M + ntok - 1) / ntok;
-  p.kc = (ntok > 64 || K % 128 != 0) ? 64 : 128;
+  p.kc = i8 ? 128 : ((ntok > 64 || K % 128 != 0) ? 64 : 128);
   GemvPlan& w = p.ws;
   w.tiles = p.row_tiles * p.tok_tiles;
   w.chunk_k = p.kc;
@@ -59,15 +65,16 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   w.K_S = K / KS;
   w.C = w.K_S / p.kc;
   w.units = w.tiles * KS;
-  // More tiles than SMs (prompt chunks): whole tiles only (no split-K
-  // fix-ups of large tiles), handed out round-robin, so that the CTAs running
-  // at the same time take the token tiles of the same weight rows and read
-  // those weights from DRAM once between them.
-  const bool many = w.tiles > num_sms;
+  // More tiles than SMs with several token tiles (prompt chunks): whole
+  // tiles only (no split-K fix-ups of large tiles), handed out round-robin, so
+  // that the CTAs running at the same time take the token tiles of the same
+  // weight rows and read those weights from DRAM once between them.  (With one
+  // token tile, e.g. N = 20480 at decode, the few leftover tiles are split.)
+  const bool many = w.tiles > num_sms && p.tok_tiles > 1;
   ws_distribute(w, num_sms, /*one_unit_each=*/true, /*force_whole=*/many);
   w.interleave = many ? 1 : 0;
-  const size_t SB = (dense_stage_bytes(ntok, p.kc, split) + 1023) & ~(size_t)1023;
-  const size_t fixed = 1024 + 8 * (2 * kDenseMaxStages + 6) + 16;
+  const size_t SB = (dense_stage_bytes(ntok, p.kc, split, i8) + 1023) & ~(size_t)1023;
+  const size_t fixed = 1024 + dense_wtile_bytes(p.kc, i8) + 8 * (2 * kDenseMaxStages + 10) + 16;
   if ((size_t)max_smem < fixed + 2 * SB) return false;
   size_t s = ((size_t)max_smem - fixed) / SB;
   if (s > (size_t)kDenseMaxStages) s = kDenseMaxStages;
@@ -93,6 +100,7 @@ cudaError_t launch_dense(Region r, ActKind ak, const DenseArgs& a, const void* x
                          cudaStream_t st, bool pdl) {
   const CUtensorMap* xh = static_cast<const CUtensorMap*>(xmap_hi);
   const CUtensorMap* xl = static_cast<const CUtensorMap*>(xmap_lo != nullptr ? xmap_lo : xmap_hi);
+  if (a.plan.i8) return ak == ActKind::F16 ? launch_dense_i8(r, a, xh, xl, st, pdl) : cudaErrorInvalidValue;
   if (ak == ActKind::F16) return launch_dense_f16(r, a, xh, xl, st, pdl);
   return launch_dense_bf16(r, a, xh, xl, st, pdl);
 }
@@ -100,6 +108,7 @@ cudaError_t launch_dense(Region r, ActKind ak, const DenseArgs& a, const void* x
 cudaError_t prepare_dense_kernels(int max_smem) {
   cudaError_t e = prepare_dense_f16(max_smem);
   if (e == cudaSuccess) e = prepare_dense_bf16(max_smem);
+  if (e == cudaSuccess) e = prepare_dense_i8(max_smem);
   return e;
 }
 

@@ -56,10 +56,13 @@
 namespace ds {
 
 constexpr int kDenseEpiWarps = 8;    // two per TMEM lane quarter, each taking half the columns
+constexpr int kDenseConvWarps = 4;   // int8 weights: warps that dequantise the codes to fp16
 constexpr int kDenseThreads = (2 + kDenseEpiWarps) * 32;
+constexpr int kDenseThreadsI8 = (2 + kDenseEpiWarps + kDenseConvWarps) * 32;
 constexpr int kDenseTmaWarp = 0;
 constexpr int kDenseMmaWarp = 1;
 constexpr int kDenseEpiWarp0 = 2;    // warps 2 .. 9
+constexpr int kDenseConvWarp0 = 10;  // int8: warps 10 .. 13
 constexpr int kDenseEpiThreads = kDenseEpiWarps * 32;
 constexpr int kDenseBarEpi = 1;      // named barrier of the four epilogue warps
 constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
@@ -125,12 +128,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 
 // ---------------------------------------------------------------- geometry
 // One ring stage: W [KC/64 atoms][128 rows][128 B], then X [KC/64][NTOK][128 B]
-// (and, for bf16, X lo the same), each part on a 1024-byte boundary.
+// (and, for bf16, X lo the same), each part on a 1024-byte boundary.  With
+// int8 weights a stage holds the TMA copy of the codes, [128 rows][KC bytes]
+// (KC = 128, 128-byte swizzle), then X; their fp16 dequantisation goes to one
+// of two W tiles after the ring, so the ring's depth (the bytes in flight)
+// does not pay for the fp16 tile.
 __host__ __device__ inline size_t dense_w_bytes(int kc) { return (size_t)128 * kc * 2; }
 __host__ __device__ inline size_t dense_x_bytes(int ntok, int kc) { return (size_t)ntok * kc * 2; }
-__host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split) {
-  return dense_w_bytes(kc) + (split ? 2 : 1) * dense_x_bytes(ntok, kc);
+__host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split, bool i8 = false) {
+  return (i8 ? (size_t)128 * kc : dense_w_bytes(kc)) + (split ? 2 : 1) * dense_x_bytes(ntok, kc);
 }
+// Shared memory after the ring: the int8 path's two fp16 W tiles.
+__host__ __device__ inline size_t dense_wtile_bytes(int kc, bool i8) { return i8 ? 2 * dense_w_bytes(kc) : 0; }
 __host__ __device__ inline uint32_t dense_tmem_cols(int ntok) {
   uint32_t c = 32;
   while (c < (uint32_t)(2 * ntok)) c <<= 1;
@@ -183,11 +192,15 @@ __device__ __forceinline__ void dense_cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-template <Region R, typename ACT>
-__global__ void __launch_bounds__(kDenseThreads, 1)
+// kI8: W is int8 codes with fp16 scales per group of qgroup along K (MoQ);
+// the converter warps dequantise each stage's codes to fp16 (q * s rounded
+// once to fp16, the MMA operand type) before its MMAs.
+template <Region R, typename ACT, bool kI8>
+__global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     dense_region_kernel(const __grid_constant__ CUtensorMap xmap_hi, const __grid_constant__ CUtensorMap xmap_lo,
                         const DenseArgs a) {
   constexpr bool kSplit = std::is_same<ACT, __nv_bfloat16>::value;
+  static_assert(!kI8 || !kSplit, "int8 tiles take fp16 activations");
   constexpr bool kStats = (R == Region::OprojRes || R == Region::FfnDown);
   extern __shared__ __align__(1024) unsigned char dsm_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
@@ -195,8 +208,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   const GemvPlan& P = DP.ws;
   const int S = DP.stages, KC = DP.kc, NTOK = DP.ntok;
   const size_t WB = dense_w_bytes(KC), XB = dense_x_bytes(NTOK, KC);
-  const size_t SB = (dense_stage_bytes(NTOK, KC, kSplit) + 1023) & ~(size_t)1023;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)S * SB);
+  const size_t SB = (dense_stage_bytes(NTOK, KC, kSplit, kI8) + 1023) & ~(size_t)1023;
+  const uint32_t XOFF = kI8 ? (uint32_t)(128 * KC) : (uint32_t)WB;  // X within a stage
+  const uint32_t wtile = smem_u32(sm + (size_t)S * SB);             // int8: the two fp16 W tiles
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)S * SB + dense_wtile_bytes(KC, kI8));
   // full[S], empty[S], acc_full[2], acc_empty[2]
   auto full_bar = [&](int i) { return smem_u32(bars + i); };
   auto empty_bar = [&](int i) { return smem_u32(bars + S + i); };
@@ -204,7 +219,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
   auto acce_bar = [&](int i) { return smem_u32(bars + 2 * S + 2 + i); };
   const uint32_t fix_bar = smem_u32(bars + 2 * S + 4);   // staged partials of a fix-up
   const uint32_t done_bar = smem_u32(bars + 2 * S + 5);  // epilogue warps done with TMEM
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
+  // int8: fp16 W tile i written (converter warps) / read by the MMAs (commit)
+  auto wfull_bar = [&](int i) { return smem_u32(bars + 2 * S + 6 + i); };
+  auto wempty_bar = [&](int i) { return smem_u32(bars + 2 * S + 8 + i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 10);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const uint32_t tcols = dense_tmem_cols(NTOK);
 
@@ -225,6 +243,11 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
     }
     mbar_init(fix_bar, 1);
     mbar_init(done_bar, kDenseEpiWarps);
+    if (kI8)
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(wfull_bar(i), kDenseConvWarps);
+        mbar_init(wempty_bar(i), 1);
+      }
     mbar_init_fence();
   }
   if (warp == kDenseMmaWarp) tmem_alloc(smem_u32(tmem_slot), tcols);
@@ -254,7 +277,11 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       // weights read once: evict first; read again by other token tiles: keep
       const uint64_t pol_w = tok_tiles > 1 ? l2_evict_normal_policy() : l2_evict_first_policy();
       const uint64_t pol_x = l2_evict_normal_policy();
-      const uint32_t tx = (uint32_t)(WB + (kSplit ? 2 : 1) * XB);
+      const uint32_t tx = (uint32_t)((kI8 ? (size_t)128 * KC : WB) + (kSplit ? 2 : 1) * XB);
+      const uint32_t woff = 0u;                                    // where W's copy lands
+      auto wk_of = [&](const Cursor& c) {                          // W's K coordinate (128-byte atoms)
+        return (c.s * P.C + c.kc) * (kI8 ? KC / 128 : KC / 64);
+      };
       long long ra, rb;
       ws_left_range(P, vcta, gridDim.x, &ra, &rb);
       const int dp_b = ws_dp_first(P, vcta);
@@ -272,7 +299,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
         const int trow = q.t / tok_tiles;
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
-        tma_load_3d(stage, tmap_w, 0, trow * 128, (q.s * P.C + q.kc) * (KC / 64), full_bar(rp.st), pol_w);
+        tma_load_3d(stage + woff, tmap_w, 0, trow * 128, wk_of(q), full_bar(rp.st), pol_w);
         last_ph[rp.st] = rp.ph;
         issued |= 1u << rp.st;
         ws_cursor_next(q, P, dp_b);
@@ -286,7 +313,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       int fpre = pre;
       auto l2_ahead = [&](int upto) {
         for (; fpre < upto && fpre < nchunks; ++fpre) {
-          tma_prefetch_3d(tmap_w, 0, (qp.t / tok_tiles) * 128, (qp.s * P.C + qp.kc) * (KC / 64));
+          tma_prefetch_3d(tmap_w, 0, (qp.t / tok_tiles) * 128, wk_of(qp));
           ws_cursor_next(qp, P, dp_b);
         }
       };
@@ -299,9 +326,9 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
           const uint32_t stage = smem_u32(sm + (size_t)r2.st * SB);
           const int jt = c.t % tok_tiles;
           const int kseg = (c.s * P.C + c.kc) * (KC / 64);
-          tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
+          tma_load_3d(stage + XOFF, &xmap_hi, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
           if constexpr (kSplit)
-            tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
+            tma_load_3d(stage + XOFF + (uint32_t)XB, &xmap_lo, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
           ws_cursor_next(c, P, dp_b);
           r2.advance(S);
         }
@@ -315,10 +342,10 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         const int trow = q.t / tok_tiles, jt = q.t % tok_tiles;
         const int kseg = (q.s * P.C + q.kc) * (KC / 64);
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
-        tma_load_3d(stage, tmap_w, 0, trow * 128, kseg, full_bar(rp.st), pol_w);
-        tma_load_3d(stage + (uint32_t)WB, &xmap_hi, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
+        tma_load_3d(stage + woff, tmap_w, 0, trow * 128, wk_of(q), full_bar(rp.st), pol_w);
+        tma_load_3d(stage + XOFF, &xmap_hi, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
         if constexpr (kSplit)
-          tma_load_3d(stage + (uint32_t)(WB + XB), &xmap_lo, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
+          tma_load_3d(stage + XOFF + (uint32_t)XB, &xmap_lo, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
         last_ph[rp.st] = rp.ph;
         issued |= 1u << rp.st;
         ws_cursor_next(q, P, dp_b);
@@ -358,6 +385,7 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       const uint32_t idesc = umma_idesc(kSplit, NTOK);
       DRing rp;
       int seg = 0;
+      int wj = 0;  // int8: chunks so far (W tile wj % 2, its use wj / 2)
       bool dead = false;
       dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int) {
         (void)u;
@@ -366,11 +394,15 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * NTOK);
         for (int kc = kc0; kc < kc1; ++kc) {
-          if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);
+          // int8: the converter has waited for this stage and filled W tile wslot
+          const int wslot = wj & 1;
+          if (kI8 && !dead) dead = !mbar_wait(wfull_bar(wslot), (uint32_t)((wj >> 1) & 1), a.status);
+          if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);  // (int8: already complete)
           if (!dead) {
             tc_fence_after();
-            const uint32_t wbase = smem_u32(sm + (size_t)rp.st * SB);
-            const uint32_t xbase = wbase + (uint32_t)WB;
+            const uint32_t sbase = smem_u32(sm + (size_t)rp.st * SB);
+            const uint32_t wbase = kI8 ? wtile + (uint32_t)(wslot * WB) : sbase;
+            const uint32_t xbase = sbase + XOFF;
 #pragma unroll 1
             for (int kb = 0; kb < KC / 64; ++kb) {
 #pragma unroll
@@ -383,13 +415,92 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
               }
             }
             umma_commit(empty_bar(rp.st));
+            if (kI8) umma_commit(wempty_bar(wslot));
           }
           rp.advance(S);
+          ++wj;
         }
         if (!dead) umma_commit(accf_bar(buf));
         ++seg;
       });
     }
+    if (KSC > 1) {
+      __syncwarp();
+      dense_cluster_sync();
+      dense_cluster_sync();
+    }
+  } else if (kI8 && warp >= kDenseConvWarp0) {
+    // ---------------------------------------------------------- int8 dequantisation
+    // Stage layout of the codes: [128 rows][128 B], 16-byte chunk c of row r
+    // at physical chunk c ^ (r & 7).  A warp reads 4 rows x 8 chunks (512
+    // contiguous bytes) per step; lane (row r, physical chunk p) converts the
+    // 16 codes of logical chunk c = p ^ (r & 7) -- elements 16c .. 16c+15 of
+    // the stage's K range -- to fp16, scales them by their group's scale and
+    // writes them into the 128-byte-swizzled fp16 atoms of W tile j % 2 (atom
+    // c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1) once the MMAs of chunk j - 2
+    // have released it.  Each lane sees the same 8 rows in every stage; their
+    // scales are loaded one stage ahead.
+    const int cw = warp - kDenseConvWarp0;
+    const uint32_t p = (uint32_t)(lane & 7);
+    const int qshift = 31 - __clz(a.qgroup);
+    const int G = a.K >> qshift;  // scale groups per weight row
+    DRing rp;
+    int wj = 0;
+    bool dead = false;
+    dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int) {
+      const int sl = u / P.tiles, t = u - sl * P.tiles;
+      const __half* srow = a.Wscale + (size_t)((t / tok_tiles) * 128) * G;
+      auto load_scales = [&](int kc, uint32_t (&sc)[8]) {
+        const int k0 = (sl * P.C + kc) * KC;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = it * 16 + cw * 4 + (lane >> 3);
+          const uint32_t c = p ^ (uint32_t)(r & 7);
+          const __half sv = srow[(size_t)r * G + ((k0 + 16 * (int)c) >> qshift)];
+          const __half2 s2 = __halves2half2(sv, sv);
+          sc[it] = *reinterpret_cast<const uint32_t*>(&s2);
+        }
+      };
+      uint32_t sc[8], scn[8];
+      load_scales(kc0, sc);
+      for (int kc = kc0; kc < kc1; ++kc) {
+        if (kc + 1 < kc1) load_scales(kc + 1, scn);
+        const int wslot = wj & 1;
+        if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);
+        if (!dead) dead = !mbar_wait(wempty_bar(wslot), (uint32_t)(((wj >> 1) & 1) ^ 1), a.status);
+        const uint32_t w8 = smem_u32(sm + (size_t)rp.st * SB);
+        const uint32_t wt = wtile + (uint32_t)(wslot * WB);
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int r = it * 16 + cw * 4 + (lane >> 3);
+          const uint32_t x = (uint32_t)(r & 7), c = p ^ x;
+          const uint4 v = lds_u128(w8 + (uint32_t)r * 128u + p * 16u);
+          uint32_t h[8];
+          i8x4_to_half2x2(v.x, h[0], h[1]);
+          i8x4_to_half2x2(v.y, h[2], h[3]);
+          i8x4_to_half2x2(v.z, h[4], h[5]);
+          i8x4_to_half2x2(v.w, h[6], h[7]);
+          const __half2 s2 = *reinterpret_cast<const __half2*>(&sc[it]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const __half2 y = __hmul2(*reinterpret_cast<const __half2*>(&h[j]), s2);
+            h[j] = *reinterpret_cast<const uint32_t*>(&y);
+          }
+          const uint32_t row = wt + (c >> 2) * (128u * 128u) + (uint32_t)r * 128u;
+          const uint32_t j0 = (c & 3u) * 2u;
+          sts_u128(row + ((j0 ^ x) * 16u), make_uint4(h[0], h[1], h[2], h[3]));
+          sts_u128(row + (((j0 + 1u) ^ x) * 16u), make_uint4(h[4], h[5], h[6], h[7]));
+        }
+        // the fp16 tile is read by the tensor cores (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(wfull_bar(wslot));
+        rp.advance(S);
+        ++wj;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) sc[it] = scn[it];
+      }
+    });
     if (KSC > 1) {
       __syncwarp();
       dense_cluster_sync();

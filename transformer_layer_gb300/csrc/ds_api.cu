@@ -119,7 +119,8 @@ struct ds_layer {
   // int8 scale group length of matrix r (0 QKV, 1 O-proj, 2 FFN-up, 3 FFN-down):
   // the FFN matrices take half the length under mlp_extra_grouping.
   int qgroup(int r) const { return (r >= 2 && cfg.mlp_extra_grouping == 1) ? cfg.quant_group / 2 : cfg.quant_group; }
-  bool tile_capable() const { return cfg.weight_dtype != DS_I8; }
+  // tensor-core tiles: fp16 / bf16 weights, and int8 codes with fp16 activations
+  bool tile_capable() const { return cfg.weight_dtype != DS_I8 || cfg.act_dtype == DS_F16; }
   int max_rows() const { return tile_capable() ? kTileMaxRows : kGemvMaxRows; }
 };
 
@@ -140,10 +141,11 @@ bool make_plans(const ds_layer& L, int M, Plans* p) {
   if (M < 1 || M > L.max_rows()) return false;
   p->tile = use_tile_path(L, M);
   if (p->tile) {
-    return dense_make_plan(ak, 3 * H, H, M, L.sms, L.max_smem, &p->tq) &&
-           dense_make_plan(ak, H, H, M, L.sms, L.max_smem, &p->to) &&
-           dense_make_plan(ak, F, H, M, L.sms, L.max_smem, &p->tu) &&
-           dense_make_plan(ak, H, F, M, L.sms, L.max_smem, &p->td);
+    const bool i8 = wk == WKind::I8;
+    return dense_make_plan(ak, 3 * H, H, M, L.sms, L.max_smem, &p->tq, i8) &&
+           dense_make_plan(ak, H, H, M, L.sms, L.max_smem, &p->to, i8) &&
+           dense_make_plan(ak, F, H, M, L.sms, L.max_smem, &p->tu, i8) &&
+           dense_make_plan(ak, H, F, M, L.sms, L.max_smem, &p->td, i8);
   }
   if (!gemv_make_plan(wk, ak, 3 * H, H, M, L.sms, L.max_smem, &p->qkv)) return false;
   if (!gemv_make_plan(wk, ak, H, H, M, L.sms, L.max_smem, &p->o)) return false;
@@ -413,6 +415,8 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     if ((e = record_patch(rec, st, 0, p1, in_if(offsetof(LnPrepArgs, x_act)), {})) != cudaSuccess) return e;
     DenseArgs r1 = base;
     r1.tmap_w = L.tmap_tile(0, P.tq.kc);
+    r1.Wscale = static_cast<const __half*>(L.w.s_qkv);  // int8 only
+    r1.qgroup = L.qgroup(0);
     r1.N = 3 * H;
     r1.K = H;
     r1.plan = P.tq;
@@ -436,6 +440,8 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     // R3: O-proj + bias + residual + LayerNorm2 statistics
     DenseArgs r3 = base;
     r3.tmap_w = L.tmap_tile(1, P.to.kc);
+    r3.Wscale = static_cast<const __half*>(L.w.s_o);  // int8 only
+    r3.qgroup = L.qgroup(1);
     r3.N = H;
     r3.K = H;
     r3.plan = P.to;
@@ -463,6 +469,8 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     if ((e = launch_ln_prep(ak, p2, st, pdl)) != cudaSuccess) return e;
     DenseArgs r4 = base;
     r4.tmap_w = L.tmap_tile(2, P.tu.kc);
+    r4.Wscale = static_cast<const __half*>(L.w.s_fc1);  // int8 only
+    r4.qgroup = L.qgroup(2);
     r4.N = F;
     r4.K = H;
     r4.plan = P.tu;
@@ -475,6 +483,8 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     // R4b: FFN-down + bias + residual (+ next LayerNorm statistics)
     DenseArgs r5 = base;
     r5.tmap_w = L.tmap_tile(3, P.td.kc);
+    r5.Wscale = static_cast<const __half*>(L.w.s_fc2);  // int8 only
+    r5.qgroup = L.qgroup(3);
     r5.N = H;
     r5.K = F;
     r5.plan = P.td;
@@ -624,7 +634,8 @@ ds_status check_forward_args(const ds_layer& L, const void* x_in, const void* x_
   if (x_in == x_out) return fail(DS_ERR_INVALID_ARG, "x_out must not alias x_in");
   if (batch < 1 || T < 1 || (long long)batch * T > L.max_rows())
     return fail(DS_ERR_UNSUPPORTED, L.tile_capable() ? "batch * new_tokens must be in 1..4096"
-                                                     : "batch * new_tokens must be in 1..64 for int8 weights");
+                                                     : "batch * new_tokens must be in 1..64 for int8 weights with "
+                                                       "bf16 activations");
   if (!aligned16(kc) || !aligned16(vc))
     return fail(DS_ERR_INVALID_ARG, "KV caches must be non-null and 16-byte aligned");
   if (max_len < 1 || max_len < T) return fail(DS_ERR_INVALID_ARG, "max_len must be >= new_tokens");
@@ -681,11 +692,16 @@ ds_status make_tensor_maps(ds_layer* L) {
                             cols[r] / grp, 8 * nb * 64 / grp))
         return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a scale matrix");
     }
-    if (!i8) {
-      for (int j = 0; j < 2; ++j)
-        if (!encode_tile_map(host.data() + (size_t)(24 + 2 * r + j) * kTensorMapBytes, W[r], rows[r], cols[r], 128,
-                             j ? 128 : 64))
-          return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight tile map");
+    if (L->tile_capable()) {
+      // fp16 / bf16: ring stages of 64 and 128 along K; int8 codes (as pairs
+      // of 16-bit elements): stages of 128 codes, in both slots
+      for (int j = 0; j < 2; ++j) {
+        const bool ok = i8 ? encode_tile_map(host.data() + (size_t)(24 + 2 * r + j) * kTensorMapBytes, W[r], rows[r],
+                                             cols[r] / 2, 128, 64)
+                           : encode_tile_map(host.data() + (size_t)(24 + 2 * r + j) * kTensorMapBytes, W[r], rows[r],
+                                             cols[r], 128, j ? 128 : 64);
+        if (!ok) return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight tile map");
+      }
     }
   }
   int cur = 0;

@@ -114,10 +114,13 @@ struct DensePlan {
   size_t smem = 0;
   int cluster = 1;     // > 1: the K slices of each tile are one thread-block cluster of this many
                        // CTAs (one slice each) whose partial sums meet in distributed shared memory
+  int i8 = 0;          // 1: int8 weight codes (fp16 activations), dequantised to fp16 in shared memory
 };
 
 struct DenseArgs {
   const void* tmap_w = nullptr;    // device address of W's tile tensor map (box 128 rows x kc)
+  const __half* Wscale = nullptr;  // int8: fp16 scales [N][K / qgroup]
+  int qgroup = 64;                 // int8: scale group length along K (a power of two, >= 64)
   int N = 0, K = 0, M = 0, B = 1, T = 1;
   DensePlan plan;
   float* partials = nullptr;       // [tiles - U_dp][maxc][ntok][128] partial sums of the leftover tiles
@@ -189,7 +192,7 @@ cudaError_t prepare_region_kernels(int max_smem);
 
 // Tile path: plan (false if the shape has no tile split), launch, and the
 // row normalisation kernel.
-bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem, DensePlan* plan);
+bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem, DensePlan* plan, bool i8 = false);
 // Encodes the tile tensor map of a row-major [rows][cols] 16-bit matrix
 // (box 128 rows x kc, or ntok rows x kc for activation operands).
 bool encode_tile_map(void* map128, const void* base, int rows, int cols, int box_rows, int kc);
