@@ -41,8 +41,8 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   int ntok = (M + 15) / 16 * 16;
   // Token tiles of up to 128 rows; fp16 prompt chunks of 256 rows and more
   // take 256 (MMA N = 256: half the weight re-reads per FLOP; the bf16 hi/lo
-  // operand would leave too shallow a ring).  int8: up to 64 rows (its two
-  // fp16 W tiles take 64 KB beside the ring).
+  // operand would leave too shallow a ring).  int8: up to 64 rows (its fp16
+  // W tiles take 32 KB each beside the ring).
   const int ntok_max = i8 ? 64 : ((!split && M >= 256) ? 256 : 128);
   if (ntok > ntok_max) ntok = ntok_max;
   p.ntok = ntok;
@@ -74,7 +74,7 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   ws_distribute(w, num_sms, /*one_unit_each=*/true, /*force_whole=*/many);
   w.interleave = many ? 1 : 0;
   const size_t SB = (dense_stage_bytes(ntok, p.kc, split, i8) + 1023) & ~(size_t)1023;
-  const size_t fixed = 1024 + dense_wtile_bytes(p.kc, i8) + 8 * (2 * kDenseMaxStages + 10) + 16;
+  const size_t fixed = 1024 + dense_wtile_bytes(p.kc, i8) + 8 * (2 * kDenseMaxStages + 6 + 2 * kDenseWTiles) + 16;
   if ((size_t)max_smem < fixed + 2 * SB) return false;
   size_t s = ((size_t)max_smem - fixed) / SB;
   if (s > (size_t)kDenseMaxStages) s = kDenseMaxStages;

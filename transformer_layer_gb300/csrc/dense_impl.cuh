@@ -56,13 +56,14 @@
 namespace ds {
 
 constexpr int kDenseEpiWarps = 8;    // two per TMEM lane quarter, each taking half the columns
-constexpr int kDenseConvWarps = 4;   // int8 weights: warps that dequantise the codes to fp16
+constexpr int kDenseConvWarps = 8;   // int8 weights: warps that dequantise the codes to fp16
+constexpr int kDenseWTiles = 2;      // int8 weights: fp16 W tiles the converters fill ahead of the MMAs
 constexpr int kDenseThreads = (2 + kDenseEpiWarps) * 32;
 constexpr int kDenseThreadsI8 = (2 + kDenseEpiWarps + kDenseConvWarps) * 32;
 constexpr int kDenseTmaWarp = 0;
 constexpr int kDenseMmaWarp = 1;
 constexpr int kDenseEpiWarp0 = 2;    // warps 2 .. 9
-constexpr int kDenseConvWarp0 = 10;  // int8: warps 10 .. 13
+constexpr int kDenseConvWarp0 = 10;  // int8: warps 10 .. 10 + kDenseConvWarps - 1
 constexpr int kDenseEpiThreads = kDenseEpiWarps * 32;
 constexpr int kDenseBarEpi = 1;      // named barrier of the four epilogue warps
 constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
@@ -131,15 +132,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // (and, for bf16, X lo the same), each part on a 1024-byte boundary.  With
 // int8 weights a stage holds the TMA copy of the codes, [128 rows][KC bytes]
 // (KC = 128, 128-byte swizzle), then X; their fp16 dequantisation goes to one
-// of two W tiles after the ring, so the ring's depth (the bytes in flight)
-// does not pay for the fp16 tile.
+// of kDenseWTiles W tiles after the ring, so the ring's depth (the bytes in
+// flight) does not pay for the fp16 tiles.
 __host__ __device__ inline size_t dense_w_bytes(int kc) { return (size_t)128 * kc * 2; }
 __host__ __device__ inline size_t dense_x_bytes(int ntok, int kc) { return (size_t)ntok * kc * 2; }
 __host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split, bool i8 = false) {
   return (i8 ? (size_t)128 * kc : dense_w_bytes(kc)) + (split ? 2 : 1) * dense_x_bytes(ntok, kc);
 }
-// Shared memory after the ring: the int8 path's two fp16 W tiles.
-__host__ __device__ inline size_t dense_wtile_bytes(int kc, bool i8) { return i8 ? 2 * dense_w_bytes(kc) : 0; }
+// Shared memory after the ring: the int8 path's fp16 W tiles.
+__host__ __device__ inline size_t dense_wtile_bytes(int kc, bool i8) { return i8 ? kDenseWTiles * dense_w_bytes(kc) : 0; }
 __host__ __device__ inline uint32_t dense_tmem_cols(int ntok) {
   uint32_t c = 32;
   while (c < (uint32_t)(2 * ntok)) c <<= 1;
@@ -221,8 +222,8 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
   const uint32_t done_bar = smem_u32(bars + 2 * S + 5);  // epilogue warps done with TMEM
   // int8: fp16 W tile i written (converter warps) / read by the MMAs (commit)
   auto wfull_bar = [&](int i) { return smem_u32(bars + 2 * S + 6 + i); };
-  auto wempty_bar = [&](int i) { return smem_u32(bars + 2 * S + 8 + i); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 10);
+  auto wempty_bar = [&](int i) { return smem_u32(bars + 2 * S + 6 + kDenseWTiles + i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6 + 2 * kDenseWTiles);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const uint32_t tcols = dense_tmem_cols(NTOK);
 
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     mbar_init(fix_bar, 1);
     mbar_init(done_bar, kDenseEpiWarps);
     if (kI8)
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < kDenseWTiles; ++i) {
         mbar_init(wfull_bar(i), kDenseConvWarps);
         mbar_init(wempty_bar(i), 1);
       }
@@ -385,7 +386,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       const uint32_t idesc = umma_idesc(kSplit, NTOK);
       DRing rp;
       int seg = 0;
-      int wj = 0;  // int8: chunks so far (W tile wj % 2, its use wj / 2)
+      int wj = 0;  // int8: chunks so far (W tile wj % kDenseWTiles, its use wj / kDenseWTiles)
       bool dead = false;
       dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int) {
         (void)u;
@@ -395,8 +396,8 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         const uint32_t d = tmem + (uint32_t)(buf * NTOK);
         for (int kc = kc0; kc < kc1; ++kc) {
           // int8: the converter has waited for this stage and filled W tile wslot
-          const int wslot = wj & 1;
-          if (kI8 && !dead) dead = !mbar_wait(wfull_bar(wslot), (uint32_t)((wj >> 1) & 1), a.status);
+          const int wslot = wj % kDenseWTiles;
+          if (kI8 && !dead) dead = !mbar_wait(wfull_bar(wslot), (uint32_t)((wj / kDenseWTiles) & 1), a.status);
           if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);  // (int8: already complete)
           if (!dead) {
             tc_fence_after();
@@ -436,11 +437,12 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     // contiguous bytes) per step; lane (row r, physical chunk p) converts the
     // 16 codes of logical chunk c = p ^ (r & 7) -- elements 16c .. 16c+15 of
     // the stage's K range -- to fp16, scales them by their group's scale and
-    // writes them into the 128-byte-swizzled fp16 atoms of W tile j % 2 (atom
-    // c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1) once the MMAs of chunk j - 2
-    // have released it.  Each lane sees the same 8 rows in every stage; their
-    // scales are loaded one stage ahead.
+    // writes them into the 128-byte-swizzled fp16 atoms of W tile j % kDenseWTiles
+    // (atom c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1) once the MMAs of chunk
+    // j - kDenseWTiles have released it.  Each lane sees the same rows in
+    // every stage; their scales are loaded one stage ahead.
     const int cw = warp - kDenseConvWarp0;
+    constexpr int kConvIters = 128 / (4 * kDenseConvWarps);  // rows of the tile per lane and stage
     const uint32_t p = (uint32_t)(lane & 7);
     const int qshift = 31 - __clz(a.qgroup);
     const int G = a.K >> qshift;  // scale groups per weight row
@@ -450,29 +452,29 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int) {
       const int sl = u / P.tiles, t = u - sl * P.tiles;
       const __half* srow = a.Wscale + (size_t)((t / tok_tiles) * 128) * G;
-      auto load_scales = [&](int kc, uint32_t (&sc)[8]) {
+      auto load_scales = [&](int kc, uint32_t (&sc)[kConvIters]) {
         const int k0 = (sl * P.C + kc) * KC;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int r = it * 16 + cw * 4 + (lane >> 3);
+        for (int it = 0; it < kConvIters; ++it) {
+          const int r = it * (4 * kDenseConvWarps) + cw * 4 + (lane >> 3);
           const uint32_t c = p ^ (uint32_t)(r & 7);
           const __half sv = srow[(size_t)r * G + ((k0 + 16 * (int)c) >> qshift)];
           const __half2 s2 = __halves2half2(sv, sv);
           sc[it] = *reinterpret_cast<const uint32_t*>(&s2);
         }
       };
-      uint32_t sc[8], scn[8];
+      uint32_t sc[kConvIters], scn[kConvIters];
       load_scales(kc0, sc);
       for (int kc = kc0; kc < kc1; ++kc) {
         if (kc + 1 < kc1) load_scales(kc + 1, scn);
-        const int wslot = wj & 1;
+        const int wslot = wj % kDenseWTiles;
         if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);
-        if (!dead) dead = !mbar_wait(wempty_bar(wslot), (uint32_t)(((wj >> 1) & 1) ^ 1), a.status);
+        if (!dead) dead = !mbar_wait(wempty_bar(wslot), (uint32_t)(((wj / kDenseWTiles) & 1) ^ 1), a.status);
         const uint32_t w8 = smem_u32(sm + (size_t)rp.st * SB);
         const uint32_t wt = wtile + (uint32_t)(wslot * WB);
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int r = it * 16 + cw * 4 + (lane >> 3);
+        for (int it = 0; it < kConvIters; ++it) {
+          const int r = it * (4 * kDenseConvWarps) + cw * 4 + (lane >> 3);
           const uint32_t x = (uint32_t)(r & 7), c = p ^ x;
           const uint4 v = lds_u128(w8 + (uint32_t)r * 128u + p * 16u);
           uint32_t h[8];
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         rp.advance(S);
         ++wj;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) sc[it] = scn[it];
+        for (int it = 0; it < kConvIters; ++it) sc[it] = scn[it];
       }
     });
     if (KSC > 1) {
