@@ -39,9 +39,9 @@
  *     quant_group 128 and no extra MLP grouping).
  *   - Rows R = B*T (batch rows x new tokens) per call: 1..4096 with fp16 /
  *     bf16 weights and with int8 weights under fp16 activations; 1..64 with
- *     int8 weights under bf16 activations.  Up to 8 rows (and always for
+ *     int8 weights under bf16 activations.  Up to 7 rows (and always for
  *     int8 under bf16) the GEMMs run as streaming skinny-GEMM kernels with
- *     the LayerNorm fused into their prologue; above 8 rows as tensor-core
+ *     the LayerNorm fused into their prologue; from 8 rows as tensor-core
  *     tile kernels (tcgen05, accumulators in tensor memory), each LayerNorm
  *     then running as a small row kernel ahead of its GEMM (seven kernels
  *     per layer instead of five).  The int8 tile kernels dequantise each

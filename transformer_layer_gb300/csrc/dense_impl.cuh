@@ -1,6 +1,6 @@
 // Tensor-core tile path of the region GEMMs (tcgen05 + TMEM), for the batch
 // rows at which the skinny GEMM becomes a real dense contraction: decode at
-// B*T = 9..64 rows and multi-token (prompt) steps of up to a few thousand rows.
+// B*T = 8..64 rows and multi-token (prompt) steps of up to a few thousand rows.
 //
 // Page cited as [P1]: "DeepSpeed Inference 内核优化深度解析：多 GPU 自适应并行、
 // 算子融合推理内核与 MoQ 量化支持".

@@ -11,7 +11,7 @@
 // Two GEMM paths serve the regions (§3 intro: the skinny GEMM at small batch):
 //  * up to 8 rows (B * T), and for int8 weights up to 64, the streaming GEMV
 //    kernels (gemv_impl.cuh) with the LayerNorm fused into their prologue;
-//  * above 8 rows with fp16 / bf16 weights, the tensor-core tile kernels
+//  * from 8 rows (fp16 / bf16 weights, or int8 with fp16 activations), the tensor-core tile kernels
 //    (dense_impl.cuh, tcgen05 + TMEM), each LayerNorm run by a small row
 //    normalisation kernel that writes the tensor-core operand.
 //
@@ -52,7 +52,7 @@ ds_status cuda_fail(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr int kGemvMaxRows = 64;   // streaming GEMV kernels: up to 8 MMA column tiles
-constexpr int kTileMinRows = 9;    // fp16 / bf16 weights: tensor-core tiles from 9 rows
+constexpr int kTileMinRows = 8;    // tensor-core tiles from 8 rows (streaming kernels below)
 constexpr int kTileMaxRows = 4096; // rows (B * T) of one tile-path call
 
 struct DevInfo {
