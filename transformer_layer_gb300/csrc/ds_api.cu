@@ -284,20 +284,28 @@ Bufs bufs_of(void* ws, const WsLayout& w) {
 // row count: op_a with K = H, op_b with K = H (attention output) and K = F
 // (GeLU output); hi and (bf16) lo parts.
 struct alignas(64) XMaps {
-  unsigned char a_hi[kTensorMapBytes], a_lo[kTensorMapBytes];
-  unsigned char bh_hi[kTensorMapBytes], bh_lo[kTensorMapBytes];
-  unsigned char bf_hi[kTensorMapBytes], bf_lo[kTensorMapBytes];
+  unsigned char aq_hi[kTensorMapBytes], aq_lo[kTensorMapBytes];  // LN1 output, read by QKV
+  unsigned char au_hi[kTensorMapBytes], au_lo[kTensorMapBytes];  // LN2 output, read by FFN-up
+  unsigned char bh_hi[kTensorMapBytes], bh_lo[kTensorMapBytes];  // attention output, read by O-proj
+  unsigned char bf_hi[kTensorMapBytes], bf_lo[kTensorMapBytes];  // GeLU output, read by FFN-down
 };
 
+// Each map's box is its reader's token tile and ring stage (the four plans
+// may differ: a prompt chunk's QKV can take 128-row tiles where the others
+// take 256).
 bool make_xmaps(const ds_layer& L, const Plans& p, const Bufs& bf, int M, XMaps* x) {
-  const int H = L.cfg.hidden, F = L.cfg.ffn, nt = p.tq.ntok, kc = p.tq.kc;
+  const int H = L.cfg.hidden, F = L.cfg.ffn;
   const bool split = L.cfg.act_dtype == DS_BF16;
   std::memset(x, 0, sizeof(*x));
-  bool ok = encode_tile_map(x->a_hi, bf.op_a_hi, M, H, nt, kc) && encode_tile_map(x->bh_hi, bf.op_b_hi, M, H, nt, kc) &&
-            encode_tile_map(x->bf_hi, bf.op_b_hi, M, F, nt, kc);
+  bool ok = encode_tile_map(x->aq_hi, bf.op_a_hi, M, H, p.tq.ntok, p.tq.kc) &&
+            encode_tile_map(x->au_hi, bf.op_a_hi, M, H, p.tu.ntok, p.tu.kc) &&
+            encode_tile_map(x->bh_hi, bf.op_b_hi, M, H, p.to.ntok, p.to.kc) &&
+            encode_tile_map(x->bf_hi, bf.op_b_hi, M, F, p.td.ntok, p.td.kc);
   if (ok && split)
-    ok = encode_tile_map(x->a_lo, bf.op_a_lo, M, H, nt, kc) && encode_tile_map(x->bh_lo, bf.op_b_lo, M, H, nt, kc) &&
-         encode_tile_map(x->bf_lo, bf.op_b_lo, M, F, nt, kc);
+    ok = encode_tile_map(x->aq_lo, bf.op_a_lo, M, H, p.tq.ntok, p.tq.kc) &&
+         encode_tile_map(x->au_lo, bf.op_a_lo, M, H, p.tu.ntok, p.tu.kc) &&
+         encode_tile_map(x->bh_lo, bf.op_b_lo, M, H, p.to.ntok, p.to.kc) &&
+         encode_tile_map(x->bf_lo, bf.op_b_lo, M, F, p.td.ntok, p.td.kc);
   return ok;
 }
 
@@ -428,7 +436,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     r1.head_dim = d;
     r1.max_len = max_len;
     r1.past_len = past_len;
-    if ((e = launch_dense(Region::LnQkv, ak, r1, xm->a_hi, split ? xm->a_lo : nullptr, st, pdl)) != cudaSuccess)
+    if ((e = launch_dense(Region::LnQkv, ak, r1, xm->aq_hi, split ? xm->aq_lo : nullptr, st, pdl)) != cudaSuccess)
       return e;
     if ((e = record(es, st)) != cudaSuccess) return e;
     // R2: attention, output in the operand format
@@ -477,7 +485,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     r4.bias = L.w.b_fc1;
     r4.out_act = bf.op_b_hi;
     r4.out_lo = bf.op_b_lo;
-    if ((e = launch_dense(Region::FfnUp, ak, r4, xm->a_hi, split ? xm->a_lo : nullptr, st, pdl)) != cudaSuccess)
+    if ((e = launch_dense(Region::FfnUp, ak, r4, xm->au_hi, split ? xm->au_lo : nullptr, st, pdl)) != cudaSuccess)
       return e;
     if ((e = record(es, st)) != cudaSuccess) return e;
     // R4b: FFN-down + bias + residual (+ next LayerNorm statistics)
