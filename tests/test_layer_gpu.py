@@ -223,6 +223,22 @@ def test_prompt_chunk_layer_4096(act, B, T, past):
         L.close()
 
 
+@pytest.mark.parametrize("act", [torch.float16, torch.bfloat16])
+def test_prompt_chunk_many_tiles(act):
+    """A chunk with more output tiles than SMs in every GEMM (4 sequences x 512
+    new tokens, hidden 2048, FFN 8192: 384 to 1024 tiles), so that CTAs take
+    several whole tiles handed out round-robin; every output element and every
+    new cache row against the oracle."""
+    H, nh, F, B, T = 2048, 16, 8192, 4, 512
+    L = DeviceLayer(H, nh, F, seed=1014, act_dtype=act, weight_dtype=act)
+    try:
+        past = [0, 17, 100, 3]
+        res = run_layer(L, B, T, past, max_len=max(past) + T + 8, seed=18)
+        check_layer(L, res, B, T, past, f"many tiles {act}")
+    finally:
+        L.close()
+
+
 @pytest.mark.parametrize("B,T,group,extra", [(2, 24, 64, 0), (1, 256, 64, 0), (2, 100, 128, 1)])
 def test_prompt_chunk_int8(B, T, group, extra):
     """Prompt chunks with MoQ int8 weights (int8 tile kernels: 48 to 256 rows,

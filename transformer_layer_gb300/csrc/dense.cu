@@ -39,11 +39,11 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   p.i8 = i8 ? 1 : 0;
   p.row_tiles = N / 128;
   int ntok = (M + 15) / 16 * 16;
-  // Token tiles of up to 128 rows; fp16 prompt chunks of 256 rows and more
-  // take 256 (MMA N = 256: half the weight re-reads per FLOP; the bf16 hi/lo
-  // operand would leave too shallow a ring).  int8: up to 64 rows (its fp16
-  // W tiles take 32 KB each beside the ring).
-  const int ntok_max = i8 ? 64 : ((!split && M >= 256) ? 256 : 128);
+  // Token tiles of up to 128 rows; prompt chunks of 256 rows and more take
+  // 256 with fp16 (MMA N = 256: half the weight re-reads per FLOP) and 192
+  // with bf16 (its hi/lo operand: a 64 KB stage, three in the ring).  int8: up
+  // to 64 rows (its fp16 W tiles take 32 KB each beside the ring).
+  const int ntok_max = i8 ? 64 : (M >= 256 ? (split ? 192 : 256) : 128);
   if (ntok > ntok_max) ntok = ntok_max;
   p.ntok = ntok;
   p.tok_tiles = (M + ntok - 1) / ntok;
