@@ -395,6 +395,10 @@ DS_API ds_status ds_tp_finish(ds_tp_layer* layer, const float* y, void* x_out, i
 /* Device-side status flags recorded in the workspace. */
 #define DS_DEVFLAG_CACHE_OVERFLOW 0x1  /* past_len[b] + T > max_len for some row */
 #define DS_DEVFLAG_WAIT_TIMEOUT 0x2    /* an in-kernel pipeline wait gave up (outputs invalid) */
+#define DS_DEVFLAG_BOUNDS 0x4          /* diagnostic build only (DS_DEBUG_BOUNDS defined, i.e.
+                                        * libdslayer_debug_bounds.so): a kernel found an index
+                                        * outside its buffer and skipped the access (outputs
+                                        * invalid); normal builds compile the checks away */
 
 /* Copies the workspace status word to *flags_out, clears it, and synchronises
  * `stream`.  Returns DS_ERR_DEVICE when a flag was set, DS_OK otherwise. */

@@ -18,6 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdslayer.so")
+# Diagnostic variant: device-side bounds checks (DS_DEBUG_BOUNDS) that record
+# DS_DEVFLAG_BOUNDS in the workspace status word and skip the access.
+BUILD_DEBUG = os.path.join(PKG, "_build_debug_bounds")
+LIB_DEBUG = os.path.join(PKG, "libdslayer_debug_bounds.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
@@ -40,23 +44,27 @@ def _inputs():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compiles and links libdslayer.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug_bounds: bool = False) -> str:
+    """Compiles and links libdslayer.so (or, with debug_bounds, the diagnostic
+    libdslayer_debug_bounds.so); returns its path."""
+    lib = LIB_DEBUG if debug_bounds else LIB
+    bdir = BUILD_DEBUG if debug_bounds else BUILD
+    flags = [*extra_flags, *(["-DDS_DEBUG_BOUNDS"] if debug_bounds else [])]
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -67,15 +75,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug_bounds="--debug-bounds" in sys.argv))

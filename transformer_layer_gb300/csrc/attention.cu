@@ -192,7 +192,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
 
   for (int t = 0; t < a.T; ++t) {
     const int St = min(past + t + 1, S_all);
-    const int n_keys = max(0, min(hi, St) - lo);
+    int n_keys = max(0, min(hi, St) - lo);
+    if (!ds_in_bounds(lo + n_keys <= a.max_len && b < a.B && h < a.heads, a.status)) n_keys = 0;
     float qv[8];
     {
       const float* qp = a.q + (size_t)(b * a.T + t) * a.H + h * D + kq * 8;
@@ -250,7 +251,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
       }
       const float o = O / L;
       const size_t oi = (size_t)(b * a.T + t) * a.H + h * D + tid;
-      if (a.out_hi != nullptr) {  // tensor-core operand: hi (and lo for bf16)
+      if (!ds_in_bounds(oi < (size_t)a.B * a.T * a.H, a.status)) {
+        // (debug builds: an output index outside the buffer; skipped)
+      } else if (a.out_hi != nullptr) {  // tensor-core operand: hi (and lo for bf16)
         const ACT hv = Act<ACT>::from_f(o);
         static_cast<ACT*>(a.out_hi)[oi] = hv;
         if (a.out_lo != nullptr) static_cast<ACT*>(a.out_lo)[oi] = Act<ACT>::from_f(o - Act<ACT>::to_f(hv));

@@ -64,6 +64,20 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) 
 // Device status flags (mirrored in ds_layer.h).
 constexpr unsigned kFlagCacheOverflow = 0x1u;
 constexpr unsigned kFlagWaitTimeout = 0x2u;
+constexpr unsigned kFlagBounds = 0x4u;  // debug builds: an index outside its buffer (the access skipped)
+
+// Device-side bounds checks of a library built with DS_DEBUG_BOUNDS: a
+// failed check records kFlagBounds in the status word and the caller skips
+// the access (never a trap).  In normal builds the check is `true` and
+// compiles away.
+#if defined(DS_DEBUG_BOUNDS)
+__device__ __forceinline__ bool ds_in_bounds(bool ok, unsigned* status) {
+  if (!ok && status != nullptr) atomicOr(status, kFlagBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool ds_in_bounds(bool, unsigned*) { return true; }
+#endif
 // Wall-clock budget of one in-kernel wait (ns).  A wait that runs out records
 // kFlagWaitTimeout and returns, so a broken pipeline ends the kernel with a
 // status flag instead of hanging the GPU.

@@ -584,8 +584,8 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int mi = c8 + i;  // column within the tile
-        const bool ok = mi < c.mrows;
         const int m = c.m0 + mi;
+        const bool ok = mi < c.mrows && ds_in_bounds(m < M && c.n < N, a.status);
         float y = (v[i] + c.bias) * c.scale;
         if constexpr (R == Region::LnQkv) {
           if (ok) {
@@ -594,8 +594,10 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
             } else {
               const int b = a.T == 1 ? m : m / a.T;
               const int pos = __float_as_int(op[i]);
-              if (pos >= 0 && pos < a.max_len)
-                c.dst[((size_t)b * a.heads * a.max_len + pos) * a.head_dim] = Act<ACT>::from_f(y);
+              if (pos >= 0 && pos < a.max_len) {
+                if (ds_in_bounds(b < a.B && c.n < 3 * a.H, a.status))
+                  c.dst[((size_t)b * a.heads * a.max_len + pos) * a.head_dim] = Act<ACT>::from_f(y);
+              }
               else
                 atomicOr(a.status, kFlagCacheOverflow);
             }

@@ -728,6 +728,7 @@ __device__ void gemv_epi_phase(const RegionArgs& a, const GemvPlan& P, const Gem
 
   auto epilogue = [&](int n, int m, float acc, const EpiOp& op) -> float {
     float v = acc + op.bias;
+    if (!ds_in_bounds(m < a.M && n < N, a.status)) return v;
     if constexpr (R == Region::LnQkv) {
       const int H = a.H;
       const int part = n / H;
@@ -740,7 +741,8 @@ __device__ void gemv_epi_phase(const RegionArgs& a, const GemvPlan& P, const Gem
         if (pos >= 0 && pos < a.max_len) {
           const int head = within / a.head_dim, dim = within - head * a.head_dim;
           ACT* cache = static_cast<ACT*>(part == 1 ? a.k_cache : a.v_cache);
-          cache[(((size_t)b * a.heads + head) * a.max_len + pos) * a.head_dim + dim] = Act<ACT>::from_f(v);
+          if (ds_in_bounds(b < a.B && head < a.heads, a.status))
+            cache[(((size_t)b * a.heads + head) * a.max_len + pos) * a.head_dim + dim] = Act<ACT>::from_f(v);
         } else {
           atomicOr(a.status, 1u);
         }

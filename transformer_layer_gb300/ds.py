@@ -13,11 +13,13 @@ import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdslayer.so")
+LIB_DEBUG_BOUNDS_PATH = os.path.join(_PKG, "libdslayer_debug_bounds.so")  # diagnostic build
 
 DS_OK, DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED, DS_ERR_CUDA, DS_ERR_WORKSPACE, DS_ERR_DEVICE = range(6)
 DS_F16, DS_BF16, DS_I8 = 0, 1, 2
 DS_DEVFLAG_CACHE_OVERFLOW = 0x1
 DS_DEVFLAG_WAIT_TIMEOUT = 0x2
+DS_DEVFLAG_BOUNDS = 0x4
 
 # Every exported symbol of include/ds_layer.h, with (restype, argtypes).
 _vp = C.c_void_p
