@@ -33,16 +33,21 @@
 //  * Warps 2..9 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
 //    32 (w % 4) ..: one weight row per thread; the two warps of a lane
 //    quarter take alternate groups of 8 token columns) and run the region
-//    epilogue, or publish a split-K partial; the last CTA to contribute to a
-//    tile (acquire-release counter, nothing waits) stages the partials in its
-//    idle ring with bulk copies, sums them in fixed order and runs the
-//    epilogue, so results are deterministic.
+//    epilogue.  When the K slices of a tile run as one cluster (one slice
+//    per CTA) their partial tiles are summed through distributed shared
+//    memory; otherwise a shared tile's partials go through global memory and
+//    its last contributor (acquire-release counter, nothing waits) stages them
+//    in its idle ring with bulk copies and sums them in fixed order.  Results
+//    are deterministic either way.
+//  * int8 weights: warps 10..17 dequantise each stage's codes to fp16 before
+//    its MMAs (see the converter role below).
 //  * Work split (work_split.h): a unit is one output tile x one K slice,
 //    chunks are KC-wide K ranges.  With at least ~60 % as many tiles as SMs
 //    each CTA takes one whole tile (no split-K); with fewer (N = 4096 at
-//    decode) each tile is cut into K slices, one per CTA; with more (long
-//    prompts) CTAs own whole tiles and/or an even share of the leftover
-//    tiles' chunks.
+//    decode) each tile is cut into K slices, one per CTA, a cluster per tile;
+//    with more, CTAs own whole tiles (round-robin when several token tiles
+//    share the weights) and, at decode, an even share of the leftover tiles'
+//    chunks.
 #pragma once
 
 #include <cuda.h>
@@ -65,7 +70,7 @@ constexpr int kDenseMmaWarp = 1;
 constexpr int kDenseEpiWarp0 = 2;    // warps 2 .. 9
 constexpr int kDenseConvWarp0 = 10;  // int8: warps 10 .. 10 + kDenseConvWarps - 1
 constexpr int kDenseEpiThreads = kDenseEpiWarps * 32;
-constexpr int kDenseBarEpi = 1;      // named barrier of the four epilogue warps
+constexpr int kDenseBarEpi = 1;      // named barrier of the eight epilogue warps
 constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
 constexpr int kL2Ahead = 8;            // weight chunks requested into L2 ahead of the ring
 
@@ -913,7 +918,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(done_bar);
   }
-  // Warp 1 frees the tensor memory once the four epilogue warps are done with
+  // Warp 1 frees the tensor memory once the eight epilogue warps are done with
   // it (an mbarrier, not a CTA barrier: the roles reach the end on different
   // paths).
   if (warp == kDenseMmaWarp) {
