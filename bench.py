@@ -340,6 +340,15 @@ def load_tensor_peak():
         return 1900.0, 1700.0, "fallback"
 
 
+def check_device(ws, stream, what):
+    """A run in which a device-side check fired (a bounded wait that gave up,
+    a bounds or cache check) produced no valid result: stop without a line."""
+    from transformer_layer_gb300 import ds
+    code, flags = ds.ds_workspace_status(ws, stream)
+    if flags != 0:
+        raise SystemExit(f"bench: device status flags 0x{flags:x} after {what} (code {code}): no result reported")
+
+
 def run_prefill(args, torch, dist, world, rank, local, dev):
     """--prefill T: one step = a prompt chunk of T new tokens per sequence
     through the 7B-shaped stack (ds_stack_forward; cache empty)."""
@@ -392,6 +401,7 @@ def run_prefill(args, torch, dist, world, rank, local, dev):
         dist.barrier()
     clocks = sampler.stop()
     launches = ds.ds_launch_count() - launches0
+    check_device(ws, stream, "the timed prompt chunks")
     ms_max = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     value = job_throughput(B * T, args.steps, world, ms_max / 1000.0)
     # end to end: prompt from pinned host memory, result back, synchronised
@@ -409,6 +419,7 @@ def run_prefill(args, torch, dist, world, rank, local, dev):
             yh.copy_(out, non_blocking=True)
         stream.synchronize()
     e2e_value = job_throughput(B * T, e2e_steps, world, max_over_ranks(time.perf_counter() - t0, world, dev))
+    check_device(ws, stream, "the end-to-end prompt chunks")
     # region kernels alone (profile mode)
     ds.ds_stack_set_profiling(stack, True)
     ds.ds_stack_region_times(stack)
@@ -417,6 +428,7 @@ def run_prefill(args, torch, dist, world, rank, local, dev):
             step(i)
     us, _ = ds.ds_stack_region_times(stack)
     ds.ds_stack_set_profiling(stack, False)
+    check_device(ws, stream, "the profiled prompt chunks")
     reg, total = prefill_flops(H, F, nh, L, B, T)
     burst, sustained, kind = load_tensor_peak()
     shares = {r: us[i] for i, r in enumerate(REGIONS)}
@@ -564,6 +576,7 @@ def main():
     clocks = sampler.stop()
     launches = ds.ds_launch_count() - launches0
     ms = ev0.elapsed_time(ev1)
+    check_device(ws, stream, "the timed decode steps")
     # host cost of one ds_stack_decode_step call (graph replay; the inputs
     # rotate over 8 buffers, so the graph's x_in node is updated each call)
     host_us = []
@@ -595,6 +608,7 @@ def main():
                                 stream)
     e2e_s = time.perf_counter() - t0
     e2e_value = job_throughput(B, e2e_steps, world, max_over_ranks(e2e_s, world, dev))
+    check_device(ws, stream, "the end-to-end decode steps")
 
     # ---- per-region kernel times (profile mode: no graph, no PDL; each kernel alone)
     ds.ds_stack_set_profiling(stack, True)
@@ -606,6 +620,7 @@ def main():
             step(i + 1)   # avoid the seq reset at i % 64 == 0 on the first profiled step
     us, counts = ds.ds_stack_region_times(stack)
     ds.ds_stack_set_profiling(stack, False)
+    check_device(ws, stream, "the profiled decode steps")
 
     peak, peak_kind = load_peak()
     rbytes = region_bytes(H, F, B, past, wbytes)

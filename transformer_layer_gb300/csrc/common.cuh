@@ -265,6 +265,11 @@ __device__ __forceinline__ void i8x4_to_bf162x2(uint32_t w, uint32_t& lo, uint32
 }
 
 // Shared-memory load / store at a 32-bit shared-window address.
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint4 lds_u128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));

@@ -39,8 +39,10 @@
 //    its last contributor (acquire-release counter, nothing waits) stages them
 //    in its idle ring with bulk copies and sums them in fixed order.  Results
 //    are deterministic either way.
-//  * int8 weights: warps 10..17 dequantise each stage's codes to fp16 before
-//    its MMAs (see the converter role below).
+//  * int8 weights: warps 10..17 dequantise each stage's codes to fp16 straight
+//    into tensor memory (tcgen05.st), where the MMAs read them as the A
+//    operand: the fp16 weights never pass through shared memory (see the
+//    converter role below).
 //  * Work split (work_split.h): a unit is one output tile x one K slice,
 //    chunks are KC-wide K ranges.  With at least ~60 % as many tiles as SMs
 //    each CTA takes one whole tile (no split-K); with fewer (N = 4096 at
@@ -62,13 +64,15 @@ namespace ds {
 
 constexpr int kDenseEpiWarps = 8;    // two per TMEM lane quarter, each taking half the columns
 constexpr int kDenseConvWarps = 8;   // int8 weights: warps that dequantise the codes to fp16
-constexpr int kDenseWTiles = 2;      // int8 weights: fp16 W tiles the converters fill ahead of the MMAs
+constexpr int kDenseWTiles = 2;      // int8 weights: fp16 W tiles (in TMEM) the converters fill ahead of the MMAs
+constexpr int kDenseWTileCols = 64;  // TMEM columns of one fp16 W tile: 128 rows x 128 codes of K
 constexpr int kDenseThreads = (2 + kDenseEpiWarps) * 32;
-constexpr int kDenseThreadsI8 = (2 + kDenseEpiWarps + kDenseConvWarps) * 32;
+constexpr int kDenseThreadsI8 = (3 + kDenseEpiWarps + kDenseConvWarps) * 32;
 constexpr int kDenseTmaWarp = 0;
 constexpr int kDenseMmaWarp = 1;
 constexpr int kDenseEpiWarp0 = 2;    // warps 2 .. 9
 constexpr int kDenseConvWarp0 = 10;  // int8: warps 10 .. 10 + kDenseConvWarps - 1
+constexpr int kDenseMma2Warp = kDenseConvWarp0 + kDenseConvWarps;  // int8: the second MMA issuer
 constexpr int kDenseEpiThreads = kDenseEpiWarps * 32;
 constexpr int kDenseBarEpi = 1;      // named barrier of the eight epilogue warps
 constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
@@ -94,6 +98,16 @@ __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t da, uint64_t 
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(da), "l"(db), "r"(idesc), "r"(acc));
 }
+// The same with A (M = 128 rows x K = 16, one row per TMEM lane, two 16-bit
+// elements per 32-bit column, the lower K index in the low half) read from
+// tensor memory at column address tmem_a.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t db, uint32_t idesc,
+                                                uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(db), "r"(idesc), "r"(acc));
+}
 // Arrives on `bar` once every tcgen05.mma issued so far by this thread is complete.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -109,6 +123,19 @@ __device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr, uint32_t ncols) 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
+// Stores 32 consecutive 32-bit columns of this thread's TMEM lane (the warp
+// writes its lane quarter); tmem_wait_st waits until they have landed.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // 8 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
@@ -136,19 +163,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 // One ring stage: W [KC/64 atoms][128 rows][128 B], then X [KC/64][NTOK][128 B]
 // (and, for bf16, X lo the same), each part on a 1024-byte boundary.  With
 // int8 weights a stage holds the TMA copy of the codes, [128 rows][KC bytes]
-// (KC = 128, 128-byte swizzle), then X; their fp16 dequantisation goes to one
-// of kDenseWTiles W tiles after the ring, so the ring's depth (the bytes in
-// flight) does not pay for the fp16 tiles.
+// (KC = 128, 128-byte swizzle), then X, then the scales of the stage's rows:
+// the aligned block of 8 groups along K that holds the stage's groups,
+// [128 rows][8 fp16] (a TMA box is at least 16 bytes wide).  The codes' fp16
+// dequantisation goes to one of kDenseWTiles W tiles in tensor memory, the
+// MMAs' A operand, so it costs neither ring depth nor shared-memory traffic.
+constexpr int kDenseScaleGroups = 8;  // int8: scale groups per row in a stage's scale box
 __host__ __device__ inline size_t dense_w_bytes(int kc) { return (size_t)128 * kc * 2; }
 __host__ __device__ inline size_t dense_x_bytes(int ntok, int kc) { return (size_t)ntok * kc * 2; }
+__host__ __device__ inline size_t dense_scale_bytes(bool i8) { return i8 ? (size_t)128 * kDenseScaleGroups * 2 : 0; }
 __host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split, bool i8 = false) {
-  return (i8 ? (size_t)128 * kc : dense_w_bytes(kc)) + (split ? 2 : 1) * dense_x_bytes(ntok, kc);
+  return (i8 ? (size_t)128 * kc : dense_w_bytes(kc)) + (split ? 2 : 1) * dense_x_bytes(ntok, kc) + dense_scale_bytes(i8);
 }
-// Shared memory after the ring: the int8 path's fp16 W tiles.
-__host__ __device__ inline size_t dense_wtile_bytes(int kc, bool i8) { return i8 ? kDenseWTiles * dense_w_bytes(kc) : 0; }
-__host__ __device__ inline uint32_t dense_tmem_cols(int ntok) {
+// Tensor memory columns: the two accumulators of NTOK columns (int8: two
+// per MMA issuer), then (int8) the fp16 W tiles; an allocation is a power of
+// two of at least 32.
+__host__ __device__ inline uint32_t dense_tmem_cols(int ntok, bool i8) {
+  const uint32_t need = (uint32_t)((i8 ? 4 : 2) * ntok) + (i8 ? (uint32_t)(kDenseWTiles * kDenseWTileCols) : 0u);
   uint32_t c = 32;
-  while (c < (uint32_t)(2 * ntok)) c <<= 1;
+  while (c < need) c <<= 1;
   return c;
 }
 
@@ -216,8 +249,8 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
   const size_t WB = dense_w_bytes(KC), XB = dense_x_bytes(NTOK, KC);
   const size_t SB = (dense_stage_bytes(NTOK, KC, kSplit, kI8) + 1023) & ~(size_t)1023;
   const uint32_t XOFF = kI8 ? (uint32_t)(128 * KC) : (uint32_t)WB;  // X within a stage
-  const uint32_t wtile = smem_u32(sm + (size_t)S * SB);             // int8: the two fp16 W tiles
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)S * SB + dense_wtile_bytes(KC, kI8));
+  const uint32_t SOFF = XOFF + (uint32_t)XB;                         // int8: the scale box within a stage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)S * SB);
   // full[S], empty[S], acc_full[2], acc_empty[2]
   auto full_bar = [&](int i) { return smem_u32(bars + i); };
   auto empty_bar = [&](int i) { return smem_u32(bars + S + i); };
@@ -230,13 +263,14 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
   auto wempty_bar = [&](int i) { return smem_u32(bars + 2 * S + 6 + kDenseWTiles + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6 + 2 * kDenseWTiles);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  const uint32_t tcols = dense_tmem_cols(NTOK);
+  const uint32_t tcols = dense_tmem_cols(NTOK, kI8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 32) {  // the descriptors' first use is the TMA warp's first copy
     if (a.sel_idx == nullptr) asm volatile("prefetch.tensormap [%0];" ::"l"(a.tmap_w) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap_hi) : "memory");
     if (kSplit) asm volatile("prefetch.tensormap [%0];" ::"l"(&xmap_lo) : "memory");
+    if (kI8) asm volatile("prefetch.tensormap [%0];" ::"l"(a.tmap_s) : "memory");
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -244,7 +278,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       mbar_init(empty_bar(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(accf_bar(i), 1);
+      mbar_init(accf_bar(i), kI8 ? 2 : 1);  // int8: one commit per MMA issuer
       mbar_init(acce_bar(i), kDenseEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(fix_bar, 1);
@@ -283,10 +317,19 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       // weights read once: evict first; read again by other token tiles: keep
       const uint64_t pol_w = tok_tiles > 1 ? l2_evict_normal_policy() : l2_evict_first_policy();
       const uint64_t pol_x = l2_evict_normal_policy();
-      const uint32_t tx = (uint32_t)((kI8 ? (size_t)128 * KC : WB) + (kSplit ? 2 : 1) * XB);
+      const uint32_t tx = (uint32_t)((kI8 ? (size_t)128 * KC : WB) + (kSplit ? 2 : 1) * XB + dense_scale_bytes(kI8));
+      const int qshift = kI8 ? 31 - __clz(a.qgroup) : 0;
       const uint32_t woff = 0u;                                    // where W's copy lands
       auto wk_of = [&](const Cursor& c) {                          // W's K coordinate (128-byte atoms)
         return (c.s * P.C + c.kc) * (kI8 ? KC / 128 : KC / 64);
+      };
+      // int8: the stage's scale box, the aligned 8 groups holding its first
+      // (K is a multiple of 8 groups, so the box never leaves the matrix)
+      auto load_scales = [&](uint32_t stage, const Cursor& c, int trow, uint32_t bar) {
+        if constexpr (kI8) {
+          const int g0 = (((c.s * P.C + c.kc) * KC) >> qshift) & ~(kDenseScaleGroups - 1);
+          tma_load_2d(stage + SOFF, a.tmap_s, g0, trow * 128, bar, pol_x);
+        }
       };
       long long ra, rb;
       ws_left_range(P, vcta, gridDim.x, &ra, &rb);
@@ -306,6 +349,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         const int trow = q.t / tok_tiles;
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
         tma_load_3d(stage + woff, tmap_w, 0, trow * 128, wk_of(q), full_bar(rp.st), pol_w);
+        load_scales(stage, q, trow, full_bar(rp.st));
         last_ph[rp.st] = rp.ph;
         issued |= 1u << rp.st;
         ws_cursor_next(q, P, dp_b);
@@ -349,6 +393,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         const int kseg = (q.s * P.C + q.kc) * (KC / 64);
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
         tma_load_3d(stage + woff, tmap_w, 0, trow * 128, wk_of(q), full_bar(rp.st), pol_w);
+        load_scales(stage, q, trow, full_bar(rp.st));
         tma_load_3d(stage + XOFF, &xmap_hi, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
         if constexpr (kSplit)
           tma_load_3d(stage + XOFF + (uint32_t)XB, &xmap_lo, 0, jt * NTOK, kseg, full_bar(rp.st), pol_x);
@@ -384,9 +429,19 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       dense_cluster_sync();
       dense_cluster_sync();
     }
-  } else if (warp == kDenseMmaWarp) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == kDenseMmaWarp || (kI8 && warp == kDenseMma2Warp)) {
+    // ---------------------------------------------------------- MMA issuer(s)
+    // One thread issues a tcgen05.mma about every 50 cycles at best, whatever
+    // NTOK: at int8's 16 KB of weights per chunk that is the chunk's cost, so
+    // int8 runs two issuers.  Issuer me takes the CTA's chunks j with
+    // j % 2 == me -- exactly those of W tile me, so it observes every phase of
+    // that tile's barriers in order (a waiter that skipped a phase would take
+    // an older completion for the one it waits for) -- into its own
+    // accumulator pair (columns 2 NTOK me ..); the epilogue adds the two.
     pdl_launch_dependents();
+    const int me = warp == kDenseMmaWarp ? 0 : 1;
+    constexpr int kIssuers = kI8 ? 2 : 1;
+    static_assert(!kI8 || kDenseWTiles == kIssuers, "int8: issuer i owns W tile i");
     if (lane == 0) {
       const uint32_t idesc = umma_idesc(kSplit, NTOK);
       DRing rp;
@@ -398,30 +453,46 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         const int buf = seg & 1;
         if (seg >= 2 && !dead) dead = !mbar_wait(acce_bar(buf), ((seg >> 1) - 1) & 1, a.status);
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * NTOK);
+        const uint32_t d = tmem + (uint32_t)((2 * me + buf) * NTOK);
+        bool first = true;  // this issuer's first chunk of the tile: overwrite the accumulator
         for (int kc = kc0; kc < kc1; ++kc) {
-          // int8: the converter has waited for this stage and filled W tile wslot
           const int wslot = wj % kDenseWTiles;
-          if (kI8 && !dead) dead = !mbar_wait(wfull_bar(wslot), (uint32_t)((wj / kDenseWTiles) & 1), a.status);
-          if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);  // (int8: already complete)
-          if (!dead) {
-            tc_fence_after();
-            const uint32_t sbase = smem_u32(sm + (size_t)rp.st * SB);
-            const uint32_t wbase = kI8 ? wtile + (uint32_t)(wslot * WB) : sbase;
-            const uint32_t xbase = sbase + XOFF;
+          if (wj % kIssuers == me) {
+            // int8: the converters have waited for this stage and filled W tile wslot
+            if (kI8 && !dead) dead = !mbar_wait(wfull_bar(wslot), (uint32_t)((wj / kDenseWTiles) & 1), a.status);
+            if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);  // (int8: already complete)
+            if (!dead) {
+              tc_fence_after();
+              // Descriptors built once per chunk and advanced by their address
+              // field (16-byte units; a stage never crosses the field's range):
+              // per-MMA operand arithmetic would add to the issue time.
+              const uint32_t sbase = smem_u32(sm + (size_t)rp.st * SB);
+              const uint64_t xd0 = umma_desc_sw128(sbase + XOFF);
+              const uint64_t wd0 = umma_desc_sw128(sbase);
+              const uint32_t acc0 = first ? 0u : 1u;
+              // int8: W tile wslot in tensor memory, 8 columns per K step of 16
+              const uint32_t wcol = tmem + (uint32_t)(4 * NTOK + wslot * kDenseWTileCols);
 #pragma unroll 1
-            for (int kb = 0; kb < KC / 64; ++kb) {
+              for (int kb = 0; kb < KC / 64; ++kb) {
+                const uint64_t xk = xd0 + (uint64_t)(kb * NTOK * 8);  // NTOK rows of 128 B per 64 K
+                const uint64_t wk = wd0 + (uint64_t)(kb * 1024);      // 128 rows of 128 B per 64 K
 #pragma unroll
-              for (int k16 = 0; k16 < 4; ++k16) {
-                const uint64_t dw = umma_desc_sw128(wbase + kb * (128 * 128) + k16 * 32);
-                const uint32_t xo = (uint32_t)(kb * NTOK * 128 + k16 * 32);
-                const uint32_t acc = (kc > kc0 || kb > 0 || k16 > 0) ? 1u : 0u;
-                umma_f16(d, dw, umma_desc_sw128(xbase + xo), idesc, acc);
-                if constexpr (kSplit) umma_f16(d, dw, umma_desc_sw128(xbase + (uint32_t)XB + xo), idesc, 1u);
+                for (int k16 = 0; k16 < 4; ++k16) {
+                  const uint32_t acc = (kb > 0 || k16 > 0) ? 1u : acc0;
+                  const uint64_t xd = xk + (uint64_t)(2 * k16);      // 32 bytes per K step of 16
+                  if constexpr (kI8) {
+                    umma_f16_tmem_a(d, wcol + (uint32_t)(8 * (4 * kb + k16)), xd, idesc, acc);
+                  } else {
+                    const uint64_t dw = wk + (uint64_t)(2 * k16);
+                    umma_f16(d, dw, xd, idesc, acc);
+                    if constexpr (kSplit) umma_f16(d, dw, xd + (uint64_t)(XB >> 4), idesc, 1u);
+                  }
+                }
               }
+              umma_commit(empty_bar(rp.st));
+              if (kI8) umma_commit(wempty_bar(wslot));
             }
-            umma_commit(empty_bar(rp.st));
-            if (kI8) umma_commit(wempty_bar(wslot));
+            first = false;
           }
           rp.advance(S);
           ++wj;
@@ -435,77 +506,67 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       dense_cluster_sync();
       dense_cluster_sync();
     }
-  } else if (kI8 && warp >= kDenseConvWarp0) {
+  } else if (kI8 && warp >= kDenseConvWarp0 && warp < kDenseConvWarp0 + kDenseConvWarps) {
     // ---------------------------------------------------------- int8 dequantisation
-    // Stage layout of the codes: [128 rows][128 B], 16-byte chunk c of row r
-    // at physical chunk c ^ (r & 7).  A warp reads 4 rows x 8 chunks (512
-    // contiguous bytes) per step; lane (row r, physical chunk p) converts the
-    // 16 codes of logical chunk c = p ^ (r & 7) -- elements 16c .. 16c+15 of
-    // the stage's K range -- to fp16, scales them by their group's scale and
-    // writes them into the 128-byte-swizzled fp16 atoms of W tile j % kDenseWTiles
-    // (atom c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1) once the MMAs of chunk
-    // j - kDenseWTiles have released it.  Each lane sees the same rows in
-    // every stage; their scales are loaded one stage ahead.
+    // Thread (row r, half h): weight row r = 32 (warp % 4) + lane -- the TMEM
+    // lane its warp may write -- and half h of a stage's 128 codes (the two
+    // warps of a lane quarter take one half each).  Stage layout of the codes:
+    // [128 rows][128 B], 16-byte chunk c of row r at physical chunk
+    // c ^ (r & 7); the thread reads chunks 4h .. 4h + 3 of its row (the 32
+    // rows of a warp spread over the 8 physical positions: no bank conflict
+    // beyond the 4 wavefronts of 512 bytes), converts the 64 codes to fp16,
+    // multiplies them by their group's scale (a group of 64 or more codes
+    // covers the half) and stores the 32 columns of fp16 pairs into W tile
+    // j % kDenseWTiles once the MMAs of chunk j - kDenseWTiles have released it.
     const int cw = warp - kDenseConvWarp0;
-    constexpr int kConvIters = 128 / (4 * kDenseConvWarps);  // rows of the tile per lane and stage
-    const uint32_t p = (uint32_t)(lane & 7);
+    const int h = cw >> 2;
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t rx = (uint32_t)(r & 7);
     const int qshift = 31 - __clz(a.qgroup);
-    const int G = a.K >> qshift;  // scale groups per weight row
+    const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(4 * NTOK + 32 * h);
     DRing rp;
     int wj = 0;
     bool dead = false;
     dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int) {
-      const int sl = u / P.tiles, t = u - sl * P.tiles;
-      const __half* srow = a.Wscale + (size_t)((t / tok_tiles) * 128) * G;
-      auto load_scales = [&](int kc, uint32_t (&sc)[kConvIters]) {
-        const int k0 = (sl * P.C + kc) * KC;
-#pragma unroll
-        for (int it = 0; it < kConvIters; ++it) {
-          const int r = it * (4 * kDenseConvWarps) + cw * 4 + (lane >> 3);
-          const uint32_t c = p ^ (uint32_t)(r & 7);
-          const __half sv = srow[(size_t)r * G + ((k0 + 16 * (int)c) >> qshift)];
-          const __half2 s2 = __halves2half2(sv, sv);
-          sc[it] = *reinterpret_cast<const uint32_t*>(&s2);
-        }
-      };
-      uint32_t sc[kConvIters], scn[kConvIters];
-      load_scales(kc0, sc);
+      const int sl = u / P.tiles;
       for (int kc = kc0; kc < kc1; ++kc) {
-        if (kc + 1 < kc1) load_scales(kc + 1, scn);
         const int wslot = wj % kDenseWTiles;
         if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);
         if (!dead) dead = !mbar_wait(wempty_bar(wslot), (uint32_t)(((wj / kDenseWTiles) & 1) ^ 1), a.status);
-        const uint32_t w8 = smem_u32(sm + (size_t)rp.st * SB);
-        const uint32_t wt = wtile + (uint32_t)(wslot * WB);
+        dead = __any_sync(0xffffffffu, dead);  // the TMEM store below is warp-collective
+        if (!dead) {
+          tc_fence_after();
+          const uint32_t sbase = smem_u32(sm + (size_t)rp.st * SB);
+          const int k0 = (sl * P.C + kc) * KC + 64 * h;  // K index of the thread's first code
+          // its group, as an index into the stage's scale box (the aligned
+          // block of kDenseScaleGroups holding the stage's first group)
+          const uint32_t g = (uint32_t)((k0 >> qshift) & (kDenseScaleGroups - 1));
+          const uint32_t sv = lds_u16(sbase + SOFF + (uint32_t)r * (2u * kDenseScaleGroups) + 2u * g);
+          const uint32_t s2u = sv | (sv << 16);
+          const __half2 s2 = *reinterpret_cast<const __half2*>(&s2u);
+          uint32_t hv[32];
 #pragma unroll
-        for (int it = 0; it < kConvIters; ++it) {
-          const int r = it * (4 * kDenseConvWarps) + cw * 4 + (lane >> 3);
-          const uint32_t x = (uint32_t)(r & 7), c = p ^ x;
-          const uint4 v = lds_u128(w8 + (uint32_t)r * 128u + p * 16u);
-          uint32_t h[8];
-          i8x4_to_half2x2(v.x, h[0], h[1]);
-          i8x4_to_half2x2(v.y, h[2], h[3]);
-          i8x4_to_half2x2(v.z, h[4], h[5]);
-          i8x4_to_half2x2(v.w, h[6], h[7]);
-          const __half2 s2 = *reinterpret_cast<const __half2*>(&sc[it]);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const __half2 y = __hmul2(*reinterpret_cast<const __half2*>(&h[j]), s2);
-            h[j] = *reinterpret_cast<const uint32_t*>(&y);
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = lds_u128(sbase + (uint32_t)r * 128u + (((uint32_t)(4 * h + i) ^ rx) * 16u));
+            i8x4_to_half2x2(v.x, hv[8 * i + 0], hv[8 * i + 1]);
+            i8x4_to_half2x2(v.y, hv[8 * i + 2], hv[8 * i + 3]);
+            i8x4_to_half2x2(v.z, hv[8 * i + 4], hv[8 * i + 5]);
+            i8x4_to_half2x2(v.w, hv[8 * i + 6], hv[8 * i + 7]);
           }
-          const uint32_t row = wt + (c >> 2) * (128u * 128u) + (uint32_t)r * 128u;
-          const uint32_t j0 = (c & 3u) * 2u;
-          sts_u128(row + ((j0 ^ x) * 16u), make_uint4(h[0], h[1], h[2], h[3]));
-          sts_u128(row + (((j0 + 1u) ^ x) * 16u), make_uint4(h[4], h[5], h[6], h[7]));
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const __half2 y = __hmul2(*reinterpret_cast<const __half2*>(&hv[j]), s2);
+            hv[j] = *reinterpret_cast<const uint32_t*>(&y);
+          }
+          tmem_st32(tlane + (uint32_t)(wslot * kDenseWTileCols), hv);
+          tmem_wait_st();
         }
-        // the fp16 tile is read by the tensor cores (async proxy)
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // the W tile is read by the tensor cores once every converter warp arrived
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(wfull_bar(wslot));
         rp.advance(S);
         ++wj;
-#pragma unroll
-        for (int it = 0; it < kConvIters; ++it) sc[it] = scn[it];
       }
     });
     if (KSC > 1) {
@@ -680,6 +741,27 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         }
       }
     };
+    // A tile's accumulator, 8 columns from c8 (tensor memory at tb): int8
+    // sums the two MMA issuers' accumulators that the segment wrote (mask bit
+    // i: issuer i took one of its chunks; warp-uniform, the loads are
+    // warp-collective).
+    auto acc_ld8 = [&](uint32_t tb, int c8, int mask, float (&v)[8]) {
+      if (!kI8 || mask == 1) {
+        tmem_ld8(tb + (uint32_t)c8, v);
+      } else if (mask == 2) {
+        tmem_ld8(tb + (uint32_t)(2 * NTOK + c8), v);
+      } else {
+        float w[8];
+        tmem_ld8(tb + (uint32_t)c8, v);
+        tmem_ld8(tb + (uint32_t)(2 * NTOK + c8), w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] += w[i];
+      }
+    };
+    // The issuers whose accumulators a segment of n chunks starting at the
+    // CTA's chunk j0 wrote (issuer i takes the chunks j with j % 2 == i).
+    auto acc_mask = [&](int j0, int n) { return !kI8 ? 1 : (n >= 2 ? 3 : 1 << (j0 & 1)); };
+    int seg_mask = 1;  // acc_mask of the segment being finished
     // Finishes the 8-column groups c0, c0 + cstep, ... of one tile, the
     // accumulator taken from tensor memory (src 0), from nk staged partial
     // slots in shared memory (src 1), from nk partials in global memory
@@ -709,7 +791,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = 0.f;
         if (src == 0) {
-          tmem_ld8(tbase + (uint32_t)c8, v);
+          acc_ld8(tbase, c8, seg_mask, v);
         } else if (src == 1) {
           const uint32_t e0 = st + (uint32_t)(c8 * 128 + r) * 4u;
 #pragma unroll 1
@@ -760,7 +842,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
 #pragma unroll 1
       for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {
         float v[8];
-        tmem_ld8(tbase + (uint32_t)c8, v);
+        acc_ld8(tbase, c8, acc_mask(0, P.C), v);  // (one whole K slice of P.C chunks per CTA)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (c8 + i < c.mrows) sts_f32(st + (uint32_t)((c8 + i) * 128 + r) * 4u, v[i]);
@@ -774,8 +856,10 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     const int nstage_slots = (int)(((size_t)S * SB) / (slot_floats * 4));  // staging slots in the ring
     int seg = 0;
     bool dead = false;
+    int j0 = 0;  // the CTA's chunks before this segment
     dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int j_slot) {
-      (void)kc0; (void)kc1;
+      seg_mask = acc_mask(j0, kc1 - kc0);
+      j0 += kc1 - kc0;
       const int buf = seg & 1;
       const int sl = u / tiles, t = u - sl * tiles;   // K slice, output tile
       const int target = ws_tile_target(t, P, gridDim.x);  // contributions that complete the tile
@@ -800,7 +884,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
 #pragma unroll 1
         for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {
           float v[8];
-          tmem_ld8(tbase + (uint32_t)c8, v);
+          acc_ld8(tbase, c8, seg_mask, v);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             if (c8 + i < c.mrows) pb[(size_t)(c8 + i) * 128] = v[i];

@@ -105,8 +105,8 @@ struct ds_layer {
   // TMA tensor maps in device memory, kTensorMapBytes each: weights of QKV,
   // O-proj, FFN-up, FFN-down for the GEMV path, one map per k-blocks-per-step
   // choice (1, 2, 4: a map's box is one chunk); then (int8) their scales in
-  // the same order; then (fp16 / bf16) the tile maps of the four matrices for
-  // ring stages of 64 and of 128 along K.
+  // the same order; then the tile maps of the four matrices: fp16 / bf16 for
+  // ring stages of 64 and of 128 along K, int8 the scales' and the codes'.
   unsigned char* tmaps = nullptr;
   static int nblk_index(int nblk) { return nblk == 4 ? 2 : (nblk == 2 ? 1 : 0); }
   const void* tmap_w(int r, int nblk) const { return tmaps + (size_t)(3 * r + nblk_index(nblk)) * kTensorMapBytes; }
@@ -115,6 +115,10 @@ struct ds_layer {
   }
   const void* tmap_tile(int r, int kc) const {
     return tmaps + (size_t)(24 + 2 * r + (kc == 128 ? 1 : 0)) * kTensorMapBytes;
+  }
+  // int8 tiles (stages of 128 codes): the scales' map, in the unused slot of stages of 64
+  const void* tmap_tile_s(int r) const {
+    return cfg.weight_dtype == DS_I8 ? tmaps + (size_t)(24 + 2 * r) * kTensorMapBytes : nullptr;
   }
   // int8 scale group length of matrix r (0 QKV, 1 O-proj, 2 FFN-up, 3 FFN-down):
   // the FFN matrices take half the length under mlp_extra_grouping.
@@ -423,7 +427,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     if ((e = record_patch(rec, st, 0, p1, in_if(offsetof(LnPrepArgs, x_act)), {})) != cudaSuccess) return e;
     DenseArgs r1 = base;
     r1.tmap_w = L.tmap_tile(0, P.tq.kc);
-    r1.Wscale = static_cast<const __half*>(L.w.s_qkv);  // int8 only
+    r1.tmap_s = L.tmap_tile_s(0);
     r1.qgroup = L.qgroup(0);
     r1.N = 3 * H;
     r1.K = H;
@@ -448,7 +452,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     // R3: O-proj + bias + residual + LayerNorm2 statistics
     DenseArgs r3 = base;
     r3.tmap_w = L.tmap_tile(1, P.to.kc);
-    r3.Wscale = static_cast<const __half*>(L.w.s_o);  // int8 only
+    r3.tmap_s = L.tmap_tile_s(1);
     r3.qgroup = L.qgroup(1);
     r3.N = H;
     r3.K = H;
@@ -477,7 +481,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     if ((e = launch_ln_prep(ak, p2, st, pdl)) != cudaSuccess) return e;
     DenseArgs r4 = base;
     r4.tmap_w = L.tmap_tile(2, P.tu.kc);
-    r4.Wscale = static_cast<const __half*>(L.w.s_fc1);  // int8 only
+    r4.tmap_s = L.tmap_tile_s(2);
     r4.qgroup = L.qgroup(2);
     r4.N = F;
     r4.K = H;
@@ -491,7 +495,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
     // R4b: FFN-down + bias + residual (+ next LayerNorm statistics)
     DenseArgs r5 = base;
     r5.tmap_w = L.tmap_tile(3, P.td.kc);
-    r5.Wscale = static_cast<const __half*>(L.w.s_fc2);  // int8 only
+    r5.tmap_s = L.tmap_tile_s(3);
     r5.qgroup = L.qgroup(3);
     r5.N = H;
     r5.K = F;
@@ -701,13 +705,14 @@ ds_status make_tensor_maps(ds_layer* L) {
         return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a scale matrix");
     }
     if (L->tile_capable()) {
-      // fp16 / bf16: ring stages of 64 and 128 along K; int8 codes (as pairs
-      // of 16-bit elements): stages of 128 codes, in both slots
+      // fp16 / bf16: ring stages of 64 and 128 along K; int8: the codes (as
+      // pairs of 16-bit elements) in stages of 128, then their scales in boxes
+      // of 8 groups x 128 rows
       for (int j = 0; j < 2; ++j) {
-        const bool ok = i8 ? encode_tile_map(host.data() + (size_t)(24 + 2 * r + j) * kTensorMapBytes, W[r], rows[r],
-                                             cols[r] / 2, 128, 64)
-                           : encode_tile_map(host.data() + (size_t)(24 + 2 * r + j) * kTensorMapBytes, W[r], rows[r],
-                                             cols[r], 128, j ? 128 : 64);
+        unsigned char* m = host.data() + (size_t)(24 + 2 * r + j) * kTensorMapBytes;
+        const bool ok = i8 ? (j ? encode_tile_map(m, W[r], rows[r], cols[r] / 2, 128, 64)
+                                : encode_scale_map(m, Sc[r], rows[r], cols[r] / L->qgroup(r), 8, 128))
+                           : encode_tile_map(m, W[r], rows[r], cols[r], 128, j ? 128 : 64);
         if (!ok) return fail(DS_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight tile map");
       }
     }

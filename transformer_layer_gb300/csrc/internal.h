@@ -20,8 +20,8 @@ constexpr int kTensorMapBytes = 128;  // sizeof(CUtensorMap)
 // [128-byte segment][row][128 bytes] with the 128-byte swizzle (the layout of
 // ring_layout.h); false if the driver entry point or the encoding fails.
 bool encode_weight_map(void* map128, const void* base, int rows, size_t row_bytes, int chunk_row_bytes);
-// Tensor map of int8 group scales (rows x groups fp16) with 16 x box_groups boxes.
-bool encode_scale_map(void* map128, const void* base, int rows, int groups, int box_groups);
+// Tensor map of int8 group scales (rows x groups fp16) with box_rows x box_groups boxes.
+bool encode_scale_map(void* map128, const void* base, int rows, int groups, int box_groups, int box_rows = 16);
 enum class ActKind : int { F16 = 0, BF16 = 1 };
 
 // The four GEMV-based region kernels ([P1] §3.2 regions 1, 3, 3/4 and 4).
@@ -119,7 +119,7 @@ struct DensePlan {
 
 struct DenseArgs {
   const void* tmap_w = nullptr;    // device address of W's tile tensor map (box 128 rows x kc)
-  const __half* Wscale = nullptr;  // int8: fp16 scales [N][K / qgroup]
+  const void* tmap_s = nullptr;    // int8: device address of the fp16 scales' [N][K / qgroup] tensor map (box 8 groups x 128 rows)
   int qgroup = 64;                 // int8: scale group length along K (a power of two, >= 64)
   int N = 0, K = 0, M = 0, B = 1, T = 1;
   DensePlan plan;

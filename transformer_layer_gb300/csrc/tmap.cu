@@ -51,12 +51,12 @@ bool encode_weight_map(void* map128, const void* base, int rows, size_t row_byte
   return r == CUDA_SUCCESS;
 }
 
-bool encode_scale_map(void* map128, const void* base, int rows, int groups, int box_groups) {
+bool encode_scale_map(void* map128, const void* base, int rows, int groups, int box_groups, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr || (groups * 2) % 16 != 0 || (box_groups * 2) % 16 != 0) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)groups, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)groups * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)box_groups, 16u};
+  const cuuint32_t box[2] = {(cuuint32_t)box_groups, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1u, 1u};
   const CUresult r = enc(static_cast<CUtensorMap*>(map128), CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
