@@ -42,8 +42,8 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   // Token tiles of up to 128 rows; prompt chunks of 256 rows and more take
   // 256 with fp16 (MMA N = 256: half the weight re-reads per FLOP) and 192
   // with bf16 (its hi/lo operand: a 64 KB stage, three in the ring).  int8: up
-  // to 64 rows, so that the two accumulators and the two fp16 W tiles fit 256
-  // tensor-memory columns.
+  // to 64 rows, so that the four accumulators (two per MMA issuer) and the
+  // four fp16 W tiles fit the 512 tensor-memory columns.
   const int ntok_max = i8 ? 64 : (M >= 256 ? (split ? 192 : 256) : 128);
   if (ntok > ntok_max) ntok = ntok_max;
   p.ntok = ntok;
@@ -75,7 +75,7 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   ws_distribute(w, num_sms, /*one_unit_each=*/true, /*force_whole=*/many);
   w.interleave = many ? 1 : 0;
   const size_t SB = (dense_stage_bytes(ntok, p.kc, split, i8) + 1023) & ~(size_t)1023;
-  const size_t fixed = 1024 + 8 * (2 * kDenseMaxStages + 6 + 2 * kDenseWTiles) + 16;
+  const size_t fixed = 1024 + 8 * (3 * kDenseMaxStages + 6 + 2 * kDenseWTiles) + 16;
   if ((size_t)max_smem < fixed + 2 * SB) return false;
   size_t s = ((size_t)max_smem - fixed) / SB;
   if (s > (size_t)kDenseMaxStages) s = kDenseMaxStages;

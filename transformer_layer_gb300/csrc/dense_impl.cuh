@@ -64,15 +64,16 @@ namespace ds {
 
 constexpr int kDenseEpiWarps = 8;    // two per TMEM lane quarter, each taking half the columns
 constexpr int kDenseConvWarps = 8;   // int8 weights: warps that dequantise the codes to fp16
-constexpr int kDenseWTiles = 2;      // int8 weights: fp16 W tiles (in TMEM) the converters fill ahead of the MMAs
+constexpr int kDenseWTiles = 4;      // int8 weights: fp16 W tiles (in TMEM) the converters fill ahead of the MMAs
 constexpr int kDenseWTileCols = 64;  // TMEM columns of one fp16 W tile: 128 rows x 128 codes of K
 constexpr int kDenseThreads = (2 + kDenseEpiWarps) * 32;
-constexpr int kDenseThreadsI8 = (3 + kDenseEpiWarps + kDenseConvWarps) * 32;
+constexpr int kDenseMaxIssuers = 2;  // int8: MMA-issuing warps (warp 1 and kDenseMma2Warp ..)
+constexpr int kDenseThreadsI8 = (1 + kDenseMaxIssuers + kDenseEpiWarps + kDenseConvWarps) * 32;
 constexpr int kDenseTmaWarp = 0;
 constexpr int kDenseMmaWarp = 1;
 constexpr int kDenseEpiWarp0 = 2;    // warps 2 .. 9
 constexpr int kDenseConvWarp0 = 10;  // int8: warps 10 .. 10 + kDenseConvWarps - 1
-constexpr int kDenseMma2Warp = kDenseConvWarp0 + kDenseConvWarps;  // int8: the second MMA issuer
+constexpr int kDenseMma2Warp = kDenseConvWarp0 + kDenseConvWarps;  // int8: MMA issuers 1 .. kDenseMaxIssuers - 1
 constexpr int kDenseEpiThreads = kDenseEpiWarps * 32;
 constexpr int kDenseBarEpi = 1;      // named barrier of the eight epilogue warps
 constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
@@ -175,11 +176,17 @@ __host__ __device__ inline size_t dense_scale_bytes(bool i8) { return i8 ? (size
 __host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split, bool i8 = false) {
   return (i8 ? (size_t)128 * kc : dense_w_bytes(kc)) + (split ? 2 : 1) * dense_x_bytes(ntok, kc) + dense_scale_bytes(i8);
 }
-// Tensor memory columns: the two accumulators of NTOK columns (int8: two
-// per MMA issuer), then (int8) the fp16 W tiles; an allocation is a power of
-// two of at least 32.
+// int8: MMA issuers.  (Four, where the tensor memory holds their
+// accumulators, were slower: a 21st warp caps every thread at 80 registers,
+// since each SM sub-partition's register file serves its quarter of the
+// warps.)
+__host__ __device__ inline int dense_i8_issuers(int /*ntok*/) { return kDenseMaxIssuers; }
+// Tensor memory columns: two accumulators of NTOK columns (int8: two per MMA
+// issuer), then (int8) the fp16 W tiles; an allocation is a power of two of
+// at least 32.
 __host__ __device__ inline uint32_t dense_tmem_cols(int ntok, bool i8) {
-  const uint32_t need = (uint32_t)((i8 ? 4 : 2) * ntok) + (i8 ? (uint32_t)(kDenseWTiles * kDenseWTileCols) : 0u);
+  const uint32_t need = (uint32_t)((i8 ? 2 * dense_i8_issuers(ntok) : 2) * ntok) +
+                        (i8 ? (uint32_t)(kDenseWTiles * kDenseWTileCols) : 0u);
   uint32_t c = 32;
   while (c < need) c <<= 1;
   return c;
@@ -251,7 +258,8 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
   const uint32_t XOFF = kI8 ? (uint32_t)(128 * KC) : (uint32_t)WB;  // X within a stage
   const uint32_t SOFF = XOFF + (uint32_t)XB;                         // int8: the scale box within a stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)S * SB);
-  // full[S], empty[S], acc_full[2], acc_empty[2]
+  // full[S], empty[S], acc_full[2], acc_empty[2], fix, done, (int8)
+  // wfull[kDenseWTiles], wempty[kDenseWTiles], xfull[S]
   auto full_bar = [&](int i) { return smem_u32(bars + i); };
   auto empty_bar = [&](int i) { return smem_u32(bars + S + i); };
   auto accf_bar = [&](int i) { return smem_u32(bars + 2 * S + i); };
@@ -261,7 +269,13 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
   // int8: fp16 W tile i written (converter warps) / read by the MMAs (commit)
   auto wfull_bar = [&](int i) { return smem_u32(bars + 2 * S + 6 + i); };
   auto wempty_bar = [&](int i) { return smem_u32(bars + 2 * S + 6 + kDenseWTiles + i); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6 + 2 * kDenseWTiles);
+  // int8, a stage's first use (the S chunks requested before the dependency
+  // wait): its full barrier counts the codes and scales only, which do not
+  // depend on the previous kernel, so the converters start on them before
+  // the wait; its X (after the wait) completes xfull, which the MMAs wait
+  // for.  Later uses count codes, scales and X on full.
+  auto xfull_bar = [&](int i) { return smem_u32(bars + 2 * S + 6 + 2 * kDenseWTiles + i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 6 + 2 * kDenseWTiles);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const uint32_t tcols = dense_tmem_cols(NTOK, kI8);
 
@@ -278,16 +292,18 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       mbar_init(empty_bar(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(accf_bar(i), kI8 ? 2 : 1);  // int8: one commit per MMA issuer
+      mbar_init(accf_bar(i), kI8 ? dense_i8_issuers(NTOK) : 1);  // int8: one commit per MMA issuer
       mbar_init(acce_bar(i), kDenseEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(fix_bar, 1);
     mbar_init(done_bar, kDenseEpiWarps);
-    if (kI8)
+    if (kI8) {
       for (int i = 0; i < kDenseWTiles; ++i) {
         mbar_init(wfull_bar(i), kDenseConvWarps);
         mbar_init(wempty_bar(i), 1);
       }
+      for (int i = 0; i < S; ++i) mbar_init(xfull_bar(i), 1);
+    }
     mbar_init_fence();
   }
   if (warp == kDenseMmaWarp) tmem_alloc(smem_u32(tmem_slot), tcols);
@@ -317,7 +333,9 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       // weights read once: evict first; read again by other token tiles: keep
       const uint64_t pol_w = tok_tiles > 1 ? l2_evict_normal_policy() : l2_evict_first_policy();
       const uint64_t pol_x = l2_evict_normal_policy();
+      // bytes a stage's full barrier counts (int8, first use: X goes to xfull)
       const uint32_t tx = (uint32_t)((kI8 ? (size_t)128 * KC : WB) + (kSplit ? 2 : 1) * XB + dense_scale_bytes(kI8));
+      const uint32_t tx_first = kI8 ? tx - (uint32_t)XB : tx;
       const int qshift = kI8 ? 31 - __clz(a.qgroup) : 0;
       const uint32_t woff = 0u;                                    // where W's copy lands
       auto wk_of = [&](const Cursor& c) {                          // W's K coordinate (128-byte atoms)
@@ -347,7 +365,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       for (int j = 0; j < pre; ++j) {
         const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
         const int trow = q.t / tok_tiles;
-        mbar_arrive_expect_tx(full_bar(rp.st), tx);
+        mbar_arrive_expect_tx(full_bar(rp.st), tx_first);
         tma_load_3d(stage + woff, tmap_w, 0, trow * 128, wk_of(q), full_bar(rp.st), pol_w);
         load_scales(stage, q, trow, full_bar(rp.st));
         last_ph[rp.st] = rp.ph;
@@ -376,7 +394,8 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
           const uint32_t stage = smem_u32(sm + (size_t)r2.st * SB);
           const int jt = c.t % tok_tiles;
           const int kseg = (c.s * P.C + c.kc) * (KC / 64);
-          tma_load_3d(stage + XOFF, &xmap_hi, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
+          if constexpr (kI8) mbar_arrive_expect_tx(xfull_bar(r2.st), (uint32_t)XB);
+          tma_load_3d(stage + XOFF, &xmap_hi, 0, jt * NTOK, kseg, kI8 ? xfull_bar(r2.st) : full_bar(r2.st), pol_x);
           if constexpr (kSplit)
             tma_load_3d(stage + XOFF + (uint32_t)XB, &xmap_lo, 0, jt * NTOK, kseg, full_bar(r2.st), pol_x);
           ws_cursor_next(c, P, dp_b);
@@ -401,13 +420,19 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         issued |= 1u << rp.st;
         ws_cursor_next(q, P, dp_b);
         rp.advance(S);
-        l2_ahead(j + 1 + kL2Ahead);
+        // (int8: the ring of 16 KB code stages already holds more than the
+        // latency needs, and one more bulk instruction per chunk would cost
+        // this thread ~600 cycles that it is short of)
+        if constexpr (!kI8) l2_ahead(j + 1 + kL2Ahead);
       }
       // No copy may still be landing in this CTA's shared memory when it
       // exits: wait (bounded) for the last copy of every stage.  Immediate in
       // normal operation, where the MMA thread has consumed them all.
       for (int st = 0; st < S; ++st)
-        if ((issued >> st) & 1u) mbar_wait(full_bar(st), last_ph[st], a.status);
+        if ((issued >> st) & 1u) {
+          mbar_wait(full_bar(st), last_ph[st], a.status);
+          if (kI8) mbar_wait(xfull_bar(st), 0, a.status);  // (every issued stage had a first use)
+        }
       // L2 prefetch of the next GEMM's first weight chunks for this CTA index.
       if (a.next_tmap_w != nullptr && blockIdx.x < a.next_plan.ws.grid) {
         const GemvPlan& Pn = a.next_plan.ws;
@@ -429,20 +454,21 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       dense_cluster_sync();
       dense_cluster_sync();
     }
-  } else if (warp == kDenseMmaWarp || (kI8 && warp == kDenseMma2Warp)) {
+  } else if (warp == kDenseMmaWarp || (kI8 && warp >= kDenseMma2Warp)) {
     // ---------------------------------------------------------- MMA issuer(s)
-    // One thread issues a tcgen05.mma about every 50 cycles at best, whatever
+    // One thread issues a tcgen05.mma about every 50-120 cycles, whatever
     // NTOK: at int8's 16 KB of weights per chunk that is the chunk's cost, so
-    // int8 runs two issuers.  Issuer me takes the CTA's chunks j with
-    // j % 2 == me -- exactly those of W tile me, so it observes every phase of
-    // that tile's barriers in order (a waiter that skipped a phase would take
-    // an older completion for the one it waits for) -- into its own
-    // accumulator pair (columns 2 NTOK me ..); the epilogue adds the two.
+    // int8 runs nis issuers.  Issuer me takes the CTA's chunks j with
+    // j % nis == me -- exactly those of W tiles me, me + nis, .., so it
+    // observes every phase of those tiles' barriers in order (a waiter that
+    // skipped a phase would take an older completion for the one it waits
+    // for) -- into its own accumulator pair (columns 2 NTOK me ..); the
+    // epilogue sums them.
     pdl_launch_dependents();
-    const int me = warp == kDenseMmaWarp ? 0 : 1;
-    constexpr int kIssuers = kI8 ? 2 : 1;
-    static_assert(!kI8 || kDenseWTiles == kIssuers, "int8: issuer i owns W tile i");
-    if (lane == 0) {
+    const int me = warp == kDenseMmaWarp ? 0 : warp - kDenseMma2Warp + 1;
+    const int nis = kI8 ? dense_i8_issuers(NTOK) : 1;
+    static_assert(kDenseWTiles % 4 == 0 && kDenseWTiles % 2 == 0, "int8: issuer i owns the W tiles i, i + nis, ...");
+    if (lane == 0 && me < nis) {
       const uint32_t idesc = umma_idesc(kSplit, NTOK);
       DRing rp;
       int seg = 0;
@@ -457,10 +483,11 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         bool first = true;  // this issuer's first chunk of the tile: overwrite the accumulator
         for (int kc = kc0; kc < kc1; ++kc) {
           const int wslot = wj % kDenseWTiles;
-          if (wj % kIssuers == me) {
+          if (wj % nis == me) {
             // int8: the converters have waited for this stage and filled W tile wslot
             if (kI8 && !dead) dead = !mbar_wait(wfull_bar(wslot), (uint32_t)((wj / kDenseWTiles) & 1), a.status);
-            if (!dead) dead = !mbar_wait(full_bar(rp.st), rp.ph, a.status);  // (int8: already complete)
+            // the stage's X (int8: its codes were waited for by the converters)
+            if (!dead) dead = !mbar_wait((kI8 && wj < S) ? xfull_bar(rp.st) : full_bar(rp.st), rp.ph, a.status);
             if (!dead) {
               tc_fence_after();
               // Descriptors built once per chunk and advanced by their address
@@ -471,7 +498,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
               const uint64_t wd0 = umma_desc_sw128(sbase);
               const uint32_t acc0 = first ? 0u : 1u;
               // int8: W tile wslot in tensor memory, 8 columns per K step of 16
-              const uint32_t wcol = tmem + (uint32_t)(4 * NTOK + wslot * kDenseWTileCols);
+              const uint32_t wcol = tmem + (uint32_t)(2 * nis * NTOK + wslot * kDenseWTileCols);
 #pragma unroll 1
               for (int kb = 0; kb < KC / 64; ++kb) {
                 const uint64_t xk = xd0 + (uint64_t)(kb * NTOK * 8);  // NTOK rows of 128 B per 64 K
@@ -523,7 +550,8 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     const int r = 32 * (warp & 3) + lane;
     const uint32_t rx = (uint32_t)(r & 7);
     const int qshift = 31 - __clz(a.qgroup);
-    const uint32_t tlane = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(4 * NTOK + 32 * h);
+    const uint32_t tlane =
+        tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(2 * dense_i8_issuers(NTOK) * NTOK + 32 * h);
     DRing rp;
     int wj = 0;
     bool dead = false;
@@ -745,6 +773,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     // sums the two MMA issuers' accumulators that the segment wrote (mask bit
     // i: issuer i took one of its chunks; warp-uniform, the loads are
     // warp-collective).
+    static_assert(kDenseMaxIssuers == 2, "the accumulator sum below takes two issuers");
     auto acc_ld8 = [&](uint32_t tb, int c8, int mask, float (&v)[8]) {
       if (!kI8 || mask == 1) {
         tmem_ld8(tb + (uint32_t)c8, v);
