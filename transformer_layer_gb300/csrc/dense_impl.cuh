@@ -66,14 +66,19 @@ constexpr int kDenseEpiWarps = 8;    // two per TMEM lane quarter, each taking h
 constexpr int kDenseConvWarps = 8;   // int8 weights: warps that dequantise the codes to fp16
 constexpr int kDenseWTiles = 4;      // int8 weights: fp16 W tiles (in TMEM) the converters fill ahead of the MMAs
 constexpr int kDenseWTileCols = 64;  // TMEM columns of one fp16 W tile: 128 rows x 128 codes of K
-constexpr int kDenseThreads = (2 + kDenseEpiWarps) * 32;
-constexpr int kDenseMaxIssuers = 2;  // int8: MMA-issuing warps (warp 1 and kDenseMma2Warp ..)
-constexpr int kDenseThreadsI8 = (1 + kDenseMaxIssuers + kDenseEpiWarps + kDenseConvWarps) * 32;
+constexpr int kDenseMaxIssuers = 2;  // MMA-issuing warps: warp 1 and (two issuers) the last warp
 constexpr int kDenseTmaWarp = 0;
 constexpr int kDenseMmaWarp = 1;
 constexpr int kDenseEpiWarp0 = 2;    // warps 2 .. 9
 constexpr int kDenseConvWarp0 = 10;  // int8: warps 10 .. 10 + kDenseConvWarps - 1
-constexpr int kDenseMma2Warp = kDenseConvWarp0 + kDenseConvWarps;  // int8: MMA issuers 1 .. kDenseMaxIssuers - 1
+// the second MMA issuer: after the epilogue warps (int8: after the converters)
+__host__ __device__ constexpr int dense_mma2_warp(bool i8) {
+  return i8 ? kDenseConvWarp0 + kDenseConvWarps : kDenseEpiWarp0 + kDenseEpiWarps;
+}
+// threads of a tile CTA with nis MMA issuers
+__host__ __device__ constexpr int dense_threads(bool i8, int nis) {
+  return (1 + nis + kDenseEpiWarps + (i8 ? kDenseConvWarps : 0)) * 32;
+}
 constexpr int kDenseEpiThreads = kDenseEpiWarps * 32;
 constexpr int kDenseBarEpi = 1;      // named barrier of the eight epilogue warps
 constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
@@ -176,17 +181,24 @@ __host__ __device__ inline size_t dense_scale_bytes(bool i8) { return i8 ? (size
 __host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split, bool i8 = false) {
   return (i8 ? (size_t)128 * kc : dense_w_bytes(kc)) + (split ? 2 : 1) * dense_x_bytes(ntok, kc) + dense_scale_bytes(i8);
 }
-// int8: MMA issuers.  (Four, where the tensor memory holds their
-// accumulators, were slower: a 21st warp caps every thread at 80 registers,
-// since each SM sub-partition's register file serves its quarter of the
-// warps.)
-__host__ __device__ inline int dense_i8_issuers(int /*ntok*/) { return kDenseMaxIssuers; }
-// Tensor memory columns: two accumulators of NTOK columns (int8: two per MMA
-// issuer), then (int8) the fp16 W tiles; an allocation is a power of two of
-// at least 32.
-__host__ __device__ inline uint32_t dense_tmem_cols(int ntok, bool i8) {
-  const uint32_t need = (uint32_t)((i8 ? 2 * dense_i8_issuers(ntok) : 2) * ntok) +
-                        (i8 ? (uint32_t)(kDenseWTiles * kDenseWTileCols) : 0u);
+// MMA issuers of a tile GEMM.  One thread issues a tcgen05.mma about every
+// 50-120 cycles whatever NTOK, so at small NTOK a chunk's MMAs (8, bf16 16)
+// take longer to issue than its bytes take to stream; two issuers split the
+// chunks.  Each issuer must see every phase of the barriers it waits on:
+// fp16 / bf16 issuers wait on the ring's stages, so the ring needs an even
+// depth (issuer i then owns the stages st % 2 == i); int8 issuers wait on
+// their own W tiles.  Their accumulator pairs must fit the 512 tensor-memory
+// columns with the int8 W tiles.  (Four int8 issuers were slower: a 21st warp
+// caps every thread at 80 registers, since each SM sub-partition's register
+// file serves its quarter of the warps.)
+__host__ __device__ inline int dense_issuers(int ntok, int stages, bool i8) {
+  if (i8) return kDenseMaxIssuers;
+  return (ntok <= 128 && stages % 2 == 0) ? kDenseMaxIssuers : 1;
+}
+// Tensor memory columns: two accumulators of NTOK columns per MMA issuer,
+// then (int8) the fp16 W tiles; an allocation is a power of two of at least 32.
+__host__ __device__ inline uint32_t dense_tmem_cols(int ntok, int nis, bool i8) {
+  const uint32_t need = (uint32_t)(2 * nis * ntok) + (i8 ? (uint32_t)(kDenseWTiles * kDenseWTileCols) : 0u);
   uint32_t c = 32;
   while (c < need) c <<= 1;
   return c;
@@ -241,8 +253,9 @@ __device__ __forceinline__ void dense_cluster_sync() {
 // kI8: W is int8 codes with fp16 scales per group of qgroup along K (MoQ);
 // the converter warps dequantise each stage's codes to fp16 (q * s rounded
 // once to fp16, the MMA operand type) before its MMAs.
-template <Region R, typename ACT, bool kI8>
-__global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
+// NIS: MMA issuers (dense_issuers of the plan; the launch picks the instance).
+template <Region R, typename ACT, bool kI8, int NIS>
+__global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
     dense_region_kernel(const __grid_constant__ CUtensorMap xmap_hi, const __grid_constant__ CUtensorMap xmap_lo,
                         const DenseArgs a) {
   constexpr bool kSplit = std::is_same<ACT, __nv_bfloat16>::value;
@@ -277,7 +290,10 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
   auto xfull_bar = [&](int i) { return smem_u32(bars + 2 * S + 6 + 2 * kDenseWTiles + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 6 + 2 * kDenseWTiles);
   int* last_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  const uint32_t tcols = dense_tmem_cols(NTOK, kI8);
+  static_assert(NIS == 1 || NIS == kDenseMaxIssuers, "one or two MMA issuers");
+  static_assert(!kI8 || NIS == kDenseMaxIssuers, "int8 issuers own W tiles: two of them");
+  constexpr int nis = NIS;
+  const uint32_t tcols = dense_tmem_cols(NTOK, nis, kI8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 32) {  // the descriptors' first use is the TMA warp's first copy
@@ -292,7 +308,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       mbar_init(empty_bar(i), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(accf_bar(i), kI8 ? dense_i8_issuers(NTOK) : 1);  // int8: one commit per MMA issuer
+      mbar_init(accf_bar(i), nis);  // one commit per MMA issuer
       mbar_init(acce_bar(i), kDenseEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(fix_bar, 1);
@@ -454,21 +470,18 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
       dense_cluster_sync();
       dense_cluster_sync();
     }
-  } else if (warp == kDenseMmaWarp || (kI8 && warp >= kDenseMma2Warp)) {
+  } else if (warp == kDenseMmaWarp || (nis > 1 && warp == dense_mma2_warp(kI8))) {
     // ---------------------------------------------------------- MMA issuer(s)
-    // One thread issues a tcgen05.mma about every 50-120 cycles, whatever
-    // NTOK: at int8's 16 KB of weights per chunk that is the chunk's cost, so
-    // int8 runs nis issuers.  Issuer me takes the CTA's chunks j with
-    // j % nis == me -- exactly those of W tiles me, me + nis, .., so it
-    // observes every phase of those tiles' barriers in order (a waiter that
-    // skipped a phase would take an older completion for the one it waits
-    // for) -- into its own accumulator pair (columns 2 NTOK me ..); the
-    // epilogue sums them.
+    // Issuer me of nis (dense_issuers) takes the CTA's chunks j with
+    // j % nis == me -- with two issuers exactly those of its ring stages
+    // (fp16 / bf16) or W tiles (int8), so it observes every phase of the
+    // barriers it waits on in order (a waiter that skipped a phase would take
+    // an older completion for the one it waits for) -- into its own
+    // accumulator pair (columns 2 NTOK me ..); the epilogue sums them.
     pdl_launch_dependents();
-    const int me = warp == kDenseMmaWarp ? 0 : warp - kDenseMma2Warp + 1;
-    const int nis = kI8 ? dense_i8_issuers(NTOK) : 1;
+    const int me = warp == kDenseMmaWarp ? 0 : 1;
     static_assert(kDenseWTiles % 4 == 0 && kDenseWTiles % 2 == 0, "int8: issuer i owns the W tiles i, i + nis, ...");
-    if (lane == 0 && me < nis) {
+    if (lane == 0) {
       const uint32_t idesc = umma_idesc(kSplit, NTOK);
       DRing rp;
       int seg = 0;
@@ -551,7 +564,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     const uint32_t rx = (uint32_t)(r & 7);
     const int qshift = 31 - __clz(a.qgroup);
     const uint32_t tlane =
-        tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(2 * dense_i8_issuers(NTOK) * NTOK + 32 * h);
+        tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(2 * nis * NTOK + 32 * h);
     DRing rp;
     int wj = 0;
     bool dead = false;
@@ -769,13 +782,13 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
         }
       }
     };
-    // A tile's accumulator, 8 columns from c8 (tensor memory at tb): int8
-    // sums the two MMA issuers' accumulators that the segment wrote (mask bit
-    // i: issuer i took one of its chunks; warp-uniform, the loads are
+    // A tile's accumulator, 8 columns from c8 (tensor memory at tb): the sum
+    // of the MMA issuers' accumulators that the segment wrote (mask bit i:
+    // issuer i took one of its chunks; warp-uniform, the loads are
     // warp-collective).
     static_assert(kDenseMaxIssuers == 2, "the accumulator sum below takes two issuers");
     auto acc_ld8 = [&](uint32_t tb, int c8, int mask, float (&v)[8]) {
-      if (!kI8 || mask == 1) {
+      if (mask == 1) {
         tmem_ld8(tb + (uint32_t)c8, v);
       } else if (mask == 2) {
         tmem_ld8(tb + (uint32_t)(2 * NTOK + c8), v);
@@ -789,7 +802,7 @@ __global__ void __launch_bounds__(kI8 ? kDenseThreadsI8 : kDenseThreads, 1)
     };
     // The issuers whose accumulators a segment of n chunks starting at the
     // CTA's chunk j0 wrote (issuer i takes the chunks j with j % 2 == i).
-    auto acc_mask = [&](int j0, int n) { return !kI8 ? 1 : (n >= 2 ? 3 : 1 << (j0 & 1)); };
+    auto acc_mask = [&](int j0, int n) { return nis == 1 ? 1 : (n >= 2 ? 3 : 1 << (j0 & 1)); };
     int seg_mask = 1;  // acc_mask of the segment being finished
     // Finishes the 8-column groups c0, c0 + cstep, ... of one tile, the
     // accumulator taken from tensor memory (src 0), from nk staged partial
