@@ -134,7 +134,7 @@ def test_skinny_gemm_sweep_layer(act, B):
 def test_int8_layer_many_rows(act, B):
     """MoQ int8 weights at 9..150 batch rows: with fp16 activations the
     tensor-core tile kernels, whose converter warps dequantise each stage of
-    codes to fp16 in shared memory (several token tiles at 150 rows); with
+    codes to fp16 in tensor memory (several token tiles at 150 rows); with
     bf16 activations the streaming GEMV kernels (up to 39 rows)."""
     H, nh, F = 1024, 8, 4096
     L = DeviceLayer(H, nh, F, seed=1011, act_dtype=act, weight_dtype=torch.int8)
@@ -142,6 +142,25 @@ def test_int8_layer_many_rows(act, B):
         past = [(17 * b) % 90 for b in range(B)]
         res = run_layer(L, B, 1, past, max_len=100, seed=15)
         check_layer(L, res, B, 1, past, f"int8 {act} B={B}")
+    finally:
+        L.close()
+
+
+@pytest.mark.parametrize("act,H,nh,F", [(torch.float16, 5120, 40, 20480), (torch.bfloat16, 5120, 40, 20480),
+                                        (torch.float16, 2560, 20, 10240)])
+def test_uneven_k_slices(act, H, nh, F):
+    """Tile GEMMs whose K slices run as one cluster per weight tile, slices
+    of unequal length: at 16 batch rows the 40 weight tiles of hidden 5120
+    take 3 slices each (O-proj 40 chunks, FFN-down 160), so that O-proj and
+    FFN-down fill 120 SMs rather than 80.  (The 20 tiles of hidden 2560 would
+    take 7, but clusters of 7 do not all fit on the GPU at once: they keep
+    4.)  Every output element checked."""
+    L = DeviceLayer(H, nh, F, seed=1013, act_dtype=act, weight_dtype=act)
+    try:
+        B = 16
+        past = [(29 * b) % 200 for b in range(B)]
+        res = run_layer(L, B, 1, past, max_len=256, seed=17)
+        check_layer(L, res, B, 1, past, f"uneven {act} H={H}")
     finally:
         L.close()
 

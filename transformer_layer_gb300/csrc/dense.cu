@@ -25,6 +25,7 @@ cudaError_t launch_dense_i8(Region r, const DenseArgs& a, const CUtensorMap* xh,
 cudaError_t prepare_dense_f16(int max_smem);
 cudaError_t prepare_dense_bf16(int max_smem);
 cudaError_t prepare_dense_i8(int max_smem);
+int dense_cluster_capacity(int size, int max_smem);
 
 namespace {
 constexpr size_t kDenseMinSmem = 120 * 1024;  // two tile CTAs never share an SM (nor its TMEM)
@@ -54,48 +55,73 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
   w.chunk_k = p.kc;
   w.nt = 1;
   w.nblk = 1;
-  // With at least ~60 % as many tiles as SMs every CTA takes one whole tile
-  // (no split-K: a fix-up costs more than the idle SMs).  With fewer, each
-  // tile is cut into KS slices along K (a power of two, at most 8), one whole
-  // unit per CTA, as many as the SMs hold.  With more tiles than SMs, the
-  // even split over CTAs (whole units first, leftover chunks spread).
-  int KS = 1;
-  if (w.tiles * 5 < num_sms * 3)
-    while (KS < 8 && w.tiles * KS * 2 <= num_sms && (K / p.kc) % (KS * 2) == 0) KS *= 2;
-  w.KS = KS;
-  w.K_S = K / KS;
-  w.C = w.K_S / p.kc;
-  w.units = w.tiles * KS;
-  // More tiles than SMs with several token tiles (prompt chunks): whole
-  // tiles only (no split-K fix-ups of large tiles), handed out round-robin, so
-  // that the CTAs running at the same time take the token tiles of the same
-  // weight rows and read those weights from DRAM once between them.  (With one
-  // token tile, e.g. N = 20480 at decode, the few leftover tiles are split.)
-  const bool many = w.tiles > num_sms && p.tok_tiles > 1;
-  ws_distribute(w, num_sms, /*one_unit_each=*/true, /*force_whole=*/many);
-  w.interleave = many ? 1 : 0;
+  p.kchunks = K / p.kc;
   const size_t SB = (dense_stage_bytes(ntok, p.kc, split, i8) + 1023) & ~(size_t)1023;
   const size_t fixed = 1024 + 8 * (3 * kDenseMaxStages + 6 + 2 * kDenseWTiles) + 16;
   if ((size_t)max_smem < fixed + 2 * SB) return false;
-  size_t s = ((size_t)max_smem - fixed) / SB;
-  if (s > (size_t)kDenseMaxStages) s = kDenseMaxStages;
-  if (s > (size_t)w.C * 2 && w.C >= 2) s = (size_t)w.C * 2;  // no deeper than the work
-  if (s < 2) s = 2;
-  // fp16 / bf16 at up to 128 token rows run two MMA issuers, each owning the
-  // ring stages of one parity: an even depth (int8 issuers own W tiles)
-  if (!i8 && ntok <= 128 && s >= 3 && (s & 1)) s -= 1;
-  p.stages = (int)s;
-  size_t smem = fixed + s * SB;
-  if (smem < kDenseMinSmem) smem = kDenseMinSmem;
-  if (smem > (size_t)max_smem) return false;
-  p.smem = smem;
-  w.stages = p.stages;
-  w.smem = smem;
-  // K-sliced tiles with one slice per CTA: the slices of a tile run as one
-  // cluster and are summed on chip (no partial sums through global memory);
-  // each CTA's partial tile is staged in its idle ring.
-  p.cluster = (KS > 1 && w.grid == w.units && w.q == 1 && w.R == 0 &&
-               (size_t)p.stages * SB >= (size_t)ntok * 128 * 4) ? KS : 1;
+  // The plan for KS slices per tile along K (uneven: a cluster's slices share
+  // the K chunks as evenly as they go); false if it does not fit.
+  auto make = [&](int KS, bool uneven, DensePlan* out) -> bool {
+    DensePlan q = p;
+    GemvPlan& w = q.ws;
+    w.KS = KS;
+    w.C = uneven ? (q.kchunks + KS - 1) / KS : q.kchunks / KS;  // (uneven: the longest slice)
+    w.K_S = w.C * q.kc;
+    w.units = w.tiles * KS;
+    // More tiles than SMs with several token tiles (prompt chunks): whole
+    // tiles only (no split-K fix-ups of large tiles), handed out round-robin,
+    // so that the CTAs running at the same time take the token tiles of the
+    // same weight rows and read those weights from DRAM once between them.
+    // (With one token tile, e.g. N = 20480 at decode, the few leftover tiles
+    // are split.)
+    const bool many = w.tiles > num_sms && q.tok_tiles > 1;
+    ws_distribute(w, num_sms, /*one_unit_each=*/true, /*force_whole=*/many);
+    w.interleave = many ? 1 : 0;
+    size_t s = ((size_t)max_smem - fixed) / SB;
+    if (s > (size_t)kDenseMaxStages) s = kDenseMaxStages;
+    if (s > (size_t)w.C * 2 && w.C >= 2) s = (size_t)w.C * 2;  // no deeper than the work
+    if (s < 2) s = 2;
+    // fp16 / bf16 at up to 128 token rows run two MMA issuers, each owning
+    // the ring stages of one parity: an even depth (int8 issuers own W tiles)
+    if (!i8 && ntok <= 128 && s >= 3 && (s & 1)) s -= 1;
+    q.stages = (int)s;
+    size_t smem = fixed + s * SB;
+    if (smem < kDenseMinSmem) smem = kDenseMinSmem;
+    if (smem > (size_t)max_smem) return false;
+    q.smem = smem;
+    w.stages = q.stages;
+    w.smem = smem;
+    // K-sliced tiles with one slice per CTA: the slices of a tile run as one
+    // cluster and are summed on chip (no partial sums through global
+    // memory); each CTA's partial tile is staged in its idle ring.
+    q.cluster = (KS > 1 && w.grid == w.units && w.q == 1 && w.R == 0 &&
+                 (size_t)q.stages * SB >= (size_t)ntok * 128 * 4) ? KS : 1;
+    if (uneven && q.cluster != KS) return false;  // uneven slices only run as clusters
+    *out = q;
+    return true;
+  };
+  // With at least ~60 % as many tiles as SMs every CTA takes one whole tile
+  // (no split-K: a fix-up costs more than the idle SMs).  With fewer, each
+  // tile is cut into KS slices along K (a power of two, at most 8, dividing
+  // the chunks), one whole unit per CTA, as many as the SMs hold; when those
+  // run as clusters, as many slices as the SMs hold (at most 8, the portable
+  // cluster size) if all the clusters fit at once, of unequal length if need
+  // be -- 40 tiles (N = 5120) take 120 SMs rather than 80.  With more tiles
+  // than SMs, the even split over CTAs (whole units first, leftover chunks
+  // spread).
+  int KS = 1;
+  if (p.ws.tiles * 5 < num_sms * 3)
+    while (KS < 8 && p.ws.tiles * KS * 2 <= num_sms && p.kchunks % (KS * 2) == 0) KS *= 2;
+  if (!make(KS, false, &p)) return false;
+  if (p.cluster > 1) {
+    // (only a size whose clusters all fit on the device at once: a second
+    // wave would cost far more than the idle SMs)
+    int KSu = num_sms / p.ws.tiles;
+    if (KSu > 8) KSu = 8;
+    if (KSu > p.kchunks) KSu = p.kchunks;
+    DensePlan q;
+    if (KSu > KS && dense_cluster_capacity(KSu, max_smem) >= p.ws.tiles && make(KSu, p.kchunks % KSu != 0, &q)) p = q;
+  }
   *plan = p;
   return true;
 }

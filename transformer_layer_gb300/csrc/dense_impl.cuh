@@ -336,6 +336,19 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
   // takes K slice s of tile t (unit s * tiles + t).
   const int KSC = DP.cluster;
   const int vcta = KSC > 1 ? (int)(blockIdx.x % KSC) * P.tiles + (int)(blockIdx.x / KSC) : (int)blockIdx.x;
+  // K slice sl's first chunk along K: a cluster's slices share the K chunks
+  // as evenly as they go (their lengths differ by one at most; a cluster CTA
+  // only ever asks for its own slice, computed once here), otherwise every
+  // slice holds P.C chunks.
+  const int cl_c0 = KSC > 1 ? (vcta / P.tiles) * DP.kchunks / KSC : 0;
+  const int cl_len = KSC > 1 ? (vcta / P.tiles + 1) * DP.kchunks / KSC - cl_c0 : 0;
+  auto slice_c0 = [&](int sl) { return KSC > 1 ? cl_c0 : sl * P.C; };
+  // This CTA's segments, f(unit, first chunk, end chunk, slot) -- with a
+  // cluster, its one whole slice.
+  auto for_segments = [&](auto&& f) {
+    if (KSC > 1) f(vcta, 0, cl_len, 0);
+    else dense_for_segments(P, vcta, f);
+  };
 
   if (warp == kDenseTmaWarp) {
     // ---------------------------------------------------------- TMA producer
@@ -355,20 +368,20 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
       const int qshift = kI8 ? 31 - __clz(a.qgroup) : 0;
       const uint32_t woff = 0u;                                    // where W's copy lands
       auto wk_of = [&](const Cursor& c) {                          // W's K coordinate (128-byte atoms)
-        return (c.s * P.C + c.kc) * (kI8 ? KC / 128 : KC / 64);
+        return (slice_c0(c.s) + c.kc) * (kI8 ? KC / 128 : KC / 64);
       };
       // int8: the stage's scale box, the aligned 8 groups holding its first
       // (K is a multiple of 8 groups, so the box never leaves the matrix)
       auto load_scales = [&](uint32_t stage, const Cursor& c, int trow, uint32_t bar) {
         if constexpr (kI8) {
-          const int g0 = (((c.s * P.C + c.kc) * KC) >> qshift) & ~(kDenseScaleGroups - 1);
+          const int g0 = (((slice_c0(c.s) + c.kc) * KC) >> qshift) & ~(kDenseScaleGroups - 1);
           tma_load_2d(stage + SOFF, a.tmap_s, g0, trow * 128, bar, pol_x);
         }
       };
       long long ra, rb;
       ws_left_range(P, vcta, gridDim.x, &ra, &rb);
       const int dp_b = ws_dp_first(P, vcta);
-      const int nchunks = (int)(rb - ra) + P.q * P.C;
+      const int nchunks = KSC > 1 ? cl_len : (int)(rb - ra) + P.q * P.C;
       bool dead = false;
       uint32_t last_ph[kDenseMaxStagesDev];  // parity of the last copy issued into each stage
       uint32_t issued = 0;                   // stages that received a copy (bit mask)
@@ -409,7 +422,7 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
         for (int j = 0; j < pre; ++j) {
           const uint32_t stage = smem_u32(sm + (size_t)r2.st * SB);
           const int jt = c.t % tok_tiles;
-          const int kseg = (c.s * P.C + c.kc) * (KC / 64);
+          const int kseg = (slice_c0(c.s) + c.kc) * (KC / 64);
           if constexpr (kI8) mbar_arrive_expect_tx(xfull_bar(r2.st), (uint32_t)XB);
           tma_load_3d(stage + XOFF, &xmap_hi, 0, jt * NTOK, kseg, kI8 ? xfull_bar(r2.st) : full_bar(r2.st), pol_x);
           if constexpr (kSplit)
@@ -425,7 +438,7 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
         if (dead) break;
         const uint32_t stage = smem_u32(sm + (size_t)rp.st * SB);
         const int trow = q.t / tok_tiles, jt = q.t % tok_tiles;
-        const int kseg = (q.s * P.C + q.kc) * (KC / 64);
+        const int kseg = (slice_c0(q.s) + q.kc) * (KC / 64);
         mbar_arrive_expect_tx(full_bar(rp.st), tx);
         tma_load_3d(stage + woff, tmap_w, 0, trow * 128, wk_of(q), full_bar(rp.st), pol_w);
         load_scales(stage, q, trow, full_bar(rp.st));
@@ -487,7 +500,7 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
       int seg = 0;
       int wj = 0;  // int8: chunks so far (W tile wj % kDenseWTiles, its use wj / kDenseWTiles)
       bool dead = false;
-      dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int) {
+      for_segments([&](int u, int kc0, int kc1, int) {
         (void)u;
         const int buf = seg & 1;
         if (seg >= 2 && !dead) dead = !mbar_wait(acce_bar(buf), ((seg >> 1) - 1) & 1, a.status);
@@ -568,7 +581,7 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
     DRing rp;
     int wj = 0;
     bool dead = false;
-    dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int) {
+    for_segments([&](int u, int kc0, int kc1, int) {
       const int sl = u / P.tiles;
       for (int kc = kc0; kc < kc1; ++kc) {
         const int wslot = wj % kDenseWTiles;
@@ -578,7 +591,7 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
         if (!dead) {
           tc_fence_after();
           const uint32_t sbase = smem_u32(sm + (size_t)rp.st * SB);
-          const int k0 = (sl * P.C + kc) * KC + 64 * h;  // K index of the thread's first code
+          const int k0 = (slice_c0(sl) + kc) * KC + 64 * h;  // K index of the thread's first code
           // its group, as an index into the stage's scale box (the aligned
           // block of kDenseScaleGroups holding the stage's first group)
           const uint32_t g = (uint32_t)((k0 >> qshift) & (kDenseScaleGroups - 1));
@@ -884,7 +897,7 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
 #pragma unroll 1
       for (int c8 = cbeg; c8 < c.mrows; c8 += 16) {
         float v[8];
-        acc_ld8(tbase, c8, acc_mask(0, P.C), v);  // (one whole K slice of P.C chunks per CTA)
+        acc_ld8(tbase, c8, acc_mask(0, cl_len), v);  // (one whole K slice per CTA)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (c8 + i < c.mrows) sts_f32(st + (uint32_t)((c8 + i) * 128 + r) * 4u, v[i]);
@@ -899,7 +912,7 @@ __global__ void __launch_bounds__(dense_threads(kI8, NIS), 1)
     int seg = 0;
     bool dead = false;
     int j0 = 0;  // the CTA's chunks before this segment
-    dense_for_segments(P, vcta, [&](int u, int kc0, int kc1, int j_slot) {
+    for_segments([&](int u, int kc0, int kc1, int j_slot) {
       seg_mask = acc_mask(j0, kc1 - kc0);
       j0 += kc1 - kc0;
       const int buf = seg & 1;

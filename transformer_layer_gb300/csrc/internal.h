@@ -113,8 +113,11 @@ struct DensePlan {
   int stages = 0;
   size_t smem = 0;
   int cluster = 1;     // > 1: the K slices of each tile are one thread-block cluster of this many
-                       // CTAs (one slice each) whose partial sums meet in distributed shared memory
-  int i8 = 0;          // 1: int8 weight codes (fp16 activations), dequantised to fp16 in shared memory
+                       // CTAs (one slice each) whose partial sums meet in distributed shared memory;
+                       // slice s then holds K chunks [s kchunks / cluster, (s + 1) kchunks / cluster)
+                       // (ws.C: the longest), else each slice holds ws.C chunks
+  int kchunks = 0;     // K / kc
+  int i8 = 0;          // 1: int8 weight codes (fp16 activations), dequantised to fp16 in tensor memory
 };
 
 struct DenseArgs {
