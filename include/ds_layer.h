@@ -45,8 +45,8 @@
  *     tile kernels (tcgen05, accumulators in tensor memory), each LayerNorm
  *     then running as a small row kernel ahead of its GEMM (seven kernels
  *     per layer instead of five).  The int8 tile kernels dequantise each
- *     stage of codes to fp16 in shared memory (q * s rounded once to fp16,
- *     the MMA operand type); the int8 streaming kernels apply each group's
+ *     stage of codes to fp16 in tensor memory, the MMAs' A operand (q * s
+ *     rounded once to fp16, the MMA operand type); the int8 streaming kernels apply each group's
  *     scale to its fp32 partial sum.  With int8 weights under bf16
  *     activations the activations staged per GEMV slice (80 KB of shared
  *     memory) bound R further: up to 39 rows for groups of 64, 19 once a
