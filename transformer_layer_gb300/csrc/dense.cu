@@ -81,9 +81,9 @@ bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem,
     if (s > (size_t)kDenseMaxStages) s = kDenseMaxStages;
     if (s > (size_t)w.C * 2 && w.C >= 2) s = (size_t)w.C * 2;  // no deeper than the work
     if (s < 2) s = 2;
-    // fp16 / bf16 at up to 128 token rows run two MMA issuers, each owning
+    // fp16 / bf16 at up to 64 token rows run two MMA issuers, each owning
     // the ring stages of one parity: an even depth (int8 issuers own W tiles)
-    if (!i8 && ntok <= 128 && s >= 3 && (s & 1)) s -= 1;
+    if (!i8 && ntok <= 64 && s >= 3 && (s & 1)) s -= 1;
     q.stages = (int)s;
     size_t smem = fixed + s * SB;
     if (smem < kDenseMinSmem) smem = kDenseMinSmem;

@@ -187,13 +187,13 @@ __host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split
 // chunks.  Each issuer must see every phase of the barriers it waits on:
 // fp16 / bf16 issuers wait on the ring's stages, so the ring needs an even
 // depth (issuer i then owns the stages st % 2 == i); int8 issuers wait on
-// their own W tiles.  Their accumulator pairs must fit the 512 tensor-memory
-// columns with the int8 W tiles.  (Four int8 issuers were slower: a 21st warp
+// their own W tiles.  Up to 64 token rows (decode: at 128, a prompt chunk's
+// tile, the MMAs run long enough for one issuer).  (Four int8 issuers were slower: a 21st warp
 // caps every thread at 80 registers, since each SM sub-partition's register
 // file serves its quarter of the warps.)
 __host__ __device__ inline int dense_issuers(int ntok, int stages, bool i8) {
   if (i8) return kDenseMaxIssuers;
-  return (ntok <= 128 && stages % 2 == 0) ? kDenseMaxIssuers : 1;
+  return (ntok <= 64 && stages % 2 == 0) ? kDenseMaxIssuers : 1;
 }
 // Tensor memory columns: two accumulators of NTOK columns per MMA issuer,
 // then (int8) the fp16 W tiles; an allocation is a power of two of at least 32.
