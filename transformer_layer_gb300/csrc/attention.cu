@@ -32,6 +32,10 @@
 // atomics, no remote loads.
 #include <math.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -270,14 +274,41 @@ size_t attn_smem_bytes(int head_dim, int stage_keys) {
   return attn_stage_offset(head_dim) + (size_t)2 * stage_keys * head_dim * 2 + 16;
 }
 
+// CTAs of the decode attention (activation ak, head size D) with `smem`
+// bytes of dynamic shared memory that one SM holds at once; 0 if unknown.
+// Cached: the launch shape is worked out per call.
+static int attn_ctas_per_sm(ActKind ak, int D, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, size_t>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_tuple(dev, (int)ak, D, smem);
+  std::lock_guard<std::mutex> lk(mu);
+  const auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  const void* k = nullptr;
+  if (ak == ActKind::F16) k = D == 64 ? (const void*)attn_decode_kernel<__half, 64> : (const void*)attn_decode_kernel<__half, 128>;
+  else k = D == 64 ? (const void*)attn_decode_kernel<__nv_bfloat16, 64> : (const void*)attn_decode_kernel<__nv_bfloat16, 128>;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kAttnThreads, smem) != cudaSuccess) {
+    n = 0;
+    (void)cudaGetLastError();
+  }
+  cache[key] = n;
+  return n;
+}
+
 // Launch shape of the decode attention for a.B, a.heads, a.max_len and
 // a.head_dim: nsplit CTAs (one cluster) per (b, h), as many as keep the
 // grid within one CTA per SM (at most 8, at least ~32 keys each); such a
 // grid stages up to all of a split's keys and asks for more than half of an
 // SM's shared memory so that the CTAs spread over the SMs.  Larger grids
-// (many sequences) take one CTA per (b, h) and a 48 KB staging budget, and
-// several share an SM.
-void attn_configure(AttnArgs& a, int num_sms, int max_smem) {
+// (many sequences) take a 48 KB staging budget, several CTAs sharing an SM,
+// and, past one wave of resident CTAs, as many splits per (b, h) as pack
+// the CTAs into whole waves: with 640 (b, h) pairs and 296 CTAs resident at
+// once, one CTA per pair leaves the third wave three-quarters empty (72 % of
+// the slots used), three splits use 93 % of them.
+void attn_configure(AttnArgs& a, ActKind ak, int num_sms, int max_smem) {
   const int bh = a.B * a.heads, D = a.head_dim;
   int ns = num_sms / (bh > 0 ? bh : 1);
   if (ns > kAttnMaxSplit) ns = kAttnMaxSplit;
@@ -285,11 +316,32 @@ void attn_configure(AttnArgs& a, int num_sms, int max_smem) {
   if (ns > cap) ns = cap;
   if (ns < 1) ns = 1;
   const bool spread = (long long)bh * ns <= num_sms;
-  const int per_split = (a.max_len + ns - 1) / ns;
   const size_t fixed = attn_smem_bytes(D, 0);
   const size_t budget = spread ? ((size_t)max_smem > fixed + 1024 ? (size_t)max_smem - fixed - 1024 : 0) : 48 * 1024;
-  int sk = (int)(budget / ((size_t)4 * D));  // K and V rows of 16-bit values
-  if (sk > per_split) sk = per_split;
+  auto stage_keys = [&](int n) {
+    int sk = (int)(budget / ((size_t)4 * D));  // K and V rows of 16-bit values
+    const int per_split = (a.max_len + n - 1) / n;
+    return sk > per_split ? per_split : sk;
+  };
+  if (!spread) {
+    const int per_sm = attn_ctas_per_sm(ak, D, attn_smem_bytes(D, stage_keys(ns)));
+    const long long slots = (long long)per_sm * num_sms;
+    // only past one wave, and only into splits of 256 keys or more (shorter
+    // ones, or splitting a grid that fits at once, measured slower)
+    if (per_sm > 0 && bh > slots) {
+      auto packing = [&](int n) {
+        const long long c = (long long)bh * n, waves = (c + slots - 1) / slots;
+        return (double)c / (double)(waves * slots);
+      };
+      const int cap_w = a.max_len / 256;
+      const int nmax = cap_w < kAttnMaxSplit ? cap_w : kAttnMaxSplit;
+      int best = ns;
+      for (int n = ns + 1; n <= nmax && packing(best) < 0.9; ++n)
+        if (packing(n) > packing(best) + 0.05) best = n;
+      ns = best;
+    }
+  }
+  const int sk = stage_keys(ns);
   size_t smem = attn_smem_bytes(D, sk);
   if (spread) {
     const size_t half = (size_t)max_smem / 2 + 1024;

@@ -390,7 +390,7 @@ cudaError_t enqueue_layer(const ds_layer& L, const Plans& P, const Bufs& bf, con
   ra.max_len = max_len;
   ra.H = H;
   ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  attn_configure(ra, L.sms, L.max_smem);
+  attn_configure(ra, akind(L.cfg.act_dtype), L.sms, L.max_smem);
   ra.status = bf.status;
   // prompt chunks: tiled flash attention; decode and short chunks: split-KV
   auto launch_attn = [&](const AttnArgs& x) {

@@ -207,7 +207,7 @@ cudaError_t prepare_moe_kernels(int max_smem);
 
 // Sets a.nsplit, a.stage_keys and a.smem of the decode attention from a.B,
 // a.heads, a.max_len and a.head_dim.
-void attn_configure(AttnArgs& a, int num_sms, int max_smem);
+void attn_configure(AttnArgs& a, ActKind ak, int num_sms, int max_smem);
 // Shared memory of the decode attention kernel staging stage_keys K and V rows.
 size_t attn_smem_bytes(int head_dim, int stage_keys);
 cudaError_t launch_attention(ActKind ak, const AttnArgs& a, cudaStream_t st, bool pdl);

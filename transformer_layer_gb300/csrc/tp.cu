@@ -383,7 +383,7 @@ ds_status ds_tp_attention_partial(ds_tp_layer* L, const void* x_in, float* x1_pa
   ra.max_len = max_len;
   ra.H = Hl;
   ra.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  attn_configure(ra, L->sms, L->max_smem);
+  attn_configure(ra, L->cfg.layer.act_dtype == DS_BF16 ? ActKind::BF16 : ActKind::F16, L->sms, L->max_smem);
   ra.status = status;
   ra.out_hi = b_hi;
   ra.out_lo = b_lo;
