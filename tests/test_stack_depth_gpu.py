@@ -1,6 +1,7 @@
 """Full-depth stack parity: the 7B-shaped fp16 stack (32 layers, hidden 4096,
 512 cached positions) and the 13B-shaped MoQ int8 stack (40 layers, hidden
-5120, groups of 64, 1024 cached positions) at batch 1, decoded for 64 steps
+5120, groups of 64, 1024 cached positions) at batch 1 (streaming kernels) and
+batch 16 (tensor-core tiles; ragged cached lengths), decoded for 64 steps
 through the graph-replayed stack step, exactly as the benchmark runs them.
 
 At decode steps 1 and 64 the first, a middle and the last layer are checked
@@ -24,9 +25,11 @@ from transformer_layer_gb300 import ds, inputs
 pytestmark = pytest.mark.gpu
 
 CASES = {
-    # name: (layers, hidden, heads, ffn, past, weight dtype, checked layers)
-    "7b_f16": (32, 4096, 32, 16384, 512, torch.float16, (0, 15, 31)),
-    "13b_int8": (40, 5120, 40, 20480, 1024, torch.int8, (0, 19, 39)),
+    # name: (layers, hidden, heads, ffn, past, weight dtype, checked layers, batch)
+    "7b_f16": (32, 4096, 32, 16384, 512, torch.float16, (0, 15, 31), 1),
+    "13b_int8": (40, 5120, 40, 20480, 1024, torch.int8, (0, 19, 39), 1),
+    "7b_f16_b16": (32, 4096, 32, 16384, 512, torch.float16, (0, 31), 16),
+    "13b_int8_b16": (40, 5120, 40, 20480, 1024, torch.int8, (0, 39), 16),
 }
 STEPS = 64
 CHECK_STEPS = (1, 64)
@@ -36,13 +39,17 @@ def _run_prefix(layers, n, x, kc, vc, seq0, max_len, stream):
     """Output of layers [0, n) on copies of their caches (n >= 1)."""
     h = ds.ds_stack_create([l.handle for l in layers[:n]])
     try:
+        B = x.shape[0]
         k2 = [k.clone() for k in kc[:n]]
         v2 = [v.clone() for v in vc[:n]]
         seq = seq0.clone()
-        nb = ds.ds_stack_workspace_bytes(h, 1)
+        nb = ds.ds_stack_workspace_bytes(h, B)
         ws = new_workspace(nb)
         out = torch.empty_like(x)
-        ds.ds_stack_decode_step(h, x, out, 1, k2, v2, max_len, seq, ws, nb, stream)
+        # the clones and the workspace are made on torch's current stream:
+        # complete before the step reads them on `stream`
+        torch.cuda.synchronize()
+        ds.ds_stack_decode_step(h, x, out, B, k2, v2, max_len, seq, ws, nb, stream)
         stream.synchronize()
         return out
     finally:
@@ -51,23 +58,25 @@ def _run_prefix(layers, n, x, kc, vc, seq0, max_len, stream):
 
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_full_depth_stack_teacher_forced(case):
-    n_layers, H, nh, F, past, wdt, checked = CASES[case]
+    n_layers, H, nh, F, past, wdt, checked, B = CASES[case]
     d, max_len, seed = H // nh, past + STEPS, 1700
+    pasts = [past - 5 * b for b in range(B)]  # ragged at batch > 1
     layers = [DeviceLayer(H, nh, F, seed, layer=l, weight_dtype=wdt) for l in range(n_layers)]
     stack = ds.ds_stack_create([l.handle for l in layers])
     try:
         kc, vc = [], []
         for l in range(n_layers):
-            k, v = inputs.kv_cache(1, nh, max_len, d, seed, layer=l, device="cuda")
+            k, v = inputs.kv_cache(B, nh, max_len, d, seed, layer=l, device="cuda")
             kc.append(k)
             vc.append(v)
-        seq = torch.tensor([past], dtype=torch.int32, device="cuda")
-        nb = ds.ds_stack_workspace_bytes(stack, 1)
+        seq = torch.tensor(pasts, dtype=torch.int32, device="cuda")
+        nb = ds.ds_stack_workspace_bytes(stack, B)
         ws = new_workspace(nb)
         stream = torch.cuda.Stream()
-        out = torch.empty(1, H, dtype=torch.float16, device="cuda")
+        out = torch.empty(B, H, dtype=torch.float16, device="cuda")
         for step in range(1, STEPS + 1):
-            x = inputs.hidden(1, 1, H, seed, step=step, device="cuda").reshape(1, H)
+            x = inputs.hidden(B, 1, H, seed, step=step, device="cuda").reshape(B, H)
+            torch.cuda.synchronize()  # (made on torch's current stream; the step runs on `stream`)
             if step in CHECK_STEPS:
                 stream.synchronize()
                 seq0 = seq.clone()
@@ -78,21 +87,21 @@ def test_full_depth_stack_teacher_forced(case):
                        for l in checked}
                 yout = {l: _run_prefix(layers, l + 1, x, kc, vc, seq0, max_len, stream)
                         for l in checked if l + 1 < n_layers}
-            ds.ds_stack_decode_step(stack, x, out, 1, kc, vc, max_len, seq, ws, nb, stream)
+            ds.ds_stack_decode_step(stack, x, out, B, kc, vc, max_len, seq, ws, nb, stream)
             if step in CHECK_STEPS:
                 stream.synchronize()
                 yout[n_layers - 1] = out.clone()
                 for l in checked:
-                    r = oracle.layer_forward(to64(xin[l]).reshape(1, 1, H), layers[l].oracle_params(), K[l], V[l],
+                    r = oracle.layer_forward(to64(xin[l]).reshape(B, 1, H), layers[l].oracle_params(), K[l], V[l],
                                              cur, nh)
-                    check_close(yout[l].reshape(1, 1, H), r["y"], torch.float16, what=f"{case} step {step} layer {l} y")
-                    check_close(kc[l][0, :, cur[0], :], r["k_new"][0, 0], torch.float16,
-                                what=f"{case} step {step} layer {l} k")
-                    check_close(vc[l][0, :, cur[0], :], r["v_new"][0, 0], torch.float16,
-                                what=f"{case} step {step} layer {l} v")
+                    check_close(yout[l].reshape(B, 1, H), r["y"], torch.float16, what=f"{case} step {step} layer {l} y")
+                    kn = torch.stack([kc[l][b, :, cur[b], :] for b in range(B)])
+                    vn = torch.stack([vc[l][b, :, cur[b], :] for b in range(B)])
+                    check_close(kn, r["k_new"][:, 0], torch.float16, what=f"{case} step {step} layer {l} k")
+                    check_close(vn, r["v_new"][:, 0], torch.float16, what=f"{case} step {step} layer {l} v")
                     layers[l]._oracle = None  # float64 copies of a large layer: release them
         stream.synchronize()
-        assert seq.cpu().tolist() == [past + STEPS]
+        assert seq.cpu().tolist() == [p + STEPS for p in pasts]
         code, flags = ds.ds_workspace_status(ws)
         assert code == ds.DS_OK and flags == 0
         assert ds.ds_stack_graph_captures(stack) == 1
