@@ -19,7 +19,9 @@
 // thread-block cluster of `nsplit` (<= 8) CTAs, as many as keep the grid
 // within one CTA per SM; such a grid asks for more than half of an SM's
 // shared memory, so that no two CTAs share an SM (the block scheduler would
-// otherwise pack them onto a fraction of the SMs).  Before griddepcontrol.wait a
+// otherwise pack them onto a fraction of the SMs).  With more (b, h) pairs
+// than one wave of resident CTAs holds, the keys are split to pack the waves
+// (attn_configure).  Before griddepcontrol.wait a
 // CTA copies the cached K and V rows of its keys that the previous kernel
 // does not write (positions < past_len) into shared memory with two TMA bulk
 // copies, so that once the QKV kernel completes only q and the new rows come

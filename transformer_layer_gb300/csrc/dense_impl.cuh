@@ -29,7 +29,10 @@
 //  * Warp 1 allocates the tensor memory and one lane issues tcgen05.mma
 //    (kind::f16, M = 128, N = NTOK, K = 16 per instruction; bf16 issues the lo
 //    operand as a second MMA into the same accumulator) and tcgen05.commit to
-//    release ring stages and to publish finished tiles.
+//    release ring stages and to publish finished tiles.  At up to 64 token
+//    rows (and for int8) a second issuing warp, the last, takes every other
+//    chunk into its own accumulator pair: one thread issues an MMA only every
+//    ~50-120 cycles, whatever N (see dense_issuers).
 //  * Warps 2..9 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
 //    32 (w % 4) ..: one weight row per thread; the two warps of a lane
 //    quarter take alternate groups of 8 token columns) and run the region
@@ -46,7 +49,8 @@
 //  * Work split (work_split.h): a unit is one output tile x one K slice,
 //    chunks are KC-wide K ranges.  With at least ~60 % as many tiles as SMs
 //    each CTA takes one whole tile (no split-K); with fewer (N = 4096 at
-//    decode) each tile is cut into K slices, one per CTA, a cluster per tile;
+//    decode) each tile is cut into K slices, one per CTA, a cluster per tile
+//    (slices of unequal length where that fills more SMs: 3 for N = 5120);
 //    with more, CTAs own whole tiles (round-robin when several token tiles
 //    share the weights) and, at decode, an even share of the leftover tiles'
 //    chunks.
