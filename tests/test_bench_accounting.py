@@ -70,3 +70,26 @@ def test_attention_bytes_are_the_kv_rows():
     H, past = 4096, 512
     S = past + 1 + 32
     assert bench.region_bytes(H, 16384, 1, past)["attention"] == 2 * S * H * 2 + 2 * H * 4
+
+
+def test_a_run_with_a_device_flag_reports_nothing(monkeypatch):
+    """bench.py reads the workspace status word after its timed, end-to-end and
+    profiled steps: a flag (a bounded wait that gave up, a bounds or cache
+    check) stops it before any result line; a clean word lets it go on."""
+    from transformer_layer_gb300 import ds
+
+    seen = []
+
+    def fake_status(flags):
+        def status(ws, stream=None):
+            seen.append((ws, stream))
+            return (ds.DS_ERR_DEVICE if flags else ds.DS_OK), flags
+        return status
+
+    monkeypatch.setattr(ds, "ds_workspace_status", fake_status(0))
+    assert bench.check_device("ws", "stream", "the timed decode steps") is None
+    monkeypatch.setattr(ds, "ds_workspace_status", fake_status(ds.DS_DEVFLAG_WAIT_TIMEOUT))
+    with pytest.raises(SystemExit) as e:
+        bench.check_device("ws", "stream", "the timed decode steps")
+    assert f"0x{ds.DS_DEVFLAG_WAIT_TIMEOUT:x}" in str(e.value) and "no result" in str(e.value)
+    assert seen == [("ws", "stream"), ("ws", "stream")]
