@@ -11,6 +11,7 @@
 
 #include "common.cuh"
 #include "dense_impl.cuh"
+#include "dense_plan.h"
 #include "internal.h"
 #include "work_split.h"
 
@@ -27,103 +28,10 @@ cudaError_t prepare_dense_bf16(int max_smem);
 cudaError_t prepare_dense_i8(int max_smem);
 int dense_cluster_capacity(int size, int max_smem);
 
-namespace {
-constexpr size_t kDenseMinSmem = 120 * 1024;  // two tile CTAs never share an SM (nor its TMEM)
-constexpr int kDenseMaxStages = kDenseMaxStagesDev;
-}  // namespace
 
 bool dense_make_plan(ActKind ak, int N, int K, int M, int num_sms, int max_smem, DensePlan* plan, bool i8) {
-  if (N <= 0 || K <= 0 || M < 1 || (N % 128) != 0 || (K % 128) != 0 || num_sms < 1) return false;
-  const bool split = (ak == ActKind::BF16);
-  if (i8 && split) return false;  // int8 tiles take fp16 activations
-  DensePlan p;
-  p.i8 = i8 ? 1 : 0;
-  p.row_tiles = N / 128;
-  int ntok = (M + 15) / 16 * 16;
-  // Token tiles of up to 128 rows; prompt chunks of 256 rows and more take
-  // 256 with fp16 (MMA N = 256: half the weight re-reads per FLOP) and 192
-  // with bf16 (its hi/lo operand: a 64 KB stage, three in the ring).  int8: up
-  // to 64 rows, so that the four accumulators (two per MMA issuer) and the
-  // four fp16 W tiles fit the 512 tensor-memory columns.
-  const int ntok_max = i8 ? 64 : (M >= 256 ? (split ? 192 : 256) : 128);
-  if (ntok > ntok_max) ntok = ntok_max;
-  p.ntok = ntok;
-  p.tok_tiles = (M + ntok - 1) / ntok;
-  p.kc = i8 ? 128 : ((ntok > 64 || K % 128 != 0) ? 64 : 128);
-  GemvPlan& w = p.ws;
-  w.tiles = p.row_tiles * p.tok_tiles;
-  w.chunk_k = p.kc;
-  w.nt = 1;
-  w.nblk = 1;
-  p.kchunks = K / p.kc;
-  const size_t SB = (dense_stage_bytes(ntok, p.kc, split, i8) + 1023) & ~(size_t)1023;
-  const size_t fixed = 1024 + 8 * (3 * kDenseMaxStages + 6 + 2 * kDenseWTiles) + 16;
-  if ((size_t)max_smem < fixed + 2 * SB) return false;
-  // The plan for KS slices per tile along K (uneven: a cluster's slices share
-  // the K chunks as evenly as they go); false if it does not fit.
-  auto make = [&](int KS, bool uneven, DensePlan* out) -> bool {
-    DensePlan q = p;
-    GemvPlan& w = q.ws;
-    w.KS = KS;
-    w.C = uneven ? (q.kchunks + KS - 1) / KS : q.kchunks / KS;  // (uneven: the longest slice)
-    w.K_S = w.C * q.kc;
-    w.units = w.tiles * KS;
-    // More tiles than SMs with several token tiles (prompt chunks): whole
-    // tiles only (no split-K fix-ups of large tiles), handed out round-robin,
-    // so that the CTAs running at the same time take the token tiles of the
-    // same weight rows and read those weights from DRAM once between them.
-    // (With one token tile, e.g. N = 20480 at decode, the few leftover tiles
-    // are split.)
-    const bool many = w.tiles > num_sms && q.tok_tiles > 1;
-    ws_distribute(w, num_sms, /*one_unit_each=*/true, /*force_whole=*/many);
-    w.interleave = many ? 1 : 0;
-    size_t s = ((size_t)max_smem - fixed) / SB;
-    if (s > (size_t)kDenseMaxStages) s = kDenseMaxStages;
-    if (s > (size_t)w.C * 2 && w.C >= 2) s = (size_t)w.C * 2;  // no deeper than the work
-    if (s < 2) s = 2;
-    // fp16 / bf16 at up to 64 token rows run two MMA issuers, each owning
-    // the ring stages of one parity: an even depth (int8 issuers own W tiles)
-    if (!i8 && ntok <= 64 && s >= 3 && (s & 1)) s -= 1;
-    q.stages = (int)s;
-    size_t smem = fixed + s * SB;
-    if (smem < kDenseMinSmem) smem = kDenseMinSmem;
-    if (smem > (size_t)max_smem) return false;
-    q.smem = smem;
-    w.stages = q.stages;
-    w.smem = smem;
-    // K-sliced tiles with one slice per CTA: the slices of a tile run as one
-    // cluster and are summed on chip (no partial sums through global
-    // memory); each CTA's partial tile is staged in its idle ring.
-    q.cluster = (KS > 1 && w.grid == w.units && w.q == 1 && w.R == 0 &&
-                 (size_t)q.stages * SB >= (size_t)ntok * 128 * 4) ? KS : 1;
-    if (uneven && q.cluster != KS) return false;  // uneven slices only run as clusters
-    *out = q;
-    return true;
-  };
-  // With at least ~60 % as many tiles as SMs every CTA takes one whole tile
-  // (no split-K: a fix-up costs more than the idle SMs).  With fewer, each
-  // tile is cut into KS slices along K (a power of two, at most 8, dividing
-  // the chunks), one whole unit per CTA, as many as the SMs hold; when those
-  // run as clusters, as many slices as the SMs hold (at most 8, the portable
-  // cluster size) if all the clusters fit at once, of unequal length if need
-  // be -- 40 tiles (N = 5120) take 120 SMs rather than 80.  With more tiles
-  // than SMs, the even split over CTAs (whole units first, leftover chunks
-  // spread).
-  int KS = 1;
-  if (p.ws.tiles * 5 < num_sms * 3)
-    while (KS < 8 && p.ws.tiles * KS * 2 <= num_sms && p.kchunks % (KS * 2) == 0) KS *= 2;
-  if (!make(KS, false, &p)) return false;
-  if (p.cluster > 1) {
-    // (only a size whose clusters all fit on the device at once: a second
-    // wave would cost far more than the idle SMs)
-    int KSu = num_sms / p.ws.tiles;
-    if (KSu > 8) KSu = 8;
-    if (KSu > p.kchunks) KSu = p.kchunks;
-    DensePlan q;
-    if (KSu > KS && dense_cluster_capacity(KSu, max_smem) >= p.ws.tiles && make(KSu, p.kchunks % KSu != 0, &q)) p = q;
-  }
-  *plan = p;
-  return true;
+  return dense_make_plan_t(ak, N, K, M, num_sms, max_smem, plan, i8,
+                           [&](int size) { return dense_cluster_capacity(size, max_smem); });
 }
 
 cudaError_t launch_dense(Region r, ActKind ak, const DenseArgs& a, const void* xmap_hi, const void* xmap_lo,

@@ -63,14 +63,12 @@
 #include "common.cuh"
 #include "internal.h"
 #include "work_split.h"
+#include "dense_plan.h"
 
 namespace ds {
 
 constexpr int kDenseEpiWarps = 8;    // two per TMEM lane quarter, each taking half the columns
 constexpr int kDenseConvWarps = 8;   // int8 weights: warps that dequantise the codes to fp16
-constexpr int kDenseWTiles = 4;      // int8 weights: fp16 W tiles (in TMEM) the converters fill ahead of the MMAs
-constexpr int kDenseWTileCols = 64;  // TMEM columns of one fp16 W tile: 128 rows x 128 codes of K
-constexpr int kDenseMaxIssuers = 2;  // MMA-issuing warps: warp 1 and (two issuers) the last warp
 constexpr int kDenseTmaWarp = 0;
 constexpr int kDenseMmaWarp = 1;
 constexpr int kDenseEpiWarp0 = 2;    // warps 2 .. 9
@@ -85,7 +83,6 @@ __host__ __device__ constexpr int dense_threads(bool i8, int nis) {
 }
 constexpr int kDenseEpiThreads = kDenseEpiWarps * 32;
 constexpr int kDenseBarEpi = 1;      // named barrier of the eight epilogue warps
-constexpr int kDenseMaxStagesDev = 8;  // ring depth limit (the host plan uses at most this)
 constexpr int kL2Ahead = 8;            // weight chunks requested into L2 ahead of the ring
 
 // ---------------------------------------------------------------- tcgen05
@@ -170,44 +167,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 
 // ---------------------------------------------------------------- geometry
-// One ring stage: W [KC/64 atoms][128 rows][128 B], then X [KC/64][NTOK][128 B]
-// (and, for bf16, X lo the same), each part on a 1024-byte boundary.  With
-// int8 weights a stage holds the TMA copy of the codes, [128 rows][KC bytes]
-// (KC = 128, 128-byte swizzle), then X, then the scales of the stage's rows:
-// the aligned block of 8 groups along K that holds the stage's groups,
-// [128 rows][8 fp16] (a TMA box is at least 16 bytes wide).  The codes' fp16
-// dequantisation goes to one of kDenseWTiles W tiles in tensor memory, the
-// MMAs' A operand, so it costs neither ring depth nor shared-memory traffic.
-constexpr int kDenseScaleGroups = 8;  // int8: scale groups per row in a stage's scale box
-__host__ __device__ inline size_t dense_w_bytes(int kc) { return (size_t)128 * kc * 2; }
-__host__ __device__ inline size_t dense_x_bytes(int ntok, int kc) { return (size_t)ntok * kc * 2; }
-__host__ __device__ inline size_t dense_scale_bytes(bool i8) { return i8 ? (size_t)128 * kDenseScaleGroups * 2 : 0; }
-__host__ __device__ inline size_t dense_stage_bytes(int ntok, int kc, bool split, bool i8 = false) {
-  return (i8 ? (size_t)128 * kc : dense_w_bytes(kc)) + (split ? 2 : 1) * dense_x_bytes(ntok, kc) + dense_scale_bytes(i8);
-}
-// MMA issuers of a tile GEMM.  One thread issues a tcgen05.mma about every
-// 50-120 cycles whatever NTOK, so at small NTOK a chunk's MMAs (8, bf16 16)
-// take longer to issue than its bytes take to stream; two issuers split the
-// chunks.  Each issuer must see every phase of the barriers it waits on:
-// fp16 / bf16 issuers wait on the ring's stages, so the ring needs an even
-// depth (issuer i then owns the stages st % 2 == i); int8 issuers wait on
-// their own W tiles.  Up to 64 token rows (decode: at 128, a prompt chunk's
-// tile, the MMAs run long enough for one issuer).  (Four int8 issuers were slower: a 21st warp
-// caps every thread at 80 registers, since each SM sub-partition's register
-// file serves its quarter of the warps.)
-__host__ __device__ inline int dense_issuers(int ntok, int stages, bool i8) {
-  if (i8) return kDenseMaxIssuers;
-  return (ntok <= 64 && stages % 2 == 0) ? kDenseMaxIssuers : 1;
-}
-// Tensor memory columns: two accumulators of NTOK columns per MMA issuer,
-// then (int8) the fp16 W tiles; an allocation is a power of two of at least 32.
-__host__ __device__ inline uint32_t dense_tmem_cols(int ntok, int nis, bool i8) {
-  const uint32_t need = (uint32_t)(2 * nis * ntok) + (i8 ? (uint32_t)(kDenseWTiles * kDenseWTileCols) : 0u);
-  uint32_t c = 32;
-  while (c < need) c <<= 1;
-  return c;
-}
-
 // A role's position in the ring (same convention as the GEMV ring).
 struct DRing {
   int st = 0;
